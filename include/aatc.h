@@ -1,0 +1,162 @@
+/*
+ * aatc.h -- C ABI of the B300 (sm_103a) library for Attention-Aware Transform
+ * Coding (AATC) of LLM KV caches: calibrate a per-head transform and bit
+ * allocation, encode keys/values into a fixed-width bit-packed per-token
+ * record, and run decode attention directly over the packed cache.
+ *
+ * Sources of the operations (page title, section):
+ *   [ABS]  "KV Cache Compression Through the Lens of Transform Coding", Abstract:
+ *          allocate bits over a calibration set to minimize attention-aware
+ *          distortion, using transform coding and reverse water-filling.
+ *   [KLT]  "Attention-Aware Transform Coding Guide: KV Compression",
+ *          "Decorrelation via the Karhunen-Loeve Transform (KLT)".
+ *   [RWF]  same page, "Optimal Bit Allocation via Reverse Water-Filling".
+ *   [ATT]  same page, "Formal Attention Distortion Model":
+ *          o = softmax(q K^T / sqrt(d)) V over the quantized K, V.
+ *   [THM]  same page, "Theorem: Additive Error Decomposition" (key error is
+ *          weighted by the query, value error by the attention weights).
+ *   [IMPL] same page, "End-to-End Implementation" (calibrate, rotate,
+ *          quantize per channel).
+ *   [NOVA] "Spend Bits Where Queries Look: KV Cache Vector Quantization with
+ *          Attention-Preserving Transforms", Abstract: non-orthogonal key
+ *          transform (generalized Parseval), fixed per-token bit count,
+ *          bandwidth-bound decoding.
+ *
+ * Conventions for every entry point
+ *   - Tensors are caller-owned, contiguous, row-major DEVICE pointers unless
+ *     a parameter says "host".  Device pointers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work is enqueued on it; only aatc_calibrate and
+ *     aatc_check synchronize it.
+ *   - Every call returns an aatc_status; no exception crosses the ABI.
+ *     Argument errors are found on the host before any launch.  Conditions
+ *     only the device can see (non-finite inputs, an eigensolver that did not
+ *     converge) set a status word inside the handle, reported by the next
+ *     aatc_calibrate / aatc_check.  aatc_last_error() gives a message for
+ *     the calling thread's last failure.
+ *   - head_dim is 128.  Query head h uses KV head h / G, G = n_q_heads / n_kv_heads.
+ *   - Nothing traps, and no kernel waits on another block.
+ */
+#ifndef AATC_H
+#define AATC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    AATC_OK = 0,
+    AATC_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size or shape */
+    AATC_ERR_UNSUPPORTED = 2,    /* head_dim != 128, budget not a multiple of 32 bits, ... */
+    AATC_ERR_CUDA = 3,           /* a CUDA runtime call failed */
+    AATC_ERR_NO_CONVERGENCE = 4, /* Jacobi did not converge within jacobi_max_sweeps */
+    AATC_ERR_NONFINITE = 5,      /* NaN/Inf in calibration or cache input */
+    AATC_ERR_CAPACITY = 6        /* start_pos + L_new > L_cap, or L > L_cap */
+} aatc_status;
+
+typedef enum { AATC_F32 = 0, AATC_BF16 = 1 } aatc_dtype;
+
+/* Opaque calibration handle, owned by the library (aatc_free). */
+typedef struct aatc_calib aatc_calib;
+
+typedef struct {
+    int head_dim;             /* must be 128 */
+    int n_kv_heads;           /* H_kv >= 1 */
+    int n_q_heads;            /* H_q, a multiple of H_kv (GQA group G = H_q / H_kv <= 16) */
+    int n_calib_tokens;       /* N >= 2 calibration tokens per head */
+    double bits_per_element;  /* average bits R; B = 128*R must be an integer multiple
+                                 of 32 and at most 8*128 (e.g. 2.0, 2.75, 4.0) */
+    aatc_dtype dtype;         /* element type of every K/V/Q input of this handle */
+    int jacobi_max_sweeps;    /* <= 0 selects 50 */
+} aatc_calib_desc;
+
+/* Calibration ([ABS], [KLT], [RWF], [THM], [NOVA]).
+ * k_cal, v_cal: device [H_kv][N][128]; q_cal: device [H_q][N][128], all of
+ * desc->dtype.  Per KV head it computes the key mean and centered covariance
+ * Sk, the value mean and covariance Sv, and the query second moment Sq pooled
+ * over the G query heads of the group; then the whitened key transform
+ * Tk = Uk^T Sq^{1/2} (Uk the eigenvectors of Sq^{1/2} Sk Sq^{1/2}) and the value
+ * KLT Tv = Uv^T, integer bit widths b_j in 0..8 summing to B for each tensor
+ * (the B largest gains lam_j 4^-t, ties to the smaller j then t), and steps
+ * Delta_j = s_{b_j} sqrt(lam_j) with s_b the MSE-optimal uniform step for a
+ * unit Gaussian.  On success *out receives a new handle (free with aatc_free).
+ * Synchronizes `stream` once.  Returns NO_CONVERGENCE / NONFINITE from the
+ * device status; the handle is not created then. */
+aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const void *v_cal,
+                           const void *q_cal, aatc_calib **out, void *stream);
+
+/* Encode ([KLT], [IMPL], [NOVA] fixed per-token bit count).
+ * k, v: device [B][H_kv][L_new][128] of the handle's dtype, the keys/values of
+ * token positions start_pos .. start_pos+L_new-1.  For each row x:
+ * c = T (x - mu); u_j = clamp(rint(c_j/Delta_j + (2^b_j - 1)/2), 0, 2^b_j - 1)
+ * (round half to even, decided on an fp32 value); the codes are packed into
+ * a record of W = B/32 little-endian u32 words: the code of channel j is split
+ * by the binary digits of b_j into fields of width 8/4/2/1 (narrower fields
+ * hold the lower bits); the record holds all 8-bit fields, then 4-bit, 2-bit,
+ * 1-bit fields, channels ascending, LSB first.
+ * k_packed, v_packed: device [B][H_kv][L_cap][W] u32; rows start_pos ..
+ * start_pos+L_new-1 are written, others untouched.  L_new = 0 is a no-op.
+ * Errors: CAPACITY if start_pos + L_new > L_cap.  Non-finite inputs set the
+ * handle's NONFINITE status (codes of such rows are unspecified). */
+aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, int B, int L_new,
+                        int start_pos, int L_cap, uint32_t *k_packed, uint32_t *v_packed,
+                        void *stream);
+
+/* Decode attention over the packed cache ([ATT], [NOVA] bandwidth-bound decode).
+ * q: device [B][H_q][128] of the handle's dtype.  k_packed, v_packed: device
+ * [B][H_kv][L_cap][W] as written by aatc_encode.  seq_lens: device int32 [B]
+ * (tokens 0..seq_lens[b]-1 of row b are attended; each in 0..L) or NULL
+ * (every row attends L tokens).  out: device fp32 [B][H_q][128],
+ *   out[b][h] = sum_i softmax_i(q . k_hat_i / sqrt(128)) v_hat_i,
+ * k_hat/v_hat the decoded keys/values, no causal mask; a row with no tokens
+ * gets zeros.  Computed without reconstructing K or V: scores use
+ * q' = (Tk^{-T} q) o Delta_K / sqrt(128) against the codes, values are
+ * accumulated in the transform domain and the inverse transform Uv is
+ * applied once per head.  workspace: device scratch of at least
+ * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned, contents
+ * need not be initialized.  Errors: CAPACITY if L > L_cap; INVALID_ARG if the
+ * workspace is too small. */
+aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
+                                  const uint32_t *k_packed, const uint32_t *v_packed, int L_cap,
+                                  const int32_t *seq_lens, int L, int B, float *out,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/* Bytes of device workspace aatc_decode_attention needs for B rows of up to
+ * L tokens (0 on invalid arguments). */
+size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L);
+
+/* W = u32 words per token record of one head and tensor (B/32), or -1. */
+int aatc_record_words(const aatc_calib *calib);
+
+/* Serialize a handle into a caller-owned HOST buffer: a versioned
+ * little-endian blob (see aatc_import_calib).  If host_buf is NULL only the
+ * size is stored in *bytes; otherwise *bytes must hold the buffer size on
+ * entry and receives the bytes written.  Synchronizes the device. */
+aatc_status aatc_export_calib(const aatc_calib *calib, void *host_buf, size_t *bytes);
+
+/* Build a handle from a HOST blob.  Layout: int32 header {magic 0x43544141
+ * ("AATC"), version 1, head_dim, n_kv_heads, n_q_heads, B bits, dtype, 0},
+ * then for each array below all KV heads in order (H = n_kv_heads, d = 128):
+ * f64 mu_k[H][d], mu_v[H][d], T_k[H][d][d], T_k_inv[H][d][d], A_k[H][d][d],
+ * T_v[H][d][d], U_v[H][d][d], lam_k[H][d], lam_v[H][d], lam_q[H][d];
+ * int32 bits_k[H][d], bits_v[H][d]; f32 step_k[H][d], step_v[H][d].
+ * Bits must sum to B per head and tensor, each in 0..8.  Derived device
+ * tables (biases, record layout, decode tables) are rebuilt on the device. */
+aatc_status aatc_import_calib(const void *host_buf, size_t bytes, aatc_calib **out);
+
+/* Synchronize the device and report (then clear) the handle's device status. */
+aatc_status aatc_check(aatc_calib *calib);
+
+/* Release a handle and its device memory.  NULL-safe. */
+void aatc_free(aatc_calib *calib);
+
+/* Message describing the calling thread's most recent failure ("" if none). */
+const char *aatc_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AATC_H */

@@ -67,6 +67,7 @@ def lib():
             "orc_layout": (None, [P, I, P]),
             "orc_pack": (None, [P, P, I, I, P]),
             "orc_unpack": (None, [P, P, I, P]),
+            "orc_unpack_rows": (None, [P, Lg, I, P, I, P]),
             "orc_encode": (None, [P, Lg, I, P, P, P, P, I, P, P, P]),
             "orc_attention": (None, [P, P, P, Lg, I, P]),
             "orc_reconstruct": (None, [P, Lg, I, I, P, P, P, P, P]),
@@ -212,6 +213,17 @@ def unpack(rec, bits) -> np.ndarray:
     bits = _i32(bits)
     u = np.empty(bits.shape[0], dtype=np.int32)
     lib().orc_unpack(_p(rec), _p(bits), bits.shape[0], _p(u))
+    return u
+
+
+def unpack_rows(rec, bits) -> np.ndarray:
+    """unpack for records rec [..][W] -> codes int32 [..][d]."""
+    rec = np.ascontiguousarray(np.asarray(rec, dtype=np.uint32))
+    bits = _i32(bits)
+    W = rec.shape[-1]
+    n = rec.size // W
+    u = np.empty(rec.shape[:-1] + (bits.shape[0],), dtype=np.int32)
+    lib().orc_unpack_rows(_p(rec), n, W, _p(bits), bits.shape[0], _p(u))
     return u
 
 

@@ -586,3 +586,10 @@ void orc_decode_head(const double *q, int G, const uint32_t *krec, const uint32_
     for (int g = 0; g < G; ++g) orc_attention(q + g * d, Kh, Vh, L, d, out + g * d);
     free(Kh); free(Vh);
 }
+
+/* orc_unpack for n records rec [n][W] -> u [n][d] (test convenience). */
+void orc_unpack_rows(const uint32_t *rec, long n, int W, const int *bits, int d, int *u)
+{
+#pragma omp parallel for schedule(static)
+    for (long i = 0; i < n; ++i) orc_unpack(rec + i * W, bits, d, u + i * d);
+}

@@ -1,0 +1,237 @@
+"""Thin ctypes binding of libaatc.so (C ABI in include/aatc.h).
+
+Argument marshalling only: every computation runs in the CUDA library.  The
+functions take torch CUDA tensors (for device memory and the current stream)
+and pass raw pointers and sizes across the ABI.  If the library is missing
+``lib()`` raises; there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import struct
+from typing import Optional
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libaatc.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_CONVERGENCE, ERR_NONFINITE, ERR_CAPACITY = range(7)
+STATUS_NAMES = ["OK", "INVALID_ARG", "UNSUPPORTED", "CUDA", "NO_CONVERGENCE", "NONFINITE", "CAPACITY"]
+F32, BF16 = 0, 1
+D = 128
+BLOB_MAGIC, BLOB_VERSION = 0x43544141, 1
+
+EXPORTED = ["aatc_calibrate", "aatc_encode", "aatc_decode_attention", "aatc_decode_workspace_size",
+            "aatc_record_words", "aatc_export_calib", "aatc_import_calib", "aatc_check", "aatc_free",
+            "aatc_last_error"]
+
+
+class AatcError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        self.status = status
+        super().__init__("%s: %s" % (STATUS_NAMES[status] if 0 <= status < 7 else status, msg))
+
+
+class CalibDesc(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("n_calib_tokens", ctypes.c_int), ("bits_per_element", ctypes.c_double),
+                ("dtype", ctypes.c_int), ("jacobi_max_sweeps", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libaatc.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libaatc.so is not built; run `python -m quantized_attention_kv_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        sig = {
+            "aatc_calibrate": (I, [ctypes.POINTER(CalibDesc), P, P, P, ctypes.POINTER(P), P]),
+            "aatc_encode": (I, [P, P, P, I, I, I, I, P, P, P]),
+            "aatc_decode_attention": (I, [P, P, P, P, I, P, I, I, P, P, S, P]),
+            "aatc_decode_workspace_size": (S, [P, I, I]),
+            "aatc_record_words": (I, [P]),
+            "aatc_export_calib": (I, [P, P, ctypes.POINTER(S)]),
+            "aatc_import_calib": (I, [P, S, ctypes.POINTER(P)]),
+            "aatc_check": (I, [P]),
+            "aatc_free": (None, [P]),
+            "aatc_last_error": (ctypes.c_char_p, []),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().aatc_last_error().decode()
+
+
+def _check(st: int):
+    if st != OK:
+        raise AatcError(st, last_error())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors passed to the library must be CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to the library must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError("inputs must be float32 or bfloat16")
+
+
+class Calib:
+    """Owning wrapper of an aatc_calib handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, dtype: torch.dtype, n_kv_heads: int, n_q_heads: int):
+        self.handle = handle
+        self.dtype = dtype
+        self.n_kv_heads = n_kv_heads
+        self.n_q_heads = n_q_heads
+
+    @property
+    def W(self) -> int:
+        return lib().aatc_record_words(self.handle)
+
+    def free(self):
+        if self.handle:
+            lib().aatc_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def check(self):
+        _check(lib().aatc_check(self.handle))
+
+    def export(self) -> dict:
+        """The calibration as numpy arrays (via aatc_export_calib)."""
+        n = ctypes.c_size_t(0)
+        _check(lib().aatc_export_calib(self.handle, None, ctypes.byref(n)))
+        buf = ctypes.create_string_buffer(n.value)
+        _check(lib().aatc_export_calib(self.handle, buf, ctypes.byref(n)))
+        return parse_blob(buf.raw[:n.value])
+
+
+def calibrate(k_cal: torch.Tensor, v_cal: torch.Tensor, q_cal: torch.Tensor, bits_per_element: float,
+              jacobi_max_sweeps: int = 0, stream=None) -> Calib:
+    """aatc_calibrate: k_cal, v_cal [H_kv][N][128], q_cal [H_q][N][128] on the GPU."""
+    Hkv, N, d = k_cal.shape
+    desc = CalibDesc(d, Hkv, q_cal.shape[0], N, float(bits_per_element), _dtype_code(k_cal.dtype),
+                     int(jacobi_max_sweeps))
+    h = ctypes.c_void_p()
+    _check(lib().aatc_calibrate(ctypes.byref(desc), _ptr(k_cal), _ptr(v_cal), _ptr(q_cal),
+                                ctypes.byref(h), _stream(stream)))
+    return Calib(h, k_cal.dtype, Hkv, q_cal.shape[0])
+
+
+def make_blob(cal: dict, n_q_heads: int, dtype: torch.dtype) -> bytes:
+    """Serialize calibration arrays into the aatc_import_calib blob format."""
+    H = np.asarray(cal["mu_k"]).shape[0]
+    Bbits = int(np.asarray(cal["bits_k"])[0].sum())
+    hdr = struct.pack("<8i", BLOB_MAGIC, BLOB_VERSION, D, H, n_q_heads, Bbits, _dtype_code(dtype), 0)
+    parts = [hdr]
+    for key in ("mu_k", "mu_v", "T_k", "T_k_inv", "A_k", "T_v", "U_v", "lam_k", "lam_v", "lam_q"):
+        parts.append(np.ascontiguousarray(cal[key], dtype="<f8").tobytes())
+    for key in ("bits_k", "bits_v"):
+        parts.append(np.ascontiguousarray(cal[key], dtype="<i4").tobytes())
+    for key in ("step_k", "step_v"):
+        parts.append(np.ascontiguousarray(cal[key], dtype="<f4").tobytes())
+    return b"".join(parts)
+
+
+def parse_blob(blob: bytes) -> dict:
+    hdr = struct.unpack_from("<8i", blob, 0)
+    if hdr[0] != BLOB_MAGIC or hdr[1] != BLOB_VERSION:
+        raise ValueError("not a calibration blob")
+    H = hdr[3]
+    off = 32
+    out = {"n_q_heads": hdr[4], "B_bits": hdr[5], "dtype": hdr[6], "W": hdr[5] // 32,
+           "G": hdr[4] // H}
+
+    def take(key, dt, shape):
+        nonlocal off
+        n = int(np.prod(shape))
+        out[key] = np.frombuffer(blob, dtype=dt, count=n, offset=off).reshape(shape).copy()
+        off += n * np.dtype(dt).itemsize
+
+    for key in ("mu_k", "mu_v"):
+        take(key, "<f8", (H, D))
+    for key in ("T_k", "T_k_inv", "A_k", "T_v", "U_v"):
+        take(key, "<f8", (H, D, D))
+    for key in ("lam_k", "lam_v", "lam_q"):
+        take(key, "<f8", (H, D))
+    for key in ("bits_k", "bits_v"):
+        take(key, "<i4", (H, D))
+    for key in ("step_k", "step_v"):
+        take(key, "<f4", (H, D))
+    return out
+
+
+def import_calib(cal: dict, n_q_heads: int, dtype: torch.dtype) -> Calib:
+    """aatc_import_calib from a dict of arrays (e.g. another calibration's export)."""
+    blob = make_blob(cal, n_q_heads, dtype)
+    h = ctypes.c_void_p()
+    _check(lib().aatc_import_calib(blob, len(blob), ctypes.byref(h)))
+    return Calib(h, dtype, np.asarray(cal["mu_k"]).shape[0], n_q_heads)
+
+
+def alloc_cache(calib: Calib, B: int, L_cap: int, device="cuda") -> torch.Tensor:
+    """An empty packed cache [B][H_kv][L_cap][W] of u32 words (stored as int32)."""
+    return torch.zeros(B, calib.n_kv_heads, L_cap, calib.W, dtype=torch.int32, device=device)
+
+
+def encode(calib: Calib, k: torch.Tensor, v: torch.Tensor, k_packed: torch.Tensor, v_packed: torch.Tensor,
+           start_pos: int = 0, stream=None):
+    """aatc_encode: k, v [B][H_kv][L_new][128] into rows start_pos.. of the packed caches."""
+    B, H, L_new, _ = k.shape
+    _check(lib().aatc_encode(calib.handle, _ptr(k), _ptr(v), B, L_new, int(start_pos), k_packed.shape[2],
+                             _ptr(k_packed), _ptr(v_packed), _stream(stream)))
+
+
+def workspace_size(calib: Calib, B: int, L: int) -> int:
+    return int(lib().aatc_decode_workspace_size(calib.handle, B, L))
+
+
+def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_packed: torch.Tensor, L: int,
+                     seq_lens: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                     workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """aatc_decode_attention: q [B][H_q][128] -> fp32 [B][H_q][128]."""
+    B = q.shape[0]
+    if out is None:
+        out = torch.empty(B, calib.n_q_heads, D, dtype=torch.float32, device=q.device)
+    need = workspace_size(calib, B, L)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    _check(lib().aatc_decode_attention(calib.handle, _ptr(q), _ptr(k_packed), _ptr(v_packed), k_packed.shape[2],
+                                       _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out

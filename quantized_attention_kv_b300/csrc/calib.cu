@@ -1,0 +1,552 @@
+// calib.cu -- device calibration pipeline: statistics, Jacobi eigensolver,
+// whitened key transform, bit allocation, step sizes and codec tables.
+//
+// Follows "Attention-Aware Transform Coding Guide: KV Compression" sections
+// "Decorrelation via the Karhunen-Loeve Transform (KLT)" (covariance + eigh)
+// and "Optimal Bit Allocation via Reverse Water-Filling", with the key metric
+// of "Theorem: Additive Error Decomposition" (key error weighted by the query)
+// and the non-orthogonal key transform of "Spend Bits Where Queries Look",
+// Abstract (generalized Parseval relation).
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int D = AATC_D;
+constexpr int MOMENT_CHUNK = 512;    // calibration rows per partial-moment block
+constexpr double JACOBI_TOL = 1e-15; // rotate (p,q) unless |a_pq| <= tol sqrt(|a_pp a_qq|)
+
+__device__ __forceinline__ double to_f64(float x) { return (double)x; }
+__device__ __forceinline__ double to_f64(__nv_bfloat16 x) { return (double)__bfloat162float(x); }
+
+// ---------------------------------------------------------------------------
+// Statistics
+// ---------------------------------------------------------------------------
+
+// mu[m][j] = mean over the n rows of matrix m (X: [M][n][D]).  One block per
+// matrix, one thread per channel, fp64 accumulation in row order.
+template <typename T>
+__global__ void k_mean(const T *__restrict__ X, long n, double *__restrict__ mu, uint32_t *status)
+{
+    const int m = blockIdx.x, j = threadIdx.x;
+    const T *x = X + (size_t)m * n * D + j;
+    double s = 0.0;
+    bool bad = false;
+    for (long i = 0; i < n; ++i) {
+        double v = to_f64(x[i * D]);
+        bad |= !isfinite(v);
+        s += v;
+    }
+    mu[m * D + j] = s / (double)n;
+    if (__syncthreads_or(bad) && j == 0) atomicOr(status, AATC_DEV_NONFINITE);
+}
+
+template <typename T>
+__global__ void k_check_finite(const T *__restrict__ x, size_t n, uint32_t *status)
+{
+    bool bad = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        bad |= !isfinite(to_f64(x[i]));
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(status, AATC_DEV_NONFINITE);
+}
+
+// Partial sums of (x - c)(x - c)^T over one chunk of MOMENT_CHUNK rows of
+// matrix m (blockIdx.y).  256 threads; thread (ty, tx) owns the 8x8 output
+// tile rows 8ty.., cols 8tx..; rows are staged 32 at a time in shared memory
+// as fp64 after subtracting the center.  partial: [M][nchunks][D][D].
+template <typename T>
+__global__ void __launch_bounds__(256) k_moment_partial(const T *__restrict__ X, long n,
+                                                        const double *__restrict__ center,
+                                                        double *__restrict__ partial)
+{
+    __shared__ double xs[32][D];
+    const int m = blockIdx.y, chunk = blockIdx.x, nchunks = gridDim.x;
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const T *x = X + (size_t)m * n * D;
+    const long r0 = (long)chunk * MOMENT_CHUNK;
+    const long r1 = min(n, r0 + MOMENT_CHUNK);
+    double acc[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.0;
+    for (long r = r0; r < r1; r += 32) {
+        const int rows = (int)min((long)32, r1 - r);
+        __syncthreads();
+        for (int e = tid; e < 32 * D; e += 256) {
+            int i = e / D, j = e % D;
+            double v = 0.0;
+            if (i < rows) v = to_f64(x[(r + i) * D + j]) - (center ? center[m * D + j] : 0.0);
+            xs[i][j] = v;
+        }
+        __syncthreads();
+        for (int i = 0; i < rows; ++i) {
+            double a[8], b[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) { a[k] = xs[i][ty * 8 + k]; b[k] = xs[i][tx * 8 + k]; }
+#pragma unroll
+            for (int p = 0; p < 8; ++p)
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[p][q] = fma(a[p], b[q], acc[p][q]);
+        }
+    }
+    double *out = partial + ((size_t)m * nchunks + chunk) * D * D;
+#pragma unroll
+    for (int p = 0; p < 8; ++p)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) out[(ty * 8 + p) * D + tx * 8 + q] = acc[p][q];
+}
+
+// out[m] = (1/n) sum over chunks (in order) of partial[m][chunk].
+__global__ void k_moment_reduce(const double *__restrict__ partial, int nchunks, long n,
+                                double *__restrict__ out)
+{
+    const int m = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= D * D) return;
+    const double *p = partial + (size_t)m * nchunks * D * D + e;
+    double s = 0.0;
+    for (int c = 0; c < nchunks; ++c) s += p[(size_t)c * D * D];
+    out[(size_t)m * D * D + e] = s / (double)n;
+}
+
+// ---------------------------------------------------------------------------
+// One-block parallel cyclic Jacobi for a symmetric 128x128 fp64 matrix.
+// ---------------------------------------------------------------------------
+// Shared memory: the upper triangle of A packed row-wise (8256 doubles) and
+// the full accumulated rotation V (16384 doubles) = 197,120 bytes.  Each sweep
+// runs the 127 rounds of a round-robin tournament: in round r index 127 meets
+// r and (r+k) meets (r-k) mod 127 for k = 1..63, so every round applies 64
+// disjoint plane rotations at once and a sweep meets every pair once.  The
+// rotation for a pair is the symmetric 2x2 Schur decomposition (Golub & Van
+// Loan, sec. 8.5); a pair is skipped when |a_pq| <= tol sqrt(|a_pp a_qq|), and
+// the iteration stops after a sweep with no rotation (the same test as a
+// cyclic-by-row order; only the order of rotations differs).
+// Output: eigenvalues descending (ties by index), eigenvectors as columns of
+// evecs [D][D], each signed so its largest-magnitude entry (lowest index on
+// ties) is positive.  A sweep cap bounds the work; hitting it sets
+// AATC_DEV_NO_CONVERGENCE.
+constexpr int JAC_THREADS = 512;
+constexpr int TRI = D * (D + 1) / 2;
+constexpr size_t JAC_SMEM = (size_t)(TRI + D * D) * sizeof(double) + 64 * 2 * sizeof(double) +
+                            64 * 2 * sizeof(int) + 4 * sizeof(int);
+
+__device__ __forceinline__ int tri(int i, int j)
+{
+    if (i > j) { int t = i; i = j; j = t; }
+    return i * D - (i * (i - 1)) / 2 + (j - i);
+}
+
+__global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict__ Ain, int max_sweeps,
+                                                        double *__restrict__ evals,
+                                                        double *__restrict__ evecs,
+                                                        uint32_t *status)
+{
+    extern __shared__ double smem[];
+    double *A = smem;                      // packed upper triangle
+    double *V = A + TRI;                   // [D][D]
+    double *cs = V + D * D;                // [64][2]
+    int *pq = (int *)(cs + 128);           // [64][2]
+    int *flag = pq + 128;                  // [0] rotated, [1] nonfinite
+    const int m = blockIdx.x, tid = threadIdx.x;
+    const double *Am = Ain + (size_t)m * D * D;
+
+    if (tid < 2) flag[tid] = 0;
+    __syncthreads();
+    for (int e = tid; e < D * D; e += JAC_THREADS) {
+        int i = e / D, j = e % D;
+        V[e] = (i == j) ? 1.0 : 0.0;
+        if (i <= j) {
+            double a = 0.5 * (Am[i * D + j] + Am[j * D + i]);
+            if (!isfinite(a)) flag[1] = 1;
+            A[tri(i, j)] = a;
+        }
+    }
+    __syncthreads();
+    if (flag[1]) {
+        if (tid == 0) atomicOr(status, AATC_DEV_NONFINITE);
+        for (int e = tid; e < D * D; e += JAC_THREADS) evecs[(size_t)m * D * D + e] = 0.0;
+        if (tid < D) evals[m * D + tid] = 0.0;
+        return;
+    }
+
+    bool converged = false;
+    for (int sweep = 0; sweep < max_sweeps && !converged; ++sweep) {
+        if (tid == 0) flag[0] = 0;
+        __syncthreads();
+        for (int r = 0; r < D - 1; ++r) {
+            if (tid < 64) {
+                int a, b;
+                if (tid == 0) { a = r; b = D - 1; }
+                else { a = (r + tid) % (D - 1); b = (r - tid + (D - 1)) % (D - 1); }
+                int p = min(a, b), q = max(a, b);
+                double apq = A[tri(p, q)], app = A[tri(p, p)], aqq = A[tri(q, q)];
+                double c = 1.0, s = 0.0;
+                if (fabs(apq) > JACOBI_TOL * sqrt(fabs(app * aqq))) {
+                    double tau = (aqq - app) / (2.0 * apq);
+                    double t = (tau >= 0.0 ? 1.0 : -1.0) / (fabs(tau) + sqrt(1.0 + tau * tau));
+                    c = 1.0 / sqrt(1.0 + t * t);
+                    s = t * c;
+                    flag[0] = 1;
+                }
+                pq[2 * tid] = p; pq[2 * tid + 1] = q;
+                cs[2 * tid] = c; cs[2 * tid + 1] = s;
+            }
+            __syncthreads();
+            // A <- J^T A J, one 2x2 block (pair k1, pair k2) per task, k1 <= k2
+            for (int blk = tid; blk < 64 * 65 / 2; blk += JAC_THREADS) {
+                int k2 = (int)((sqrt(8.0 * blk + 1.0) - 1.0) * 0.5);
+                while (k2 * (k2 + 1) / 2 > blk) --k2;
+                while ((k2 + 1) * (k2 + 2) / 2 <= blk) ++k2;
+                int k1 = blk - k2 * (k2 + 1) / 2;
+                int p1 = pq[2 * k1], q1 = pq[2 * k1 + 1];
+                double c1 = cs[2 * k1], s1 = cs[2 * k1 + 1];
+                if (k1 == k2) {
+                    double app = A[tri(p1, p1)], aqq = A[tri(q1, q1)], apq = A[tri(p1, q1)];
+                    if (s1 != 0.0) {
+                        A[tri(p1, p1)] = c1 * c1 * app - 2.0 * c1 * s1 * apq + s1 * s1 * aqq;
+                        A[tri(q1, q1)] = s1 * s1 * app + 2.0 * c1 * s1 * apq + c1 * c1 * aqq;
+                        A[tri(p1, q1)] = 0.0;
+                    }
+                } else {
+                    int p2 = pq[2 * k2], q2 = pq[2 * k2 + 1];
+                    double c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
+                    int i_pp = tri(p1, p2), i_pq = tri(p1, q2), i_qp = tri(q1, p2), i_qq = tri(q1, q2);
+                    double xpp = A[i_pp], xpq = A[i_pq], xqp = A[i_qp], xqq = A[i_qq];
+                    // rows: R1^T X  (R = [[c, s], [-s, c]])
+                    double ypp = c1 * xpp - s1 * xqp, ypq = c1 * xpq - s1 * xqq;
+                    double yqp = s1 * xpp + c1 * xqp, yqq = s1 * xpq + c1 * xqq;
+                    // columns: (R1^T X) R2
+                    A[i_pp] = c2 * ypp - s2 * ypq;
+                    A[i_pq] = s2 * ypp + c2 * ypq;
+                    A[i_qp] = c2 * yqp - s2 * yqq;
+                    A[i_qq] = s2 * yqp + c2 * yqq;
+                }
+            }
+            // V <- V J
+            for (int e = tid; e < D * 64; e += JAC_THREADS) {
+                int i = e >> 6, k = e & 63;
+                double c = cs[2 * k], s = cs[2 * k + 1];
+                if (s == 0.0) continue;
+                int p = pq[2 * k], q = pq[2 * k + 1];
+                double vp = V[i * D + p], vq = V[i * D + q];
+                V[i * D + p] = c * vp - s * vq;
+                V[i * D + q] = s * vp + c * vq;
+            }
+            __syncthreads();
+        }
+        converged = (flag[0] == 0);
+        __syncthreads();
+    }
+    if (!converged && tid == 0) atomicOr(status, AATC_DEV_NO_CONVERGENCE);
+
+    // sort descending (stable in index) and sign-normalize
+    if (tid < D) {
+        double li = A[tri(tid, tid)];
+        int rank = 0;
+        for (int k = 0; k < D; ++k) {
+            double lk = A[tri(k, k)];
+            rank += (lk > li) || (lk == li && k < tid);
+        }
+        evals[m * D + rank] = li;
+        int arg = 0;
+        double best = -1.0;
+        for (int i = 0; i < D; ++i) {
+            double v = fabs(V[i * D + tid]);
+            if (v > best) { best = v; arg = i; }
+        }
+        double sg = V[arg * D + tid] < 0.0 ? -1.0 : 1.0;
+        double *out = evecs + (size_t)m * D * D;
+        for (int i = 0; i < D; ++i) out[i * D + rank] = sg * V[i * D + tid];
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Small fp64 products: C[m] = op(A[m]) diag(f(lam[m])) op(B[m])
+// ---------------------------------------------------------------------------
+enum DiagMode { DIAG_NONE = 0, DIAG_SQRT = 1, DIAG_INVSQRT = 2 };
+
+// f(l) = sqrt / 1/sqrt of max(l, 1e-12 * lam[0]) (lam sorted descending).
+__global__ void k_gemm64(const double *__restrict__ A, int transA, const double *__restrict__ lam,
+                         int mode, const double *__restrict__ B, int transB, double *__restrict__ C)
+{
+    __shared__ double f[D];
+    const int m = blockIdx.y;
+    const double *Am = A + (size_t)m * D * D, *Bm = B + (size_t)m * D * D;
+    if (threadIdx.x < D) {
+        double v = 1.0;
+        if (mode != DIAG_NONE) {
+            double fl = 1e-12 * fmax(lam[m * D], 0.0);
+            double l = fmax(lam[m * D + threadIdx.x], fl);
+            if (l <= 0.0) l = 1e-300;
+            v = (mode == DIAG_SQRT) ? sqrt(l) : 1.0 / sqrt(l);
+        }
+        f[threadIdx.x] = v;
+    }
+    __syncthreads();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= D * D) return;
+    const int i = e / D, j = e % D;
+    double s = 0.0;
+    for (int k = 0; k < D; ++k) {
+        double a = transA ? Am[k * D + i] : Am[i * D + k];
+        double b = transB ? Bm[j * D + k] : Bm[k * D + j];
+        s += a * f[k] * b;
+    }
+    C[(size_t)m * D * D + e] = s;
+}
+
+// Y[m] = X[m]^T for [M][D][D] fp64 matrices.
+__global__ void k_transpose64(const double *__restrict__ X, double *__restrict__ Y)
+{
+    const int m = blockIdx.y;
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= D * D) return;
+    const int i = e / D, j = e % D;
+    Y[(size_t)m * D * D + e] = X[(size_t)m * D * D + j * D + i];
+}
+
+// ---------------------------------------------------------------------------
+// Bit allocation and step sizes
+// ---------------------------------------------------------------------------
+
+__device__ double gauss_pdf(double x) { return exp(-0.5 * x * x) * 0.3989422804014327; }
+__device__ double gauss_cdf(double x) { return 0.5 * erfc(-x * 0.7071067811865476); }
+
+// Centroid map of a mid-rise uniform quantizer with N levels on N(0,1): given
+// the step D (which fixes the cells), the step whose levels c_u D best fit
+// the cell means in the MSE sense, sum_u c_u E[x; cell_u] / sum_u c_u^2 P_u.
+__device__ double centroid_step(int N, double Dlt)
+{
+    double num = 0.0, den = 0.0;
+    for (int u = 0; u < N; ++u) {
+        double c = u - 0.5 * (N - 1);
+        double lo = (u - 0.5 * N) * Dlt, hi = (u + 1 - 0.5 * N) * Dlt;
+        double Plo = (u == 0) ? 0.0 : gauss_cdf(lo), Phi = (u == N - 1) ? 1.0 : gauss_cdf(hi);
+        double flo = (u == 0) ? 0.0 : gauss_pdf(lo), fhi = (u == N - 1) ? 0.0 : gauss_pdf(hi);
+        num += c * (flo - fhi);
+        den += c * c * (Phi - Plo);
+    }
+    return num / den;
+}
+
+// The MSE-optimal step is the fixed point of centroid_step; solved by the
+// secant method on centroid_step(D) - D from D0 = 4/N.
+__device__ double gauss_uniform_step(int b)
+{
+    const int N = 1 << b;
+    double x0 = 4.0 / N, x1 = centroid_step(N, x0);
+    double r0 = x1 - x0;
+    for (int it = 0; it < 200; ++it) {
+        double r1 = centroid_step(N, x1) - x1;
+        if (r1 == 0.0 || r1 == r0) break;
+        double x2 = x1 - r1 * (x1 - x0) / (r1 - r0);
+        x0 = x1; r0 = r1; x1 = x2;
+        if (fabs(x1 - x0) <= 1e-16 * x1) break;
+    }
+    return x1;
+}
+
+// One block of 1024 threads per (head, tensor); thread t owns the gain of
+// channel j = t/8 for its (t%8+1)-th bit, g = lam_j 4^{-(t%8)}.  The B
+// largest gains are selected exactly: a bisection over the ordered bit
+// patterns of the non-negative doubles finds the B-th largest gain value g*
+// (count(g >= lo) >= B > count(g >= hi) is kept invariant), every gain above
+// g* is taken, and gains equal to g* are taken in (j, t) order until the
+// budget is met.  b_j = number of taken gains of channel j.
+// Delta_j = s_{b_j} sqrt(lam_j) rounded to fp32.
+__global__ void __launch_bounds__(1024) k_waterfill(const double *__restrict__ lam_k,
+                                                    const double *__restrict__ lam_v, int Bbits,
+                                                    int32_t *__restrict__ bits_k, int32_t *__restrict__ bits_v,
+                                                    float *__restrict__ step_k, float *__restrict__ step_v)
+{
+    __shared__ double gain[D * AATC_MAXB];
+    __shared__ double s_tab[AATC_MAXB + 1];
+    __shared__ int nb[D];
+    __shared__ unsigned long long mx;
+    const int h = blockIdx.x, tensor = blockIdx.y, t = threadIdx.x;
+    const double *lam = (tensor == 0 ? lam_k : lam_v) + h * D;
+    const int j = t >> 3, tb = t & 7;
+    const double g = ldexp(fmax(lam[j], 0.0), -2 * tb);
+    gain[t] = g;
+    if (t <= AATC_MAXB) s_tab[t] = (t == 0) ? 0.0 : gauss_uniform_step(t);
+    if (t < D) nb[t] = 0;
+    if (t == 0) mx = 0ull;
+    __syncthreads();
+    atomicMax(&mx, (unsigned long long)__double_as_longlong(g));
+    __syncthreads();
+    long long lo = 0, hi = (long long)mx + 1;   // count(g >= 0) = all >= B > 0 = count(g >= hi)
+    while (hi - lo > 1) {
+        long long mid = lo + (hi - lo) / 2;
+        int c = __syncthreads_count(g >= __longlong_as_double(mid));
+        if (c >= Bbits) lo = mid; else hi = mid;
+    }
+    const double gstar = __longlong_as_double(lo);
+    const int above = __syncthreads_count(g > gstar);
+    bool take = g > gstar;
+    if (g == gstar) {
+        int before = 0;
+        for (int k = 0; k < t; ++k) before += (gain[k] == gstar);
+        take = (above + before) < Bbits;
+    }
+    if (take) atomicAdd(&nb[j], 1);
+    __syncthreads();
+    if (t < D) {
+        int b = nb[t];
+        (tensor == 0 ? bits_k : bits_v)[h * D + t] = b;
+        float st = b > 0 ? (float)(s_tab[b] * sqrt(fmax(lam[t], 0.0))) : 0.0f;
+        (tensor == 0 ? step_k : step_v)[h * D + t] = st;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Derived fp32 operands and codec tables
+// ---------------------------------------------------------------------------
+
+// One block of 128 threads per (head, tensor): record layout offsets (all
+// 8-bit fields, then 4-, 2-, 1-bit fields, channels ascending), 1/Delta,
+// midpoints, and the bias b = T mu.
+__global__ void k_tables(const int32_t *__restrict__ bits_k, const int32_t *__restrict__ bits_v,
+                         const float *__restrict__ step_k, const float *__restrict__ step_v,
+                         const double *__restrict__ T_k, const double *__restrict__ T_v,
+                         const double *__restrict__ mu_k, const double *__restrict__ mu_v,
+                         CodecTables *__restrict__ tab, float *__restrict__ bk32, float *__restrict__ bv32)
+{
+    __shared__ int bs[D];
+    const int h = blockIdx.x, tensor = blockIdx.y, j = threadIdx.x;
+    const int32_t *bits = (tensor == 0 ? bits_k : bits_v) + h * D;
+    const float *step = (tensor == 0 ? step_k : step_v) + h * D;
+    CodecTables &T = tab[h * 2 + tensor];
+    const int b = bits[j];
+    bs[j] = b;
+    __syncthreads();
+    int pos = 0;
+    for (int s = 3; s >= 0; --s) {
+        int before = 0, total = 0;
+        for (int k = 0; k < D; ++k) {
+            int has = (bs[k] >> s) & 1;
+            total += has;
+            before += has && k < j;
+        }
+        T.off[j][s] = ((b >> s) & 1) ? (int16_t)(pos + before * (1 << s)) : (int16_t)-1;
+        pos += total * (1 << s);
+    }
+    const float st = step[j];
+    T.bits[j] = (uint8_t)b;
+    T.step[j] = st;
+    T.inv_step[j] = b > 0 ? __frcp_rn(st) : 0.0f;
+    T.mid[j] = b > 0 ? 0.5f * (float)((1 << b) - 1) : 0.0f;
+    T.top[j] = (float)((1 << b) - 1);
+    const double *Tm = (tensor == 0 ? T_k : T_v) + (size_t)h * D * D;
+    const double *mu = (tensor == 0 ? mu_k : mu_v) + h * D;
+    double acc = 0.0;
+    for (int k = 0; k < D; ++k) acc += Tm[j * D + k] * mu[k];
+    (tensor == 0 ? bk32 : bv32)[h * D + j] = (float)acc;
+}
+
+__global__ void k_to_f32(const double *__restrict__ x, float *__restrict__ y, size_t n)
+{
+    size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) y[i] = (float)x[i];
+}
+
+template <typename T>
+aatc_status launch_stats(const T *k, const T *v, const T *q, aatc_calib *h, int N, double *Sk,
+                         double *Sv, double *Sq, double *partial, cudaStream_t s)
+{
+    const int H = h->Hkv, G = h->G;
+    k_mean<T><<<H, D, 0, s>>>(k, N, h->mu_k, h->status);
+    k_mean<T><<<H, D, 0, s>>>(v, N, h->mu_v, h->status);
+    {   // q enters only through its second moment; check it for NaN/Inf
+        const size_t nq = (size_t)h->Hq * N * D;
+        const size_t blocks = (nq + 255) / 256 < 4096 ? (nq + 255) / 256 : 4096;
+        k_check_finite<T><<<(unsigned)blocks, 256, 0, s>>>(q, nq, h->status);
+    }
+    const int nck = (N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
+    const long nq = (long)G * N;
+    const int nckq = (int)((nq + MOMENT_CHUNK - 1) / MOMENT_CHUNK);
+    k_moment_partial<T><<<dim3(nck, H), 256, 0, s>>>(k, N, h->mu_k, partial);
+    k_moment_reduce<<<dim3(D * D / 256, H), 256, 0, s>>>(partial, nck, N, Sk);
+    k_moment_partial<T><<<dim3(nck, H), 256, 0, s>>>(v, N, h->mu_v, partial);
+    k_moment_reduce<<<dim3(D * D / 256, H), 256, 0, s>>>(partial, nck, N, Sv);
+    k_moment_partial<T><<<dim3(nckq, H), 256, 0, s>>>(q, nq, nullptr, partial);
+    k_moment_reduce<<<dim3(D * D / 256, H), 256, 0, s>>>(partial, nckq, nq, Sq);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}
+
+}  // namespace
+
+size_t calib_work_bytes(int Hkv, int Hq, int N)
+{
+    const int G = Hq / Hkv;
+    const size_t mat = (size_t)D * D * sizeof(double);
+    const size_t nck = (size_t)(N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
+    const size_t nckq = ((size_t)G * N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
+    const size_t partial = (size_t)Hkv * (nck > nckq ? nck : nckq) * mat;
+    return partial + (size_t)Hkv * 7 * mat;   // Sk Sv Sq Uq Sh Si Mk
+}
+
+aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const void *q_cal,
+                      int N, int max_sweeps, void *work, cudaStream_t s)
+{
+    const int H = h->Hkv;
+    const size_t M = (size_t)D * D;
+    double *base = (double *)work;
+    const int G = h->G;
+    const size_t nck = (size_t)(N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
+    const size_t nckq = ((size_t)G * N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
+    double *partial = base;
+    double *Sk = partial + (size_t)H * (nck > nckq ? nck : nckq) * M;
+    double *Sv = Sk + H * M, *Sq = Sv + H * M, *Uq = Sq + H * M, *Sh = Uq + H * M,
+           *Si = Sh + H * M, *Mk = Si + H * M;
+    aatc_status st;
+    if (h->dtype == AATC_BF16)
+        st = launch_stats((const __nv_bfloat16 *)k_cal, (const __nv_bfloat16 *)v_cal,
+                          (const __nv_bfloat16 *)q_cal, h, N, Sk, Sv, Sq, partial, s);
+    else
+        st = launch_stats((const float *)k_cal, (const float *)v_cal, (const float *)q_cal, h, N,
+                          Sk, Sv, Sq, partial, s);
+    if (st != AATC_OK) return st;
+
+    AATC_CUDA(cudaFuncSetAttribute(k_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)JAC_SMEM));
+    // query metric: Sq = Uq Lq Uq^T ; Sh = Sq^{1/2}, Si = Sq^{-1/2}
+    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Sq, max_sweeps, h->lam_q, Uq, h->status);
+    const dim3 gg(D * D / 256, H);
+    k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_SQRT, Uq, 1, Sh);
+    k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_INVSQRT, Uq, 1, Si);
+    // whitened key covariance Mk = Sh Sk Sh (Jacobi reads its symmetric part)
+    k_gemm64<<<gg, 256, 0, s>>>(Sh, 0, nullptr, DIAG_NONE, Sk, 0, Uq);       // Uq reused as tmp
+    k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, nullptr, DIAG_NONE, Sh, 0, Mk);
+    // KLTs: Mk = Uk Lk Uk^T (Uk kept in Uq), Sv = Uv Lv Uv^T
+    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Mk, max_sweeps, h->lam_k, Uq, h->status);
+    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Sv, max_sweeps, h->lam_v, h->U_v, h->status);
+    // Tk = Uk^T Sh, Ak = Uk^T Si, Tk^{-1} = Si Uk, Tv = Uv^T
+    k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Sh, 0, h->T_k);
+    k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Si, 0, h->A_k);
+    k_gemm64<<<gg, 256, 0, s>>>(Si, 0, nullptr, DIAG_NONE, Uq, 0, h->T_k_inv);
+    k_transpose64<<<gg, 256, 0, s>>>(h->U_v, h->T_v);
+    AATC_CUDA(cudaGetLastError());
+    k_waterfill<<<dim3(H, 2), 1024, 0, s>>>(h->lam_k, h->lam_v, h->Bbits, h->bits_k, h->bits_v,
+                                            h->step_k, h->step_v);
+    AATC_CUDA(cudaGetLastError());
+    return calib_derive(h, s);
+}
+
+aatc_status calib_derive(aatc_calib *h, cudaStream_t s)
+{
+    const int H = h->Hkv;
+    const size_t n = (size_t)H * D * D;
+    const int blocks = (int)((n + 255) / 256);
+    k_to_f32<<<blocks, 256, 0, s>>>(h->T_k, h->Tk32, n);
+    k_to_f32<<<blocks, 256, 0, s>>>(h->T_v, h->Tv32, n);
+    k_to_f32<<<blocks, 256, 0, s>>>(h->A_k, h->Ak32, n);
+    k_to_f32<<<blocks, 256, 0, s>>>(h->U_v, h->Uv32, n);
+    k_to_f32<<<(H * D + 255) / 256, 256, 0, s>>>(h->mu_v, h->muv32, (size_t)H * D);
+    k_tables<<<dim3(H, 2), D, 0, s>>>(h->bits_k, h->bits_v, h->step_k, h->step_v, h->T_k, h->T_v,
+                                      h->mu_k, h->mu_v, h->tab, h->bk32, h->bv32);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}

@@ -1,0 +1,129 @@
+// encode.cu -- transform, quantize and bit-pack keys/values into fixed-width
+// per-token records.
+//
+// "Attention-Aware Transform Coding Guide: KV Compression", section
+// "End-to-End Implementation" (rotate into the calibrated basis, quantize each
+// channel at its allocated width) and "Spend Bits Where Queries Look",
+// Abstract (fixed per-token bit count).
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int D = AATC_D;
+constexpr int ENC_TILE = 128;     // tokens per block, one thread per token
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// One block per (128-token tile, KV head, batch row x tensor).  Each thread
+// owns one token: c = T x - T mu (fp32 FMA with T in shared memory),
+// v = c * (1/Delta) + mid, u = clamp(rint(v), 0, 2^b - 1), then the fields of
+// u are ORed into the token's record in shared memory and the record is
+// written to rows start_pos + token of the packed cache.
+template <typename T>
+__global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
+    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, int L_cap, int Hkv,
+    int W, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
+    const float *__restrict__ bv, const CodecTables *__restrict__ tabs, uint32_t *__restrict__ kp,
+    uint32_t *__restrict__ vp, uint32_t *status)
+{
+    extern __shared__ float sm[];
+    float *Ts = sm;                          // [D][D] transposed: Ts[kk][j] = T[j][kk]
+    float *xs = Ts + D * D;                  // [ENC_TILE][D+1]
+    uint32_t *rec = (uint32_t *)(xs + ENC_TILE * (D + 1));   // [ENC_TILE][W+1]
+    const int tile = blockIdx.x, h = blockIdx.y;
+    const int b = blockIdx.z >> 1, tensor = blockIdx.z & 1;
+    const int t = threadIdx.x;
+    const T *x = (tensor == 0 ? k : v) + (((size_t)b * Hkv + h) * L_new) * D;
+    const float *Tm = (tensor == 0 ? Tk : Tv) + (size_t)h * D * D;
+    const float *bias = (tensor == 0 ? bk : bv) + h * D;
+    const CodecTables &tb = tabs[h * 2 + tensor];
+    uint32_t *out = (tensor == 0 ? kp : vp) + ((size_t)b * Hkv + h) * L_cap * W;
+
+    for (int e = t; e < D * D; e += ENC_TILE) {
+        int j = e / D, kk = e % D;
+        Ts[kk * D + j] = Tm[e];
+    }
+    const int tok0 = tile * ENC_TILE;
+    const int ntok = min(ENC_TILE, L_new - tok0);
+    bool bad = false;
+    for (int e = t; e < ENC_TILE * D; e += ENC_TILE) {
+        int i = e / D, kk = e % D;
+        float val = 0.f;
+        if (i < ntok) val = to_f32(x[(size_t)(tok0 + i) * D + kk]);
+        bad |= !isfinite(val);
+        xs[i * (D + 1) + kk] = val;
+    }
+    for (int w = 0; w < W; ++w) rec[t * (W + 1) + w] = 0u;
+    if (__syncthreads_or(bad) && t == 0) atomicOr(status, AATC_DEV_NONFINITE);
+
+    const float *xr = xs + t * (D + 1);
+    uint32_t *myrec = rec + t * (W + 1);
+    for (int j0 = 0; j0 < D; j0 += 16) {
+        float acc[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) acc[q] = 0.f;
+        for (int kk = 0; kk < D; ++kk) {
+            const float xv = xr[kk];
+            const float4 *tr = (const float4 *)(Ts + kk * D + j0);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                float4 tv = tr[q4];
+                acc[4 * q4 + 0] = fmaf(tv.x, xv, acc[4 * q4 + 0]);
+                acc[4 * q4 + 1] = fmaf(tv.y, xv, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(tv.z, xv, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(tv.w, xv, acc[4 * q4 + 3]);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int j = j0 + q;
+            const int bj = tb.bits[j];
+            if (bj == 0) continue;
+            const float c = acc[q] - bias[j];
+            float vq = fmaf(c, tb.inv_step[j], tb.mid[j]);
+            vq = fminf(fmaxf(rintf(vq), 0.f), tb.top[j]);
+            const uint32_t u = (uint32_t)vq;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                const int o = tb.off[j][s];
+                if (o < 0) continue;
+                const int width = 1 << s;
+                const uint32_t f = (u >> (bj & (width - 1))) & ((1u << width) - 1u);
+                myrec[o >> 5] |= f << (o & 31);
+            }
+        }
+    }
+    __syncthreads();
+    // coalesced copy of the tile's records (rows start_pos + tok0 ..)
+    uint32_t *dst = out + (size_t)(start_pos + tok0) * W;
+    for (int e = t; e < ntok * W; e += ENC_TILE) dst[e] = rec[(e / W) * (W + 1) + (e % W)];
+}
+
+}  // namespace
+
+aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
+                       int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+{
+    if (L_new == 0 || B == 0) return AATC_OK;
+    const size_t smem = (size_t)D * D * 4 + (size_t)ENC_TILE * (D + 1) * 4 +
+                        (size_t)ENC_TILE * (h->W + 1) * 4;
+    const dim3 grid((L_new + ENC_TILE - 1) / ENC_TILE, h->Hkv, 2 * B);
+    if (h->dtype == AATC_BF16) {
+        auto kern = k_encode_simple<__nv_bfloat16>;
+        AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        kern<<<grid, ENC_TILE, smem, s>>>((const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, L_new,
+                                          start_pos, L_cap, h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32,
+                                          h->bv32, h->tab, kp, vp, h->status);
+    } else {
+        auto kern = k_encode_simple<float>;
+        AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        kern<<<grid, ENC_TILE, smem, s>>>((const float *)k, (const float *)v, L_new, start_pos, L_cap,
+                                          h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, kp,
+                                          vp, h->status);
+    }
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}

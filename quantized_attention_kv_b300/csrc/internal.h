@@ -1,0 +1,77 @@
+// internal.h -- private declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "aatc.h"
+
+#define AATC_D 128          // head dimension
+#define AATC_MAXB 8         // widest per-channel code
+#define AATC_MAX_G 16       // widest GQA group served by one decode block
+
+// Device status bits (the handle's status word, set with atomicOr).
+enum : uint32_t {
+    AATC_DEV_NONFINITE = 1u,
+    AATC_DEV_NO_CONVERGENCE = 2u,
+};
+
+// Per (KV head, tensor) codec tables, fp32/int, derived from bits and steps.
+// One struct per (head, tensor); tensor 0 = K, 1 = V.
+struct CodecTables {
+    float inv_step[AATC_D];   // 1 / Delta_j (correctly rounded), 0 if b_j = 0
+    float mid[AATC_D];        // (2^b_j - 1) / 2, 0 if b_j = 0
+    float top[AATC_D];        // 2^b_j - 1
+    float step[AATC_D];       // Delta_j
+    int16_t off[AATC_D][4];   // record bit offset of the width-2^s field, -1 if absent
+    uint8_t bits[AATC_D];     // b_j
+};
+
+struct aatc_calib {
+    int d, Hkv, Hq, G, Bbits, W;
+    aatc_dtype dtype;
+    void *arena;              // one cudaMalloc backing every device array below
+    // fp64 calibration results, [H] leading (exported by aatc_export_calib)
+    double *mu_k, *mu_v;                      // [H][d]
+    double *T_k, *T_k_inv, *A_k, *T_v, *U_v;  // [H][d][d]
+    double *lam_k, *lam_v, *lam_q;            // [H][d]
+    int32_t *bits_k, *bits_v;                 // [H][d]
+    float *step_k, *step_v;                   // [H][d]
+    // fp32 operands of the encode / decode kernels
+    float *Tk32, *Tv32;       // [H][d][d] transform rows (coefficient i = row i . x)
+    float *bk32, *bv32;       // [H][d] T mu
+    float *Ak32;              // [H][d][d] Tk^{-T}: q' = A_k q
+    float *Uv32;              // [H][d][d] inverse value transform
+    float *muv32;             // [H][d]
+    CodecTables *tab;         // [H][2]
+    uint32_t *status;         // device status word
+};
+
+// ---- error reporting (api.cu) ----
+aatc_status aatc_fail(aatc_status st, const char *fmt, ...);
+aatc_status aatc_cuda_fail(cudaError_t e, const char *what);
+#define AATC_CUDA(call)                                                   \
+    do {                                                                  \
+        cudaError_t _e = (call);                                          \
+        if (_e != cudaSuccess) return aatc_cuda_fail(_e, #call);          \
+    } while (0)
+
+// ---- calibration kernels (calib.cu) ----
+// Runs the whole device calibration pipeline for handle h on stream s.
+// Inputs as in aatc_calibrate.  Scratch is taken from `work` (bytes from
+// calib_work_bytes).  Returns a launch error, device conditions go to h->status.
+size_t calib_work_bytes(int Hkv, int Hq, int N);
+aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const void *q_cal,
+                      int N, int max_sweeps, void *work, cudaStream_t s);
+// Rebuild the fp32 operands and codec tables from the fp64 results.
+aatc_status calib_derive(aatc_calib *h, cudaStream_t s);
+
+// ---- encode (encode.cu) ----
+aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
+                       int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s);
+
+// ---- decode (decode.cu) ----
+size_t decode_ws_bytes(const aatc_calib *h, int B, int L);
+aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, const uint32_t *vp,
+                       int L_cap, const int32_t *seq_lens, int L, int B, float *out, void *ws,
+                       size_t ws_bytes, cudaStream_t s);
