@@ -1,0 +1,350 @@
+"""Benchmark of the AATC hot path on one B300 per rank.
+
+One step = the workload's whole pass through the codec on synthetic data:
+encode the full prefill (all KV heads, keys and values) into the packed
+cache, then one decode step (encode the new token at position L, then decode
+attention of every query head over the L+1 packed tokens).  Calibration is an
+offline, once-per-layer step: it runs (and is timed) once before the loop.
+
+Headline `value`: decode-attention packed-KV GB/s = (packed K + packed V
+bytes + q bytes + output bytes) / decode time, CUDA events on the launching
+stream; `encode` reports prefill token positions per second per layer.  The
+L2 (126 MB) is flushed by writing a 256 MB buffer before each decode call, so
+the packed cache is read from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama_32k]
+    python bench.py --impl reference     # the CPU oracle on a bounded sample
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_attention_kv_b300 import synth  # noqa: E402
+
+DECODE_KERNELS_PER_CALL = 3     # query prep, split-K attention, combine
+ENCODE_KERNELS_PER_CALL = 1
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6400.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_ours(args, ws, rank, local):
+    from quantized_attention_kv_b300 import aatc
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = synth.WORKLOADS[args.workload]
+    L = args.seq_len or wl.seq_len
+    B, Hkv, Hq = wl.batch, wl.n_kv_heads, wl.n_q_heads
+    bits = args.bits or wl.bits
+
+    # inputs resident in HBM before anything is timed
+    k_cal, v_cal, q_cal = synth.calib_inputs(wl, device=dev)
+    kc, vc = synth.cache_inputs(wl, device=dev, seq_len=L)
+    kn, vn = synth.cache_inputs(wl, layer=1, device=dev, seq_len=1)
+    q = synth.query_inputs(wl, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cal = aatc.calibrate(k_cal, v_cal, q_cal, bits)
+    torch.cuda.synchronize()
+    calib_ms = (time.perf_counter() - t0) * 1e3
+    W = cal.W
+    kp = aatc.alloc_cache(cal, B, L + 1, device=dev)
+    vp = aatc.alloc_cache(cal, B, L + 1, device=dev)
+    out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
+    wsb = torch.empty(max(aatc.workspace_size(cal, B, L + 1), 16), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    packed_bytes = 2 * B * Hkv * (L + 1) * W * 4
+    q_bytes = q.numel() * q.element_size()
+    out_bytes = out.numel() * 4
+    decode_bytes = packed_bytes + q_bytes + out_bytes
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        aatc.encode(cal, kc, vc, kp, vp, start_pos=0)
+        if evs:
+            evs[1].record(stream)
+        aatc.encode(cal, kn, vn, kp, vp, start_pos=L)
+        flush.zero_()
+        if evs:
+            evs[2].record(stream)
+        aatc.decode_attention(cal, q, kp, vp, L + 1, out=out, workspace=wsb)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        for s in range(args.steps):
+            step(evs[s])
+        torch.cuda.synchronize()
+        _barrier(ws)
+        wall = time.perf_counter() - w0
+    enc_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    wall = _max_over_ranks(wall, ws)
+    dec_total_s = _max_over_ranks(sum(dec_ms) / 1e3, ws)
+    enc_total_s = _max_over_ranks(sum(enc_ms) / 1e3, ws)
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs (query, new key/value token), append + decode, D2H of the output
+    qh = q.cpu().pin_memory()
+    knh, vnh = kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    outh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
+    qd, knd, vnd = torch.empty_like(q), torch.empty_like(kn), torch.empty_like(vn)
+
+    def e2e_step(evs=None):
+        flush.zero_()
+        if evs:
+            evs[0].record(stream)
+        qd.copy_(qh, non_blocking=True)
+        knd.copy_(knh, non_blocking=True)
+        vnd.copy_(vnh, non_blocking=True)
+        aatc.encode(cal, knd, vnd, kp, vp, start_pos=L)
+        aatc.decode_attention(cal, qd, kp, vp, L + 1, out=out, workspace=wsb)
+        outh.copy_(out, non_blocking=True)
+        if evs:
+            evs[1].record(stream)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_evs = [[ev() for _ in range(2)] for _ in range(args.steps)]
+    for s in range(args.steps):
+        e2e_step(e2e_evs[s])
+    torch.cuda.synchronize()
+    e2e_ms = [e[0].elapsed_time(e[1]) for e in e2e_evs]
+    e2e_s = _max_over_ranks(sum(e2e_ms) / 1e3, ws)
+    h2d = q_bytes + knh.numel() * 2 + vnh.numel() * 2
+    d2h = out_bytes
+
+    peak, peak_kind = _peaks()
+    value = decode_bytes * args.steps * ws / dec_total_s / 1e9
+    per_launch_s = dec_total_s / args.steps
+    achieved = decode_bytes / per_launch_s / 1e9
+    res = {
+        "metric": "decode-attn packed-KV GB/s (% of HBM peak) and encode tokens/s at 32k ctx",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(wall / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+        "data": "synthetic (seeded Gaussian KV shaped like the workload; no weights or datasets)",
+        "config": {"workload": wl.name, "batch": B, "seq_len": L + 1, "n_q_heads": Hq, "n_kv_heads": Hkv,
+                   "head_dim": 128, "bits_per_element": bits, "record_words": W,
+                   "l2": "flushed (256 MB write) before every decode call",
+                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+        "pct_of_hbm_peak": round(100 * value / ws / peak, 2),
+        "encode": {"value": round(L * args.steps * ws / enc_total_s, 1), "unit": "tokens/s",
+                   "ms": round(enc_total_s / args.steps * 1e3, 4),
+                   "gb_s": round((2 * B * Hkv * L * (128 * kc.element_size() + W * 4)) * args.steps
+                                 / enc_total_s / 1e9, 2)},
+        "decode_us": round(per_launch_s * 1e6, 3),
+        "calibrate_ms": round(calib_ms, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "decode_attention (query prep + split-K + combine, timed together)",
+                     "peak_kind": peak_kind},
+        "e2e": {"value": round(decode_bytes * args.steps * ws / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (2 * ENCODE_KERNELS_PER_CALL + DECODE_KERNELS_PER_CALL),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, L, bits)
+    return res
+
+
+def cpu_baseline(wl, L, bits, budget_s=20.0):
+    """The fp64 oracle on the host cores: decode attention of ONE KV head (its
+    G query heads) over the full context, from records the oracle encoded."""
+    import numpy as np
+
+    import oracle
+    k_cal, v_cal, q_cal = synth.calib_inputs(wl, device="cpu")
+    h = 0
+    G = wl.group
+    sub = lambda t: t[h:h + 1].double().numpy()  # noqa: E731
+    cal = oracle.calibrate(sub(k_cal), sub(v_cal), q_cal[h * G:(h + 1) * G].double().numpy(), bits)
+    kc, vc = synth.cache_inputs(synth.dataclasses.replace(wl, n_kv_heads=1, n_q_heads=G, batch=1),
+                                device="cpu", seq_len=L)
+    t0 = time.perf_counter()
+    kp, _, _ = oracle.encode_cache(kc.double().numpy(), cal, "k")
+    vp, _, _ = oracle.encode_cache(vc.double().numpy(), cal, "v")
+    enc_s = time.perf_counter() - t0
+    q = synth.query_inputs(wl, batch=1)[:, h * G:(h + 1) * G].double().numpy()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle.decode_attention(q, kp, vp, cal)
+        n += 1
+        if time.perf_counter() - t0 > min(budget_s, 5.0) or n >= 3:
+            break
+    dec_s = (time.perf_counter() - t0) / n
+    W = cal["W"]
+    nbytes = 2 * L * W * 4 + G * 128 * 2 + G * 128 * 4
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(nbytes / dec_s / 1e9, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": "1 of %d KV heads (%d query heads) at %d tokens: decode %.3f s/call; encode %d tokens x K,V "
+                      "%.2f s (%.0f tokens/s)" % (wl.n_kv_heads, G, L, dec_s, L, enc_s, L / enc_s),
+            "encode_tokens_per_s": round(L / enc_s, 1)}
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the CPU oracle, as it stands, on a bounded sample of the
+    same workload; each step decodes one KV head over the full context."""
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[args.workload]
+    L = args.seq_len or wl.seq_len
+    bits = args.bits or wl.bits
+    base = cpu_baseline(wl, L, bits)
+    import oracle  # noqa: F401
+    return {
+        "impl": "reference",
+        "metric": "decode-attn packed-KV GB/s (% of HBM peak) and encode tokens/s at 32k ctx",
+        "value": base["value"], "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "seq_len": L, "bits_per_element": bits},
+        "cpu_baseline": {"kind": "oracle", "cores": base["cores"], "sample": base["sample"], "value": base["value"]},
+        "e2e": {"value": base["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama_32k", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seq-len", type=int, default=None)
+    ap.add_argument("--bits", type=float, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        res = run_reference(args, ws, rank)
+    else:
+        from quantized_attention_kv_b300 import build
+        if rank == 0:
+            build.build()
+        _barrier(ws)
+        res = run_ours(args, ws, rank, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

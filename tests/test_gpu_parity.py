@@ -1,0 +1,247 @@
+"""GPU parity: the CUDA library (through its C ABI) against the fp64 oracle.
+
+Per-kernel checks import the oracle's calibration into a GPU handle and feed
+identical inputs (and, for decode, identical oracle-packed records), so each
+kernel is isolated.  End-to-end checks run GPU calibration + encode + decode
+on the full workload sizes and compare with the oracle's own pipeline on
+sampled heads.  Tolerances are those of tests/parity_util.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import ATTN_RTOL, as_u32, attn_rel_err, compare_codes, to_np64
+from quantized_attention_kv_b300 import aatc, synth
+
+pytestmark = pytest.mark.gpu
+WL = synth.WORKLOADS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_attention_kv_b300 import build
+    build.build()
+    aatc.lib()
+    yield
+    torch.cuda.synchronize()
+
+
+def _oracle_cal(k, v, q, bits):
+    return oracle.calibrate(to_np64(k), to_np64(v), to_np64(q), bits)
+
+
+# ----------------------------------------------------------------- calibration
+_tiny_cache = {}
+
+
+def _tiny():
+    if not _tiny_cache:
+        wl = WL["tiny"]
+        k, v, q = synth.calib_inputs(wl, device="cuda")
+        _tiny_cache.update(wl=wl, k=k, v=v, q=q, ocal=_oracle_cal(k, v, q, wl.bits))
+    return _tiny_cache
+
+
+def _check_calibration(gcal: dict, ocal: dict, H: int):
+    ties = 0
+    for t in ("k", "v"):
+        for h in range(H):
+            gb, ob = gcal["bits_" + t][h], ocal["bits_" + t][h]
+            if not np.array_equal(gb, ob):
+                assert ocal["margin_" + t][h] < 1e-9, ("allocation differs away from a tie", t, h)
+                ties += 1
+                continue
+            assert gb.sum() == ocal["W"] * 32
+            gs, os_ = gcal["step_" + t][h], ocal["step_" + t][h]
+            ulp = np.spacing(np.abs(os_).astype(np.float32))
+            assert np.all(np.abs(gs.astype(np.float64) - os_) <= 1.0 * ulp), (t, h)
+        lam_g, lam_o = gcal["lam_" + t], ocal["lam_" + t]
+        assert np.abs(lam_g - lam_o).max() <= 1e-10 * np.abs(lam_o).max()
+    np.testing.assert_allclose(gcal["mu_k"], ocal["mu_k"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gcal["mu_v"], ocal["mu_v"], rtol=0, atol=1e-12)
+    for key in ("T_k", "A_k", "T_k_inv", "T_v", "U_v"):
+        g, o = gcal[key], ocal[key]
+        assert np.abs(g - o).max() <= 1e-7 * np.abs(o).max(), key
+    return ties
+
+
+def test_calibration_matches_oracle_tiny():
+    c = _tiny()
+    g = aatc.calibrate(c["k"], c["v"], c["q"], c["wl"].bits)
+    gcal = g.export()
+    assert gcal["W"] == 11
+    _check_calibration(gcal, c["ocal"], 1)
+    # generalized Parseval with the GPU transform and the data's query moment
+    Q = to_np64(c["q"]).reshape(-1, 128)
+    Sq = Q.T @ Q / Q.shape[0]
+    Ti = gcal["T_k_inv"][0]
+    assert np.abs(Ti.T @ Sq @ Ti - np.eye(128)).max() < 1e-8
+
+
+def test_calibration_errors_reported():
+    c = _tiny()
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.calibrate(c["k"], c["v"], c["q"], c["wl"].bits, jacobi_max_sweeps=1)
+    assert e.value.status == aatc.ERR_NO_CONVERGENCE
+    kb = c["k"].clone()
+    kb[0, 17, 5] = float("nan")
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.calibrate(kb, c["v"], c["q"], c["wl"].bits)
+    assert e.value.status == aatc.ERR_NONFINITE
+    # the context stays usable afterwards
+    aatc.calibrate(c["k"], c["v"], c["q"], c["wl"].bits).free()
+
+
+# ----------------------------------------------------------------- encode
+@pytest.mark.parametrize("L_new,start,L_cap", [(1024, 0, 1024), (1000, 24, 1100), (1, 7, 9), (129, 0, 129)])
+def test_encode_matches_oracle_with_imported_calibration(L_new, start, L_cap):
+    c = _tiny()
+    wl, ocal = c["wl"], c["ocal"]
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=L_new, batch=2)
+    kp = torch.full((2, 1, L_cap, 11), -1, dtype=torch.int32, device="cuda")
+    vp = kp.clone()
+    aatc.encode(g, kc, vc, kp, vp, start_pos=start)
+    torch.cuda.synchronize()
+    for t, x, p in (("k", kc, kp), ("v", vc, vp)):
+        _, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
+        rec = as_u32(p)
+        compare_codes(rec[:, :, start:start + L_new], codes, pre, ocal["bits_" + t][0])
+        # rows outside the written range are untouched
+        assert np.all(rec[:, :, :start] == 0xFFFFFFFF) and np.all(rec[:, :, start + L_new:] == 0xFFFFFFFF)
+    g.check()
+
+
+def test_encode_rejects_capacity_and_flags_nonfinite():
+    c = _tiny()
+    g = aatc.import_calib(c["ocal"], 16, torch.float32)
+    kc, vc = synth.cache_inputs(c["wl"], device="cuda", seq_len=16)
+    kp = torch.zeros(1, 1, 20, 11, dtype=torch.int32, device="cuda")
+    vp = kp.clone()
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.encode(g, kc, vc, kp, vp, start_pos=5)
+    assert e.value.status == aatc.ERR_CAPACITY
+    kc[0, 0, 3, 3] = float("inf")
+    aatc.encode(g, kc, vc, kp, vp, start_pos=0)
+    with pytest.raises(aatc.AatcError) as e:
+        g.check()
+    assert e.value.status == aatc.ERR_NONFINITE
+    g.check()      # the status was cleared
+
+
+# ----------------------------------------------------------------- decode
+def _oracle_records(wl, ocal, B, L, layer=0):
+    kc, vc = synth.cache_inputs(wl, layer=layer, device="cpu", seq_len=L, batch=B)
+    kp, _, _ = oracle.encode_cache(to_np64(kc), ocal, "k")
+    vp, _, _ = oracle.encode_cache(to_np64(vc), ocal, "v")
+    return kp, vp
+
+
+@pytest.mark.parametrize("lens", [[1024], [1, 1024, 0], [127, 129, 1000]])
+def test_decode_matches_oracle_from_identical_codes(lens):
+    c = _tiny()
+    wl, ocal = c["wl"], c["ocal"]
+    B, L = len(lens), max(lens)
+    kp, vp = _oracle_records(wl, ocal, B, 1024)
+    q = synth.query_inputs(wl, device="cuda", batch=B)
+    ref = oracle.decode_attention(to_np64(q), kp, vp, ocal, seq_lens=lens)
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kpt = torch.from_numpy(kp.view(np.int32)).cuda()
+    vpt = torch.from_numpy(vp.view(np.int32)).cuda()
+    sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = aatc.decode_attention(g, q, kpt, vpt, L, seq_lens=sl).cpu().numpy()
+    for b in range(B):
+        if lens[b] == 0:
+            assert np.all(out[b] == 0)
+        else:
+            assert attn_rel_err(out[b], ref[b]) <= ATTN_RTOL, (b, attn_rel_err(out[b], ref[b]))
+    # without seq_lens every row attends L tokens
+    out2 = aatc.decode_attention(g, q, kpt, vpt, L).cpu().numpy()
+    ref2 = oracle.decode_attention(to_np64(q), kp, vp, ocal, seq_lens=[L] * B)
+    assert attn_rel_err(out2, ref2) <= ATTN_RTOL
+    g.check()
+
+
+def test_decode_workspace_and_capacity_errors():
+    c = _tiny()
+    g = aatc.import_calib(c["ocal"], 16, torch.float32)
+    q = synth.query_inputs(c["wl"], device="cuda")
+    kp = torch.zeros(1, 1, 64, 11, dtype=torch.int32, device="cuda")
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.decode_attention(g, q, kp, kp, 65)
+    assert e.value.status == aatc.ERR_CAPACITY
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.decode_attention(g, q, kp, kp, 64, workspace=ws)
+    assert e.value.status == aatc.ERR_INVALID_ARG
+    out = aatc.decode_attention(g, q, kp, kp, 0)
+    assert torch.all(out == 0)
+
+
+# ----------------------------------------------------------------- end to end
+def _end_to_end(wl, sample, layer=0, seq_len=None, bits=None, decode_step=False):
+    """GPU pipeline on the full workload vs the oracle pipeline on sampled (b, h)."""
+    bits = bits or wl.bits
+    L = seq_len or wl.seq_len
+    k, v, q = synth.calib_inputs(wl, layer=layer, device="cuda")
+    g = aatc.calibrate(k, v, q, bits)
+    ocal = _oracle_cal(k, v, q, bits)
+    gcal = g.export()
+    ties = _check_calibration(gcal, ocal, wl.n_kv_heads)
+    kc, vc = synth.cache_inputs(wl, layer=layer, device="cuda", seq_len=L)
+    L_cap = L + 1
+    kp = aatc.alloc_cache(g, wl.batch, L_cap)
+    vp = aatc.alloc_cache(g, wl.batch, L_cap)
+    aatc.encode(g, kc, vc, kp, vp)
+    Ltot = L
+    if decode_step:
+        # one decode step: encode the new token at position L, attend over L + 1
+        kn, vn = synth.cache_inputs(wl, layer=layer + 1, device="cuda", seq_len=1, batch=wl.batch)
+        aatc.encode(g, kn, vn, kp, vp, start_pos=L)
+        kc = torch.cat([kc, kn], dim=2)
+        vc = torch.cat([vc, vn], dim=2)
+        Ltot = L + 1
+    qd = synth.query_inputs(wl, layer=layer, device="cuda")
+    out = aatc.decode_attention(g, qd, kp, vp, Ltot).cpu().numpy()
+    g.check()
+    kpn, vpn = as_u32(kp), as_u32(vp)
+    G = wl.group
+    worst = 0.0
+    for (b, h) in sample:
+        if not np.array_equal(gcal["bits_k"][h], ocal["bits_k"][h]) or \
+                not np.array_equal(gcal["bits_v"][h], ocal["bits_v"][h]):
+            continue        # a reported allocation tie: codes are not comparable
+        sub = {key: (val[h:h + 1] if isinstance(val, np.ndarray) and val.ndim >= 1 and val.shape[0] == wl.n_kv_heads
+                     else val) for key, val in ocal.items()}
+        xk = to_np64(kc[b:b + 1, h:h + 1, :Ltot])
+        xv = to_np64(vc[b:b + 1, h:h + 1, :Ltot])
+        rk, ck, pk = oracle.encode_cache(xk, sub, "k", want_codes=True, want_pre=True)
+        rv, cv, pv = oracle.encode_cache(xv, sub, "v", want_codes=True, want_pre=True)
+        compare_codes(kpn[b:b + 1, h:h + 1, :Ltot], ck, pk, sub["bits_k"][0])
+        compare_codes(vpn[b:b + 1, h:h + 1, :Ltot], cv, pv, sub["bits_v"][0])
+        qq = to_np64(qd[b:b + 1, h * G:(h + 1) * G])
+        ref = oracle.decode_attention(qq, rk, rv, sub)
+        err = attn_rel_err(out[b, h * G:(h + 1) * G], ref[0])
+        worst = max(worst, err)
+        assert err <= ATTN_RTOL, (b, h, err)
+    g.free()
+    return worst, ties
+
+
+def test_end_to_end_llama_32k_with_decode_step():
+    _end_to_end(WL["llama_32k"], sample=[(0, 0), (0, 5)], decode_step=True)
+
+
+def test_end_to_end_llama_b16_8k():
+    _end_to_end(WL["llama_b16_8k"], sample=[(0, 0), (15, 7)])
+
+
+def test_end_to_end_qwen_128k():
+    _end_to_end(WL["qwen_128k"], sample=[(3, 2)])
+
+
+@pytest.mark.parametrize("bits", [2.0, 2.75, 4.0])
+def test_end_to_end_stack_layer_budgets(bits):
+    _end_to_end(WL["llama_stack"], sample=[(0, 3)], layer=31, seq_len=4096, bits=bits)
