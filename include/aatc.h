@@ -128,6 +128,29 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
  * L tokens (0 on invalid arguments). */
 size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L);
 
+/* Decode attention that allocates nothing.  The pages have no counterpart:
+ * this is a library convenience.  It computes exactly what
+ * aatc_decode_attention computes, with the same arguments except that there
+ * is no workspace: the scratch is a fixed 4 MiB array built into the library
+ * (every GPU that loads the library holds it until the process exits).  It is
+ * meant for callers that cannot hand over device memory -- e.g. an engine
+ * plugin whose memory planner has already given out all device memory, or a
+ * latency-critical path where cudaMalloc, which may synchronize the device,
+ * is not allowed.  It calls no cudaMalloc/cudaFree.
+ *   - Shapes needing more scratch than 4 MiB (aatc_decode_workspace_size)
+ *     are rejected with AATC_ERR_CAPACITY before any launch.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call on a device shares the one array and overwrites what the
+ *     previous call left there (nothing in it needs to start at zero).  Calls
+ *     that overlap on the GPU -- on different streams, or from several host
+ *     threads -- race on it: order them on one stream. */
+aatc_status aatc_decode_attention_static(const aatc_calib *calib, const void *q,
+                                         const uint32_t *k_packed, const uint32_t *v_packed,
+                                         int L_cap, const int32_t *seq_lens, int L, int B,
+                                         float *out, void *stream);
+
 /* W = u32 words per token record of one head and tensor (B/32), or -1. */
 int aatc_record_words(const aatc_calib *calib);
 
