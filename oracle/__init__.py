@@ -64,7 +64,10 @@ def lib():
             "orc_quantize": (None, [P, P, P, I, P]),
             "orc_prequant": (None, [P, P, P, I, P]),
             "orc_dequantize": (None, [P, P, P, I, P]),
+            "orc_record_order": (I, [P, I, P]),
             "orc_layout": (None, [P, I, P]),
+            "orc_cache_put": (None, [P, Lg, I, I, Lg, P]),
+            "orc_cache_get": (None, [P, Lg, I, I, Lg, P]),
             "orc_pack": (None, [P, P, I, I, P]),
             "orc_unpack": (None, [P, P, I, P]),
             "orc_unpack_rows": (None, [P, Lg, I, P, I, P]),
@@ -191,12 +194,71 @@ def dequantize(u, step, bits) -> np.ndarray:
     return c
 
 
-def layout(bits) -> np.ndarray:
-    """Record bit offset of each (channel, field width 2^s): int32 [d][4], -1 = absent."""
+def record_order(bits) -> np.ndarray:
+    """Order in which the codes of the non-pruned channels follow one another
+    in a record (see orc_record_order)."""
     bits = _i32(bits)
-    off = np.empty((bits.shape[0], 4), dtype=np.int32)
+    order = np.empty(max(1, bits.shape[0]), dtype=np.int32)
+    n = lib().orc_record_order(_p(bits), bits.shape[0], _p(order))
+    return order[:n].copy()
+
+
+def layout(bits) -> np.ndarray:
+    """Record bit offset of each channel's code: int32 [d], -1 = pruned."""
+    bits = _i32(bits)
+    off = np.empty(bits.shape[0], dtype=np.int32)
     lib().orc_layout(_p(bits), bits.shape[0], _p(off))
     return off
+
+
+KEYS, VALUES = 0, 1
+TILE = 32
+
+
+def cache_put(rec, kind: int, cache=None, start: int = 0, L_cap=None) -> np.ndarray:
+    """Place records rec [n][W] of tokens start.. into a tiled cache slab
+    (uint32 [L_cap * W]); a new zeroed slab is made if cache is None."""
+    rec = np.ascontiguousarray(np.asarray(rec, dtype=np.uint32))
+    n, W = rec.shape
+    if cache is None:
+        L_cap = L_cap if L_cap is not None else -(-(start + n) // TILE) * TILE
+        cache = np.zeros(L_cap * W, dtype=np.uint32)
+    assert cache.dtype == np.uint32 and cache.flags["C_CONTIGUOUS"]
+    assert cache.size % (TILE * W) == 0 and start + n <= cache.size // W
+    lib().orc_cache_put(_p(rec), n, W, int(kind), int(start), _p(cache))
+    return cache
+
+
+def cache_get(cache, W: int, kind: int, n: int, start: int = 0) -> np.ndarray:
+    """Records [n][W] of tokens start..start+n-1 from a tiled cache slab."""
+    cache = np.ascontiguousarray(np.asarray(cache, dtype=np.uint32)).reshape(-1)
+    assert start + n <= cache.size // W
+    rec = np.empty((n, W), dtype=np.uint32)
+    lib().orc_cache_get(_p(cache), int(n), int(W), int(kind), int(start), _p(rec))
+    return rec
+
+
+def to_cache(rec, kind: int, L_cap: int) -> np.ndarray:
+    """Records [B][H][L][W] -> tiled caches uint32 [B][H][L_cap*W]."""
+    rec = np.asarray(rec, dtype=np.uint32)
+    Bsz, H, L, W = rec.shape
+    out = np.zeros((Bsz, H, L_cap * W), dtype=np.uint32)
+    for b in range(Bsz):
+        for h in range(H):
+            cache_put(rec[b, h], kind, out[b, h])
+    return out
+
+
+def from_cache(cache, W: int, kind: int, L: int) -> np.ndarray:
+    """Tiled caches [B][H][L_cap*W] -> records [B][H][L][W]."""
+    cache = np.asarray(cache).view(np.uint32) if np.asarray(cache).dtype != np.uint32 else np.asarray(cache)
+    Bsz, H = cache.shape[:2]
+    cache = cache.reshape(Bsz, H, -1)
+    out = np.empty((Bsz, H, L, W), dtype=np.uint32)
+    for b in range(Bsz):
+        for h in range(H):
+            out[b, h] = cache_get(np.ascontiguousarray(cache[b, h]), W, kind, L)
+    return out
 
 
 def pack(u, bits) -> np.ndarray:

@@ -32,7 +32,7 @@
 
 #define ORC_MAXB 8 /* largest per-channel bit width */
 
-int orc_abi_version(void) { return 1; }
+int orc_abi_version(void) { return 2; }
 
 /* ------------------------------------------------------------------------ */
 /* Statistics  [KLT], [IMPL] covariance step                                 */
@@ -434,59 +434,144 @@ void orc_dequantize(const int *u, const float *step, const int *bits, int d, dou
 
 /* Reading (the pages fix only that every token takes the same number of
  * bits): a record of B = sum_j b_j bits, stored as B/32 little-endian u32
- * words, bit k of the record being bit k%32 of word k/32.  Each code u_j is
- * split by the binary digits of b_j into fields of width 8, 4, 2 and 1; the
- * field of width 2^s holds the bits of u_j starting at P = b_j mod 2^s (the
- * narrower fields hold the lower bits).  The record holds first every 8-bit
- * field (channels in increasing j), then every 4-bit field, then every 2-bit
- * field, then every 1-bit field.  Each field therefore starts at a multiple
- * of its own width and never crosses a byte or word boundary.
- * off[j*4 + s] = record bit offset of the width-2^s field of channel j, or -1. */
+ * words, record bit k being bit k%32 of word k/32.  Each code u_j is stored
+ * whole, in b_j consecutive record bits, least significant bit first.
+ * Pruned channels (b_j = 0) take no bits.  The channels follow one another
+ * in the order given by orc_record_order:
+ *
+ *   candidates = channels with b_j > 0;  p2 = p1 = 8;
+ *   repeat until no candidate is left:
+ *       need = 7 - p2 - p1;
+ *       pick the candidate of smallest width b >= need (ties: smallest j);
+ *       if no candidate is that wide, pick the widest (ties: smallest j);
+ *       append it;  p2 = p1;  p1 = its width.
+ *
+ * The rule tries to keep any three consecutive codes at 7 bits or more, so
+ * that few bytes of the record hold parts of more than four codes (the
+ * decoder is fastest then; correctness does not depend on it: the layout is
+ * defined by the rule above alone).
+ * order[0..n-1] receives the channel order; returns n. */
+int orc_record_order(const int *bits, int d, int *order)
+{
+    char *used = (char *)calloc((size_t)d, 1);
+    int n = 0, total = 0, p2 = 8, p1 = 8;
+    for (int j = 0; j < d; ++j) total += bits[j] > 0;
+    while (n < total) {
+        int need = 7 - p2 - p1, pick = -1, widest = -1;
+        for (int j = 0; j < d; ++j) {
+            if (used[j] || bits[j] <= 0) continue;
+            if (bits[j] >= need && (pick < 0 || bits[j] < bits[pick])) pick = j;
+            if (widest < 0 || bits[j] > bits[widest]) widest = j;
+        }
+        if (pick < 0) pick = widest;
+        used[pick] = 1;
+        order[n++] = pick;
+        p2 = p1;
+        p1 = bits[pick];
+    }
+    free(used);
+    return n;
+}
+
+/* off[j] = record bit offset of the code of channel j, -1 if b_j = 0. */
 void orc_layout(const int *bits, int d, int *off)
 {
-    int pos = 0;
-    for (int s = 3; s >= 0; --s)
-        for (int j = 0; j < d; ++j) {
-            if (bits[j] & (1 << s)) { off[j * 4 + s] = pos; pos += 1 << s; }
-            else off[j * 4 + s] = -1;
-        }
+    int *order = (int *)malloc(sizeof(int) * (d > 0 ? d : 1));
+    int n = orc_record_order(bits, d, order), pos = 0;
+    for (int j = 0; j < d; ++j) off[j] = -1;
+    for (int k = 0; k < n; ++k) { off[order[k]] = pos; pos += bits[order[k]]; }
+    free(order);
 }
 
 void orc_pack(const int *u, const int *bits, int d, int W, uint32_t *rec)
 {
-    int *off = (int *)malloc(sizeof(int) * d * 4);
+    int *off = (int *)malloc(sizeof(int) * d);
     orc_layout(bits, d, off);
     for (int w = 0; w < W; ++w) rec[w] = 0u;
-    for (int j = 0; j < d; ++j)
-        for (int s = 0; s < 4; ++s) {
-            int o = off[j * 4 + s];
-            if (o < 0) continue;
-            int width = 1 << s;
-            int P = bits[j] & (width - 1);
-            uint32_t f = ((uint32_t)u[j] >> P) & ((1u << width) - 1u);
-            for (int k = 0; k < width; ++k)     /* bit by bit: obviously right */
-                if ((f >> k) & 1u) rec[(o + k) >> 5] |= 1u << ((o + k) & 31);
-        }
+    for (int j = 0; j < d; ++j) {
+        if (off[j] < 0) continue;
+        for (int k = 0; k < bits[j]; ++k)       /* bit by bit: obviously right */
+            if (((uint32_t)u[j] >> k) & 1u) rec[(off[j] + k) >> 5] |= 1u << ((off[j] + k) & 31);
+    }
     free(off);
 }
 
 void orc_unpack(const uint32_t *rec, const int *bits, int d, int *u)
 {
-    int *off = (int *)malloc(sizeof(int) * d * 4);
+    int *off = (int *)malloc(sizeof(int) * d);
     orc_layout(bits, d, off);
     for (int j = 0; j < d; ++j) {
         uint32_t v = 0;
-        for (int s = 0; s < 4; ++s) {
-            int o = off[j * 4 + s];
-            if (o < 0) continue;
-            int width = 1 << s;
-            int P = bits[j] & (width - 1);
-            for (int k = 0; k < width; ++k)
-                if ((rec[(o + k) >> 5] >> ((o + k) & 31)) & 1u) v |= 1u << (P + k);
-        }
+        if (off[j] >= 0)
+            for (int k = 0; k < bits[j]; ++k)
+                if ((rec[(off[j] + k) >> 5] >> ((off[j] + k) & 31)) & 1u) v |= 1u << k;
         u[j] = (int)v;
     }
     free(off);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache tiling: where each token's record lives in the packed cache        */
+/* ------------------------------------------------------------------------ */
+
+/* Reading (the pages give no cache layout): the cache of one (batch row,
+ * KV head) is a run of 32-token tiles, tile t holding tokens 32t..32t+31 in
+ * 32*W consecutive words.  Within a tile, token i (0..31):
+ *
+ * keys (kind 0): half h = i/16 covers words [16W h, 16W (h+1)); inside it
+ *   record word w sits in row r = w/4 (rows of n_r = min(4, W-4r) words,
+ *   row r starting 64 r words into the half), at
+ *       64 r + (i%16 / 2) * 2 n_r + 2 (w - 4r) + (i % 2);
+ *   i.e. for each row, token pairs in order, each pair giving its row words
+ *   in order, the two tokens of a pair side by side.
+ * values (kind 1): the record is read as 2W half-words (half-word e = bits
+ *   16e..16e+15 of the record); word 16 e + i/2 of the tile holds half-word e
+ *   of token i in bits 0..15 when i is even and in bits 16..31 when i is odd.
+ *
+ * Both place every bit of every record exactly once.  Returns the word index
+ * within the tile (keys) or the word index with *half = 0/1 (values). */
+static long key_word_pos(int i, int w, int W)
+{
+    int r = w / 4, nr = W - 4 * r < 4 ? W - 4 * r : 4, ii = i % 16;
+    return (long)16 * W * (i / 16) + 64L * r + (ii / 2) * 2L * nr + 2L * (w - 4 * r) + (ii % 2);
+}
+
+/* Write the records rec[n][W] of tokens start..start+n-1 into the cache
+ * slab (words of tokens outside that range are left as they are). */
+void orc_cache_put(const uint32_t *rec, long n, int W, int kind, long start, uint32_t *cache)
+{
+    for (long a = 0; a < n; ++a) {
+        long t = start + a, base = (t / 32) * 32L * W;
+        int i = (int)(t % 32);
+        if (kind == 0) {
+            for (int w = 0; w < W; ++w) cache[base + key_word_pos(i, w, W)] = rec[a * W + w];
+        } else {
+            for (int e = 0; e < 2 * W; ++e) {
+                uint32_t hw = (rec[a * W + e / 2] >> (16 * (e % 2))) & 0xFFFFu;
+                uint32_t *p = &cache[base + 16L * e + i / 2];
+                if (i % 2) *p = (*p & 0x0000FFFFu) | (hw << 16);
+                else       *p = (*p & 0xFFFF0000u) | hw;
+            }
+        }
+    }
+}
+
+/* Read back the records of tokens start..start+n-1 from the cache slab. */
+void orc_cache_get(const uint32_t *cache, long n, int W, int kind, long start, uint32_t *rec)
+{
+    for (long a = 0; a < n; ++a) {
+        long t = start + a, base = (t / 32) * 32L * W;
+        int i = (int)(t % 32);
+        if (kind == 0) {
+            for (int w = 0; w < W; ++w) rec[a * W + w] = cache[base + key_word_pos(i, w, W)];
+        } else {
+            for (int w = 0; w < W; ++w) rec[a * W + w] = 0u;
+            for (int e = 0; e < 2 * W; ++e) {
+                uint32_t hw = (cache[base + 16L * e + i / 2] >> (16 * (i % 2))) & 0xFFFFu;
+                rec[a * W + e / 2] |= hw << (16 * (e % 2));
+            }
+        }
+    }
 }
 
 /* ------------------------------------------------------------------------ */

@@ -28,22 +28,35 @@ def test_pack_hand_built_records(golden_dir):
         assert list(oracle.unpack(rec, bits)) == codes
 
 
-def test_layout_fields_aligned_and_disjoint():
+def test_layout_codes_contiguous_and_disjoint():
+    """Every record bit belongs to exactly one code; pruned channels take none."""
     rng = np.random.default_rng(3)
     for _ in range(50):
         bits = np.sort(rng.integers(0, 9, size=128))[::-1]
         off = oracle.layout(bits)
+        order = oracle.record_order(bits)
+        assert sorted(order.tolist()) == [j for j in range(128) if bits[j] > 0]
         used = np.zeros(int(bits.sum()), dtype=int)
+        pos = 0
+        for j in order:                                     # codes follow the order, back to back
+            assert off[j] == pos
+            used[pos:pos + bits[j]] += 1
+            pos += bits[j]
+        assert np.all(off[bits == 0] == -1)
+        assert np.all(used == 1)
+
+
+def test_order_keeps_three_consecutive_codes_at_seven_bits():
+    """On the workloads' spectra the order rule leaves no byte of a record
+    holding parts of more than four codes."""
+    for lam_decay, B in ((0.95, 352), (0.93, 352), (0.9, 352), (0.95, 256), (0.95, 512)):
+        bits, _ = oracle.allocate_bits(lam_decay ** np.arange(128), B)
+        off = oracle.layout(bits)
+        per_byte = np.zeros(B // 8, dtype=int)
         for j in range(128):
-            for s in range(4):
-                if bits[j] >> s & 1:
-                    o, w = off[j, s], 1 << s
-                    assert o % w == 0                       # aligned to its width
-                    assert o // 32 == (o + w - 1) // 32     # never crosses a word
-                    used[o:o + w] += 1
-                else:
-                    assert off[j, s] == -1
-        assert np.all(used == 1)                            # every bit used exactly once
+            if bits[j]:
+                per_byte[off[j] // 8:(off[j] + bits[j] - 1) // 8 + 1] += 1
+        assert per_byte.max() <= 4, (lam_decay, B, per_byte.max())
 
 
 def test_pack_unpack_roundtrip_random():
@@ -112,3 +125,52 @@ def test_compression_ratio_arithmetic():
         assert rec.nbytes == nbytes
         assert abs(16 * 128 / (rec.nbytes * 8) - ratio) < 1e-3
     assert round(16 / 2.75, 1) == 5.8
+
+
+def test_cache_tiling_hand_positions():
+    """Positions worked out by hand from the tiling rule (W = 11 words): keys of
+    token 19 word 9 -> tile word 176 + 128 + 6 + 2 + 1 = 313; token 45 word 2
+    -> 352 + 6*8 + 4 + 1 = 405.  Values: half-word e of token 19 -> word
+    16 e + 9 (high half); of token 45 -> 352 + 16 e + 6 (high half)."""
+    W, L = 11, 64
+    rec = np.array([[(t << 8) | w for w in range(W)] for t in range(L)], dtype=np.uint32)
+    kc = oracle.cache_put(rec, oracle.KEYS)
+    assert kc.size == L * W
+    assert kc[313] == rec[19, 9] and kc[405] == rec[45, 2]
+    assert kc[0] == rec[0, 0] and kc[1] == rec[1, 0] and kc[2] == rec[0, 1]
+    vc = oracle.cache_put(rec, oracle.VALUES)
+    for e in range(2 * W):
+        hw = lambda t: (int(rec[t, e // 2]) >> (16 * (e % 2))) & 0xFFFF  # noqa: E731
+        assert int(vc[16 * e + 9]) >> 16 == hw(19)
+        assert int(vc[352 + 16 * e + 6]) >> 16 == hw(45)
+        assert int(vc[16 * e]) & 0xFFFF == hw(0) and int(vc[16 * e]) >> 16 == hw(1)
+
+
+def test_cache_tiling_is_a_permutation_and_round_trips():
+    rng = np.random.default_rng(7)
+    for W in (8, 11, 16, 5, 1):
+        L = 96
+        rec = rng.integers(0, 2 ** 32, size=(L, W), dtype=np.uint64).astype(np.uint32)
+        for kind in (oracle.KEYS, oracle.VALUES):
+            c = oracle.cache_put(rec, kind)
+            assert np.array_equal(oracle.cache_get(c, W, kind, L), rec)
+            # each cache bit comes from exactly one record bit: place one-hot records
+            seen = np.zeros(L * W * 32, dtype=int)
+            for t in (0, 1, 15, 16, 31, 32, 63, 95):
+                for w in range(W):
+                    for k in (0, 13, 16, 31):
+                        one = np.zeros((L, W), dtype=np.uint32)
+                        one[t, w] = np.uint32(1 << k)
+                        cc = oracle.cache_put(one, kind)
+                        nz = np.flatnonzero(cc)
+                        assert nz.size == 1
+                        bit = nz[0] * 32 + int(np.log2(int(cc[nz[0]])))
+                        seen[bit] += 1
+            assert seen.max() == 1
+        # partial writes leave other tokens alone
+        c = oracle.cache_put(rec, oracle.VALUES)
+        new = rng.integers(0, 2 ** 32, size=(3, W), dtype=np.uint64).astype(np.uint32)
+        oracle.cache_put(new, oracle.VALUES, cache=c, start=33)
+        back = oracle.cache_get(c, W, oracle.VALUES, L)
+        assert np.array_equal(back[33:36], new)
+        assert np.array_equal(back[:33], rec[:33]) and np.array_equal(back[36:], rec[36:])
