@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 from quantized_attention_kv_b300 import synth  # noqa: E402
 
-DECODE_KERNELS_PER_CALL = 3     # query prep, split-K attention, combine
+DECODE_KERNELS_PER_CALL = 2     # query prep + fused split-K attention/merge (fast path)
 ENCODE_KERNELS_PER_CALL = 1
 
 

@@ -54,7 +54,8 @@ typedef enum {
     AATC_ERR_CUDA = 3,           /* a CUDA runtime call failed */
     AATC_ERR_NO_CONVERGENCE = 4, /* Jacobi did not converge within jacobi_max_sweeps */
     AATC_ERR_NONFINITE = 5,      /* NaN/Inf in calibration or cache input */
-    AATC_ERR_CAPACITY = 6        /* start_pos + L_new > L_cap, or L > L_cap */
+    AATC_ERR_CAPACITY = 6,       /* start_pos + L_new > L_cap, or L > L_cap */
+    AATC_ERR_TIMEOUT = 7         /* a bounded wait inside a kernel gave up (reported by aatc_check) */
 } aatc_status;
 
 typedef enum { AATC_F32 = 0, AATC_BF16 = 1 } aatc_dtype;
@@ -88,26 +89,49 @@ typedef struct {
 aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const void *v_cal,
                            const void *q_cal, aatc_calib **out, void *stream);
 
+/* Packed cache layout ([NOVA] fixed per-token bit count; the layout itself
+ * is this library's reading -- the pages give none).
+ *
+ * Record: every token of every (KV head, tensor) takes exactly W = B/32
+ * little-endian u32 words, record bit k = bit k%32 of word k/32.  The code
+ * u_j of each channel with b_j > 0 is stored whole, least significant bit
+ * first, in b_j consecutive record bits; pruned channels (b_j = 0) take no
+ * bits.  The channels follow one another in this order: start with
+ * p2 = p1 = 8; repeatedly take the narrowest remaining channel whose width is
+ * at least 7 - p2 - p1 (or the widest remaining one if none is that wide;
+ * ties to the lower channel index), then p2 = p1, p1 = its width.
+ *
+ * Cache: the cache of one (batch row b, KV head h) is L_cap*W words starting
+ * at word (b*H_kv + h)*L_cap*W, L_cap a multiple of 32, made of 32-token
+ * tiles (tile t = tokens 32t..32t+31, words 32*W*t ..).  Within a tile,
+ * token i (0..31):
+ *   keys:   record word w is tile word
+ *             16*W*(i/16) + 64*r + ((i%16)/2)*2*n_r + 2*(w-4r) + i%2,
+ *           r = w/4, n_r = min(4, W-4r);
+ *   values: half-word e of the record (bits 16e..16e+15, e < 2W) is bits
+ *           16*(i%2)..16*(i%2)+15 of tile word 16*e + i/2.
+ * Every cache bit belongs to exactly one record bit. */
+
 /* Encode ([KLT], [IMPL], [NOVA] fixed per-token bit count).
  * k, v: device [B][H_kv][L_new][128] of the handle's dtype, the keys/values of
  * token positions start_pos .. start_pos+L_new-1.  For each row x:
  * c = T (x - mu); u_j = clamp(rint(c_j/Delta_j + (2^b_j - 1)/2), 0, 2^b_j - 1)
  * (round half to even, decided on an fp32 value); the codes are packed into
- * a record of W = B/32 little-endian u32 words: the code of channel j is split
- * by the binary digits of b_j into fields of width 8/4/2/1 (narrower fields
- * hold the lower bits); the record holds all 8-bit fields, then 4-bit, 2-bit,
- * 1-bit fields, channels ascending, LSB first.
- * k_packed, v_packed: device [B][H_kv][L_cap][W] u32; rows start_pos ..
- * start_pos+L_new-1 are written, others untouched.  L_new = 0 is a no-op.
- * Errors: CAPACITY if start_pos + L_new > L_cap.  Non-finite inputs set the
- * handle's NONFINITE status (codes of such rows are unspecified). */
+ * the token's record and placed in the cache as described above.
+ * k_packed, v_packed: device u32 caches of B*H_kv*L_cap*W words (layout
+ * above); L_cap must be a multiple of 32.  Only the bits of tokens
+ * start_pos .. start_pos+L_new-1 are written (value words are shared by two
+ * tokens and written 16 bits at a time).  L_new = 0 is a no-op.
+ * Errors: CAPACITY if start_pos + L_new > L_cap; INVALID_ARG if L_cap is not a
+ * multiple of 32.  Non-finite inputs set the handle's NONFINITE status (codes
+ * of such rows are unspecified). */
 aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, int B, int L_new,
                         int start_pos, int L_cap, uint32_t *k_packed, uint32_t *v_packed,
                         void *stream);
 
 /* Decode attention over the packed cache ([ATT], [NOVA] bandwidth-bound decode).
  * q: device [B][H_q][128] of the handle's dtype.  k_packed, v_packed: device
- * [B][H_kv][L_cap][W] as written by aatc_encode.  seq_lens: device int32 [B]
+ * caches as written by aatc_encode (L_cap a multiple of 32).  seq_lens: device int32 [B]
  * (tokens 0..seq_lens[b]-1 of row b are attended; each in 0..L) or NULL
  * (every row attends L tokens).  out: device fp32 [B][H_q][128],
  *   out[b][h] = sum_i softmax_i(q . k_hat_i / sqrt(128)) v_hat_i,
@@ -117,8 +141,11 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
  * accumulated in the transform domain and the inverse transform Uv is
  * applied once per head.  workspace: device scratch of at least
  * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned, contents
- * need not be initialized.  Errors: CAPACITY if L > L_cap; INVALID_ARG if the
- * workspace is too small. */
+ * need not be initialized (the call sets up what it needs, on `stream`);
+ * calls that share a workspace must be ordered on one stream.  Up to three
+ * kernels are launched, the second with programmatic dependent launch.
+ * Errors: CAPACITY if L > L_cap; INVALID_ARG if the workspace is too small or
+ * L_cap is not a multiple of 32. */
 aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
                                   const uint32_t *k_packed, const uint32_t *v_packed, int L_cap,
                                   const int32_t *seq_lens, int L, int B, float *out,

@@ -18,8 +18,10 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libaatc.so")
 
-OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_CONVERGENCE, ERR_NONFINITE, ERR_CAPACITY = range(7)
-STATUS_NAMES = ["OK", "INVALID_ARG", "UNSUPPORTED", "CUDA", "NO_CONVERGENCE", "NONFINITE", "CAPACITY"]
+(OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CUDA, ERR_NO_CONVERGENCE, ERR_NONFINITE, ERR_CAPACITY,
+ ERR_TIMEOUT) = range(8)
+STATUS_NAMES = ["OK", "INVALID_ARG", "UNSUPPORTED", "CUDA", "NO_CONVERGENCE", "NONFINITE", "CAPACITY", "TIMEOUT"]
+TILE = 32      # cache tiles hold 32 tokens; L_cap is a multiple of this
 F32, BF16 = 0, 1
 D = 128
 BLOB_MAGIC, BLOB_VERSION = 0x43544141, 1
@@ -32,7 +34,7 @@ EXPORTED = ["aatc_calibrate", "aatc_encode", "aatc_decode_attention", "aatc_deco
 class AatcError(RuntimeError):
     def __init__(self, status: int, msg: str):
         self.status = status
-        super().__init__("%s: %s" % (STATUS_NAMES[status] if 0 <= status < 7 else status, msg))
+        super().__init__("%s: %s" % (STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else status, msg))
 
 
 class CalibDesc(ctypes.Structure):
@@ -204,15 +206,35 @@ def import_calib(cal: dict, n_q_heads: int, dtype: torch.dtype) -> Calib:
     return Calib(h, dtype, np.asarray(cal["mu_k"]).shape[0], n_q_heads)
 
 
-def alloc_cache(calib: Calib, B: int, L_cap: int, device="cuda") -> torch.Tensor:
-    """An empty packed cache [B][H_kv][L_cap][W] of u32 words (stored as int32)."""
-    return torch.zeros(B, calib.n_kv_heads, L_cap, calib.W, dtype=torch.int32, device=device)
+def cache_capacity(L: int) -> int:
+    """Smallest valid L_cap (a multiple of 32) holding L tokens."""
+    return max(TILE, -(-int(L) // TILE) * TILE)
+
+
+def alloc_cache(calib: Calib, B: int, L: int, device="cuda") -> torch.Tensor:
+    """A zeroed packed cache for B rows of up to L tokens: int32 [B][H_kv][L_cap][W]
+    words with L_cap = cache_capacity(L), in the tiled layout of aatc_encode
+    (the [L_cap][W] axes are the slab's size, not one record per row)."""
+    return torch.zeros(B, calib.n_kv_heads, cache_capacity(L), calib.W, dtype=torch.int32, device=device)
+
+
+def _check_cache(calib: Calib, B: int, *caches: torch.Tensor) -> int:
+    """Caches must be [B][H_kv][L_cap][W] (the tiled slab of aatc_encode); returns L_cap."""
+    for c in caches:
+        if c.dim() != 4 or tuple(c.shape[:2]) != (B, calib.n_kv_heads) or c.shape[3] != calib.W or \
+                c.shape[2] % TILE or c.element_size() != 4:
+            raise ValueError("packed caches must be 4-byte [B=%d][H_kv=%d][L_cap (multiple of %d)][W=%d], got %s"
+                             % (B, calib.n_kv_heads, TILE, calib.W, tuple(c.shape)))
+    if len({tuple(c.shape) for c in caches}) != 1:
+        raise ValueError("key and value caches must have the same shape")
+    return caches[0].shape[2]
 
 
 def encode(calib: Calib, k: torch.Tensor, v: torch.Tensor, k_packed: torch.Tensor, v_packed: torch.Tensor,
            start_pos: int = 0, stream=None):
-    """aatc_encode: k, v [B][H_kv][L_new][128] into rows start_pos.. of the packed caches."""
+    """aatc_encode: k, v [B][H_kv][L_new][128] into tokens start_pos.. of the packed caches."""
     B, H, L_new, _ = k.shape
+    _check_cache(calib, B, k_packed, v_packed)
     _check(lib().aatc_encode(calib.handle, _ptr(k), _ptr(v), B, L_new, int(start_pos), k_packed.shape[2],
                              _ptr(k_packed), _ptr(v_packed), _stream(stream)))
 
@@ -226,6 +248,7 @@ def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_pa
                      workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """aatc_decode_attention: q [B][H_q][128] -> fp32 [B][H_q][128]."""
     B = q.shape[0]
+    _check_cache(calib, B, k_packed, v_packed)
     if out is None:
         out = torch.empty(B, calib.n_q_heads, D, dtype=torch.float32, device=q.device)
     need = workspace_size(calib, B, L)

@@ -21,7 +21,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Sizes of the arena pieces, in the order they are carved.
 struct Layout {
-    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, total;
+    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, total;
 };
 
 Layout layout_for(int H)
@@ -34,7 +34,9 @@ Layout layout_for(int H)
     L.f32_vec = up((size_t)H * D * sizeof(float));
     L.f32_mat = up((size_t)H * D * D * sizeof(float));
     L.tabs = up((size_t)H * 2 * sizeof(CodecTables));
-    L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs + 256;
+    L.plans = up((size_t)H * 2 * sizeof(HeadPlan));
+    L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
+              L.plans + 256;
     return L;
 }
 
@@ -73,9 +75,10 @@ aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib 
     h->muv32 = (float *)take(L.f32_vec);
     h->Tk32 = (float *)take(L.f32_mat);
     h->Tv32 = (float *)take(L.f32_mat);
-    h->Ak32 = (float *)take(L.f32_mat);
-    h->Uv32 = (float *)take(L.f32_mat);
+    h->AkT32 = (float *)take(L.f32_mat);
+    h->UvT32 = (float *)take(L.f32_mat);
     h->tab = (CodecTables *)take(L.tabs);
+    h->plan = (HeadPlan *)take(L.plans);
     h->status = (uint32_t *)take(256);
     e = cudaMemset(h->status, 0, sizeof(uint32_t));
     if (e != cudaSuccess) { cudaFree(h->arena); delete h; return aatc_cuda_fail(e, "cudaMemset"); }
@@ -88,6 +91,8 @@ aatc_status status_from_device(uint32_t st)
     if (st & AATC_DEV_NONFINITE) return aatc_fail(AATC_ERR_NONFINITE, "non-finite value in an input");
     if (st & AATC_DEV_NO_CONVERGENCE)
         return aatc_fail(AATC_ERR_NO_CONVERGENCE, "Jacobi eigensolver did not converge");
+    if (st & AATC_DEV_TIMEOUT)
+        return aatc_fail(AATC_ERR_TIMEOUT, "a kernel gave up waiting for its own copies; results are invalid");
     return AATC_OK;
 }
 
@@ -107,6 +112,19 @@ size_t blob_bytes(int H)
     const size_t v = (size_t)H * D, m = (size_t)H * D * D;
     return 8 * sizeof(int32_t) + (2 * v + 5 * m + 3 * v) * sizeof(double) + 2 * v * sizeof(int32_t) +
            2 * v * sizeof(float);
+}
+
+// Copy the bit allocations back and build the record layouts (one sync).
+aatc_status build_plans_from_device(aatc_calib *h)
+{
+    const size_t n = (size_t)h->Hkv * D;
+    int32_t *bk = new (std::nothrow) int32_t[2 * n];
+    if (!bk) return aatc_fail(AATC_ERR_INVALID_ARG, "out of host memory");
+    cudaError_t e = cudaMemcpy(bk, h->bits_k, n * sizeof(int32_t), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemcpy(bk + n, h->bits_v, n * sizeof(int32_t), cudaMemcpyDeviceToHost);
+    aatc_status st = e == cudaSuccess ? plan_build(h, bk, bk + n) : aatc_cuda_fail(e, "cudaMemcpy(bits)");
+    delete[] bk;
+    return st;
 }
 
 }  // namespace
@@ -170,6 +188,7 @@ aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const
     }
     cudaFree(work);
     if (st == AATC_OK) st = status_from_device(dev);
+    if (st == AATC_OK) st = build_plans_from_device(h);
     if (st != AATC_OK) { aatc_free(h); return st; }
     *out = h;
     return AATC_OK;
@@ -183,6 +202,7 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
     if (B < 0 || L_new < 0 || start_pos < 0 || L_cap < 0)
         return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
     if (B > 32767 || L_cap > (1 << 28)) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
+    if (L_cap % 32) return aatc_fail(AATC_ERR_INVALID_ARG, "L_cap = %d is not a multiple of 32", L_cap);
     if ((long)start_pos + L_new > L_cap)
         return aatc_fail(AATC_ERR_CAPACITY, "start_pos + L_new = %ld exceeds L_cap = %d",
                          (long)start_pos + L_new, L_cap);
@@ -207,6 +227,7 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const 
     if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
     if (B < 0 || L < 0 || L_cap < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
     if (B > 65535 || L_cap > (1 << 28)) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
+    if (L_cap % 32) return aatc_fail(AATC_ERR_INVALID_ARG, "L_cap = %d is not a multiple of 32", L_cap);
     if (L > L_cap) return aatc_fail(AATC_ERR_CAPACITY, "L = %d exceeds L_cap = %d", L, L_cap);
     if (B == 0) return AATC_OK;
     if (!q || !out || !aligned16(q) || !aligned16(out))
@@ -296,6 +317,7 @@ aatc_status aatc_import_calib(const void *host_buf, size_t bytes, aatc_calib **o
         p += sz[i];
     }
     st = calib_derive(h, 0);
+    if (st == AATC_OK) st = plan_build(h, bk, bv);
     if (st == AATC_OK) {
         cudaError_t e = cudaDeviceSynchronize();
         if (e != cudaSuccess) st = aatc_cuda_fail(e, "import");

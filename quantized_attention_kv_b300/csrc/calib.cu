@@ -414,25 +414,11 @@ __global__ void k_tables(const int32_t *__restrict__ bits_k, const int32_t *__re
                          const double *__restrict__ mu_k, const double *__restrict__ mu_v,
                          CodecTables *__restrict__ tab, float *__restrict__ bk32, float *__restrict__ bv32)
 {
-    __shared__ int bs[D];
     const int h = blockIdx.x, tensor = blockIdx.y, j = threadIdx.x;
     const int32_t *bits = (tensor == 0 ? bits_k : bits_v) + h * D;
     const float *step = (tensor == 0 ? step_k : step_v) + h * D;
     CodecTables &T = tab[h * 2 + tensor];
     const int b = bits[j];
-    bs[j] = b;
-    __syncthreads();
-    int pos = 0;
-    for (int s = 3; s >= 0; --s) {
-        int before = 0, total = 0;
-        for (int k = 0; k < D; ++k) {
-            int has = (bs[k] >> s) & 1;
-            total += has;
-            before += has && k < j;
-        }
-        T.off[j][s] = ((b >> s) & 1) ? (int16_t)(pos + before * (1 << s)) : (int16_t)-1;
-        pos += total * (1 << s);
-    }
     const float st = step[j];
     T.bits[j] = (uint8_t)b;
     T.step[j] = st;
@@ -444,6 +430,13 @@ __global__ void k_tables(const int32_t *__restrict__ bits_k, const int32_t *__re
     double acc = 0.0;
     for (int k = 0; k < D; ++k) acc += Tm[j * D + k] * mu[k];
     (tensor == 0 ? bk32 : bv32)[h * D + j] = (float)acc;
+}
+
+// y[h][c][r] = x[h][r][c] for H square [D][D] blocks (fp64 -> fp32, transposed)
+__global__ void k_to_f32_t(const double *__restrict__ x, float *__restrict__ y)
+{
+    const int h = blockIdx.y, r = blockIdx.x, c = threadIdx.x;
+    y[((size_t)h * D + c) * D + r] = (float)x[((size_t)h * D + r) * D + c];
 }
 
 __global__ void k_to_f32(const double *__restrict__ x, float *__restrict__ y, size_t n)
@@ -542,8 +535,8 @@ aatc_status calib_derive(aatc_calib *h, cudaStream_t s)
     const int blocks = (int)((n + 255) / 256);
     k_to_f32<<<blocks, 256, 0, s>>>(h->T_k, h->Tk32, n);
     k_to_f32<<<blocks, 256, 0, s>>>(h->T_v, h->Tv32, n);
-    k_to_f32<<<blocks, 256, 0, s>>>(h->A_k, h->Ak32, n);
-    k_to_f32<<<blocks, 256, 0, s>>>(h->U_v, h->Uv32, n);
+    k_to_f32_t<<<dim3(D, H), D, 0, s>>>(h->A_k, h->AkT32);
+    k_to_f32_t<<<dim3(D, H), D, 0, s>>>(h->U_v, h->UvT32);
     k_to_f32<<<(H * D + 255) / 256, 256, 0, s>>>(h->mu_v, h->muv32, (size_t)H * D);
     k_tables<<<dim3(H, 2), D, 0, s>>>(h->bits_k, h->bits_v, h->step_k, h->step_v, h->T_k, h->T_v,
                                       h->mu_k, h->mu_v, h->tab, h->bk32, h->bv32);

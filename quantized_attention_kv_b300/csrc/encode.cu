@@ -5,6 +5,12 @@
 // "End-to-End Implementation" (rotate into the calibrated basis, quantize each
 // channel at its allocated width) and "Spend Bits Where Queries Look",
 // Abstract (fixed per-token bit count).
+//
+// Cache tiling (per batch row and KV head, 32-token tiles of 32*W words):
+// keys: token i of a tile, record word w -> half i/16 (16*W words each), row
+// r = w/4 (n_r = min(4, W-4r) words, row r at 64*r), word
+//     64 r + ((i%16)/2) * 2 n_r + 2 (w - 4r) + i%2;
+// values: half-word e of token i -> bits 16*(i%2).. of word 16 e + i/2.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -22,17 +28,24 @@ __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162flo
 // v = c * (1/Delta) + mid, u = clamp(rint(v), 0, 2^b - 1), then the fields of
 // u are ORed into the token's record in shared memory and the record is
 // written to rows start_pos + token of the packed cache.
+__device__ __forceinline__ int key_word_pos(int i, int w, int W)
+{
+    const int r = w >> 2, nr = min(4, W - 4 * r), ii = i & 15;
+    return 16 * W * (i >> 4) + 64 * r + (ii >> 1) * 2 * nr + 2 * (w - 4 * r) + (ii & 1);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, int L_cap, int Hkv,
     int W, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
-    const float *__restrict__ bv, const CodecTables *__restrict__ tabs, uint32_t *__restrict__ kp,
-    uint32_t *__restrict__ vp, uint32_t *status)
+    const float *__restrict__ bv, const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
+    uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
 {
     extern __shared__ float sm[];
     float *Ts = sm;                          // [D][D] transposed: Ts[kk][j] = T[j][kk]
     float *xs = Ts + D * D;                  // [ENC_TILE][D+1]
     uint32_t *rec = (uint32_t *)(xs + ENC_TILE * (D + 1));   // [ENC_TILE][W+1]
+    __shared__ int16_t offs[D];
     const int tile = blockIdx.x, h = blockIdx.y;
     const int b = blockIdx.z >> 1, tensor = blockIdx.z & 1;
     const int t = threadIdx.x;
@@ -40,6 +53,7 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     const float *Tm = (tensor == 0 ? Tk : Tv) + (size_t)h * D * D;
     const float *bias = (tensor == 0 ? bk : bv) + h * D;
     const CodecTables &tb = tabs[h * 2 + tensor];
+    offs[t] = plans[h * 2 + tensor].off[t];
     uint32_t *out = (tensor == 0 ? kp : vp) + ((size_t)b * Hkv + h) * L_cap * W;
 
     for (int e = t; e < D * D; e += ENC_TILE) {
@@ -86,20 +100,28 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
             float vq = fmaf(c, tb.inv_step[j], tb.mid[j]);
             vq = fminf(fmaxf(rintf(vq), 0.f), tb.top[j]);
             const uint32_t u = (uint32_t)vq;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-                const int o = tb.off[j][s];
-                if (o < 0) continue;
-                const int width = 1 << s;
-                const uint32_t f = (u >> (bj & (width - 1))) & ((1u << width) - 1u);
-                myrec[o >> 5] |= f << (o & 31);
-            }
+            const int o = offs[j], sh = o & 31;
+            myrec[o >> 5] |= u << sh;
+            if (sh + bj > 32) myrec[(o >> 5) + 1] |= u >> (32 - sh);
         }
     }
     __syncthreads();
-    // coalesced copy of the tile's records (rows start_pos + tok0 ..)
-    uint32_t *dst = out + (size_t)(start_pos + tok0) * W;
-    for (int e = t; e < ntok * W; e += ENC_TILE) dst[e] = rec[(e / W) * (W + 1) + (e % W)];
+    // scatter the records into the tiled cache (positions start_pos + tok0 + i)
+    const int p0 = start_pos + tok0;
+    if (tensor == 0) {
+        for (int e = t; e < ntok * W; e += ENC_TILE) {
+            const int i = e / W, w = e % W, pos = p0 + i;
+            out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, w, W)] = rec[i * (W + 1) + w];
+        }
+    } else {
+        uint16_t *out16 = (uint16_t *)out;
+        for (int e = t; e < ntok * 2 * W; e += ENC_TILE) {
+            const int i = e / (2 * W), q = e % (2 * W), pos = p0 + i;
+            const uint32_t wv = rec[i * (W + 1) + (q >> 1)];
+            const size_t word = (size_t)(pos >> 5) * 32 * W + 16 * q + ((pos & 31) >> 1);
+            out16[2 * word + (pos & 1)] = (uint16_t)(wv >> (16 * (q & 1)));
+        }
+    }
 }
 
 }  // namespace
@@ -116,13 +138,13 @@ aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B,
         AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<grid, ENC_TILE, smem, s>>>((const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, L_new,
                                           start_pos, L_cap, h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32,
-                                          h->bv32, h->tab, kp, vp, h->status);
+                                          h->bv32, h->tab, h->plan, kp, vp, h->status);
     } else {
         auto kern = k_encode_simple<float>;
         AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<grid, ENC_TILE, smem, s>>>((const float *)k, (const float *)v, L_new, start_pos, L_cap,
-                                          h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, kp,
-                                          vp, h->status);
+                                          h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, h->plan,
+                                          kp, vp, h->status);
     }
     AATC_CUDA(cudaGetLastError());
     return AATC_OK;

@@ -14,6 +14,7 @@
 enum : uint32_t {
     AATC_DEV_NONFINITE = 1u,
     AATC_DEV_NO_CONVERGENCE = 2u,
+    AATC_DEV_TIMEOUT = 4u,        // a bounded wait inside a kernel gave up
 };
 
 // Per (KV head, tensor) codec tables, fp32/int, derived from bits and steps.
@@ -23,8 +24,29 @@ struct CodecTables {
     float mid[AATC_D];        // (2^b_j - 1) / 2, 0 if b_j = 0
     float top[AATC_D];        // 2^b_j - 1
     float step[AATC_D];       // Delta_j
-    int16_t off[AATC_D][4];   // record bit offset of the width-2^s field, -1 if absent
     uint8_t bits[AATC_D];     // b_j
+};
+
+// Record layout of one (head, tensor), computed on the host from the bits
+// (plan.cu).  Codes are stored whole, LSB first, channels in the order of
+// the record-order rule; off[j] is the record bit offset of channel j.
+//
+// For the fast decoder every byte of the record is cut into at most
+// AATC_PIECES pieces (the parts of codes lying in it).  A 32-bit word x of
+// a record (keys) or a pair word holding the same half-word of two tokens
+// (values) is read through 8 masks: slot k < 4 is x & mask[k] (piece k of
+// bytes 0 and 2 of x, or of byte 0 of both half-words), slot k >= 4 is
+// (x >> 8) & mask[k] (piece k-4 of bytes 1 and 3).  Each masked 16-bit half
+// is a piece value times 2^p, p its bit position in its byte, and read as an
+// fp16 it equals piece * 2^(p-24) exactly (exponent field 0).
+#define AATC_PIECES 4
+#define AATC_PLAN_SLOTS 32    // record words (keys) or half-words (values) covered
+struct HeadPlan {
+    int16_t off[AATC_D];                  // record bit offset of each code, -1 if pruned
+    int32_t max_pieces;                   // largest number of pieces in one byte
+    uint32_t mask[AATC_PLAN_SLOTS][8];    // keys: per record word; values: per half-word
+    int8_t ch[AATC_PLAN_SLOTS][8][2];     // channel of the piece in the low/high half, -1 = none
+    int8_t ex[AATC_PLAN_SLOTS][8][2];     // code bit offset of the piece minus p
 };
 
 struct aatc_calib {
@@ -40,10 +62,12 @@ struct aatc_calib {
     // fp32 operands of the encode / decode kernels
     float *Tk32, *Tv32;       // [H][d][d] transform rows (coefficient i = row i . x)
     float *bk32, *bv32;       // [H][d] T mu
-    float *Ak32;              // [H][d][d] Tk^{-T}: q' = A_k q
-    float *Uv32;              // [H][d][d] inverse value transform
+    float *AkT32;             // [H][d][d] (Tk^{-T})^T: q'_j = sum_k AkT32[k][j] q_k
+    float *UvT32;             // [H][d][d] Uv^T: o_j = sum_k UvT32[k][j] c_k
     float *muv32;             // [H][d]
     CodecTables *tab;         // [H][2]
+    HeadPlan *plan;           // [H][2] record layout and decode masks
+    bool fast_layout;         // every record byte of every head holds <= AATC_PIECES pieces
     uint32_t *status;         // device status word
 };
 
@@ -65,6 +89,13 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
                       int N, int max_sweeps, void *work, cudaStream_t s);
 // Rebuild the fp32 operands and codec tables from the fp64 results.
 aatc_status calib_derive(aatc_calib *h, cudaStream_t s);
+
+// ---- record layout (plan.cu) ----
+// Build the plans of every head from host copies of the bits ([H][d] each)
+// and upload them to h->plan.  Synchronous.
+aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits_v);
+// Host-side plan of one bit allocation (exposed for the ABI tests).
+void plan_one(const int32_t *bits, int W, HeadPlan *out);
 
 // ---- encode (encode.cu) ----
 aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,

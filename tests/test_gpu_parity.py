@@ -95,34 +95,81 @@ def test_calibration_errors_reported():
 
 
 # ----------------------------------------------------------------- encode
-@pytest.mark.parametrize("L_new,start,L_cap", [(1024, 0, 1024), (1000, 24, 1100), (1, 7, 9), (129, 0, 129)])
+def _records(cache_t, W, kind, L, start=0):
+    """Records [B][H][L][W] of tokens start.. read from a GPU cache through the oracle's tiling."""
+    c = as_u32(cache_t)
+    Bsz, H = c.shape[:2]
+    c = c.reshape(Bsz, H, -1)
+    out = np.empty((Bsz, H, L, W), dtype=np.uint32)
+    for b in range(Bsz):
+        for h in range(H):
+            out[b, h] = oracle.cache_get(np.ascontiguousarray(c[b, h]), W, kind, L, start)
+    return out
+
+
+@pytest.mark.parametrize("L_new,start,L_cap", [(1024, 0, 1024), (1000, 24, 1056), (1, 7, 32), (129, 0, 160),
+                                               (45, 31, 96)])
 def test_encode_matches_oracle_with_imported_calibration(L_new, start, L_cap):
     c = _tiny()
     wl, ocal = c["wl"], c["ocal"]
+    W = ocal["W"]
     g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
     kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=L_new, batch=2)
-    kp = torch.full((2, 1, L_cap, 11), -1, dtype=torch.int32, device="cuda")
+    kp = torch.full((2, 1, L_cap, W), -1, dtype=torch.int32, device="cuda")
     vp = kp.clone()
     aatc.encode(g, kc, vc, kp, vp, start_pos=start)
     torch.cuda.synchronize()
-    for t, x, p in (("k", kc, kp), ("v", vc, vp)):
+    for t, kind, x, p in (("k", oracle.KEYS, kc, kp), ("v", oracle.VALUES, vc, vp)):
         _, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
-        rec = as_u32(p)
-        compare_codes(rec[:, :, start:start + L_new], codes, pre, ocal["bits_" + t][0])
-        # rows outside the written range are untouched
-        assert np.all(rec[:, :, :start] == 0xFFFFFFFF) and np.all(rec[:, :, start + L_new:] == 0xFFFFFFFF)
+        compare_codes(_records(p, W, kind, L_new, start), codes, pre, ocal["bits_" + t][0])
+        # every bit of every other token is untouched: overwrite the written
+        # tokens with ones through the oracle's tiling and expect all ones
+        cc = as_u32(p).reshape(2, -1).copy()
+        ones = np.full((L_new, W), 0xFFFFFFFF, dtype=np.uint32)
+        for b in range(2):
+            oracle.cache_put(ones, kind, cache=cc[b], start=start)
+        assert np.all(cc == 0xFFFFFFFF), t
     g.check()
+
+
+def test_encode_writes_the_oracle_cache_bit_for_bit():
+    """Away from rounding ties the whole tiled cache equals the oracle's."""
+    c = _tiny()
+    wl, ocal = c["wl"], c["ocal"]
+    W = ocal["W"]
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=200, batch=1)
+    kp = aatc.alloc_cache(g, 1, 200)
+    vp = aatc.alloc_cache(g, 1, 200)
+    aatc.encode(g, kc, vc, kp, vp)
+    for t, kind, x, p in (("k", oracle.KEYS, kc, kp), ("v", oracle.VALUES, vc, vp)):
+        rec, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
+        ref = oracle.to_cache(rec, kind, p.shape[2])
+        got = as_u32(p).reshape(ref.shape)
+        near_tie = np.abs(pre - np.floor(pre) - 0.5) < 1e-3
+        clean = ~near_tie.any(axis=-1)[0, 0]          # tokens with no near-tie code
+        gr = oracle.from_cache(got, W, kind, 200)[0, 0]
+        assert np.array_equal(gr[clean], rec[0, 0][clean])
+        if clean.all():
+            assert np.array_equal(got, ref)
 
 
 def test_encode_rejects_capacity_and_flags_nonfinite():
     c = _tiny()
     g = aatc.import_calib(c["ocal"], 16, torch.float32)
     kc, vc = synth.cache_inputs(c["wl"], device="cuda", seq_len=16)
-    kp = torch.zeros(1, 1, 20, 11, dtype=torch.int32, device="cuda")
+    kp = torch.zeros(1, 1, 32, 11, dtype=torch.int32, device="cuda")
     vp = kp.clone()
     with pytest.raises(aatc.AatcError) as e:
-        aatc.encode(g, kc, vc, kp, vp, start_pos=5)
+        aatc.encode(g, kc, vc, kp, vp, start_pos=20)
     assert e.value.status == aatc.ERR_CAPACITY
+    bad = torch.zeros(1, 1, 20, 11, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):                 # the binding checks the cache shape
+        aatc.encode(g, kc, vc, bad, bad, start_pos=0)
+    import ctypes
+    st = aatc.lib().aatc_encode(g.handle, ctypes.c_void_p(kc.data_ptr()), ctypes.c_void_p(vc.data_ptr()), 1, 16, 0,
+                                20, ctypes.c_void_p(bad.data_ptr()), ctypes.c_void_p(bad.data_ptr()), None)
+    assert st == aatc.ERR_INVALID_ARG and "multiple of 32" in aatc.last_error()
     kc[0, 0, 3, 3] = float("inf")
     aatc.encode(g, kc, vc, kp, vp, start_pos=0)
     with pytest.raises(aatc.AatcError) as e:
@@ -139,7 +186,13 @@ def _oracle_records(wl, ocal, B, L, layer=0):
     return kp, vp
 
 
-@pytest.mark.parametrize("lens", [[1024], [1, 1024, 0], [127, 129, 1000]])
+def _upload(rec, kind, L_cap):
+    Bsz, H, _, W = rec.shape
+    c = oracle.to_cache(rec, kind, L_cap).view(np.int32).reshape(Bsz, H, L_cap, W)
+    return torch.from_numpy(c).cuda()
+
+
+@pytest.mark.parametrize("lens", [[1024], [1, 1024, 0], [127, 129, 1000], [31, 32, 33, 64, 2]])
 def test_decode_matches_oracle_from_identical_codes(lens):
     c = _tiny()
     wl, ocal = c["wl"], c["ocal"]
@@ -148,8 +201,7 @@ def test_decode_matches_oracle_from_identical_codes(lens):
     q = synth.query_inputs(wl, device="cuda", batch=B)
     ref = oracle.decode_attention(to_np64(q), kp, vp, ocal, seq_lens=lens)
     g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
-    kpt = torch.from_numpy(kp.view(np.int32)).cuda()
-    vpt = torch.from_numpy(vp.view(np.int32)).cuda()
+    kpt, vpt = _upload(kp, oracle.KEYS, 1024), _upload(vp, oracle.VALUES, 1024)
     sl = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = aatc.decode_attention(g, q, kpt, vpt, L, seq_lens=sl).cpu().numpy()
     for b in range(B):
@@ -162,6 +214,90 @@ def test_decode_matches_oracle_from_identical_codes(lens):
     ref2 = oracle.decode_attention(to_np64(q), kp, vp, ocal, seq_lens=[L] * B)
     assert attn_rel_err(out2, ref2) <= ATTN_RTOL
     g.check()
+
+
+def _synthetic_calibration(G, bits_k, bits_v, seed=0):
+    """A calibration with chosen bit allocations (orthogonal transforms from
+    QR, steps from the oracle), to reach every decode path."""
+    rng = np.random.default_rng(seed)
+    d = 128
+    cal = {}
+    Qk, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    Qv, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    lam_k = 0.95 ** np.arange(d)
+    lam_v = 0.93 ** np.arange(d)
+    cal["mu_k"] = rng.standard_normal((1, d))
+    cal["mu_v"] = rng.standard_normal((1, d))
+    cal["T_k"] = Qk.T[None]
+    cal["T_k_inv"] = Qk[None]
+    cal["A_k"] = Qk.T[None]
+    cal["T_v"] = Qv.T[None]
+    cal["U_v"] = Qv[None]
+    cal["lam_k"], cal["lam_v"], cal["lam_q"] = lam_k[None], lam_v[None], np.ones((1, d))
+    cal["bits_k"] = np.asarray(bits_k, dtype=np.int32)[None]
+    cal["bits_v"] = np.asarray(bits_v, dtype=np.int32)[None]
+    cal["step_k"] = oracle.steps(lam_k, bits_k)[None]
+    cal["step_v"] = oracle.steps(lam_v, bits_v)[None]
+    cal["W"] = int(np.sum(bits_k)) // 32
+    cal["G"] = G
+    return cal
+
+
+@pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "bits2", "bits4"])
+def test_decode_paths_match_oracle(case):
+    """Fast path (GQA groups of 1..8, 2.0..4.0 bits) and the general path
+    (records above 16 words, bytes holding more than four code pieces)."""
+    lam = 0.95 ** np.arange(128)
+    G, B_bits = 4, 352
+    if case == "G1":
+        G = 1
+    elif case in ("G7", "G8"):
+        G = int(case[1:])
+    elif case == "wide_W20":
+        B_bits = 640
+    elif case == "bits2":
+        B_bits = 256
+    elif case == "bits4":
+        B_bits = 512
+    bk, _ = oracle.allocate_bits(lam, B_bits)
+    bv, _ = oracle.allocate_bits(0.93 ** np.arange(128), B_bits)
+    if case == "many_pieces":
+        # 96 two-bit and 32 one-bit codes: the order rule puts the last 1-bit
+        # codes eight to a byte, beyond what the fast decoder reads
+        bk = np.array([2] * 96 + [1] * 32, dtype=np.int32)
+        bv = bk.copy()
+    cal = _synthetic_calibration(G, bk, bv)
+    W = cal["W"]
+    L, Bsz = 333, 2
+    rng = np.random.default_rng(1)
+    kp = np.stack([[oracle.pack(rng.integers(0, 2 ** np.maximum(bk, 1)) * (bk > 0), bk) for _ in range(L)]
+                   for _ in range(Bsz)])[:, None]
+    vp = np.stack([[oracle.pack(rng.integers(0, 2 ** np.maximum(bv, 1)) * (bv > 0), bv) for _ in range(L)]
+                   for _ in range(Bsz)])[:, None]
+    q = torch.from_numpy(rng.standard_normal((Bsz, G, 128)).astype(np.float32) * 3).cuda()
+    g = aatc.import_calib(cal, G, torch.float32)
+    L_cap = aatc.cache_capacity(L)
+    out = aatc.decode_attention(g, q, _upload(kp, oracle.KEYS, L_cap), _upload(vp, oracle.VALUES, L_cap), L)
+    ref = oracle.decode_attention(to_np64(q), kp, vp, cal)
+    err = attn_rel_err(out.cpu().numpy(), ref)
+    assert err <= ATTN_RTOL, (case, err)
+    g.check()
+
+
+def test_decode_workspace_reuse_across_shapes():
+    """One workspace, calls of different shapes in a row: each call sets up
+    its own merge state, so nothing left by the previous call leaks."""
+    c = _tiny()
+    wl, ocal = c["wl"], c["ocal"]
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kp, vp = _oracle_records(wl, ocal, 3, 700)
+    kpt, vpt = _upload(kp, oracle.KEYS, 704), _upload(vp, oracle.VALUES, 704)
+    ws = torch.full((aatc.workspace_size(g, 3, 700),), 0x7F, dtype=torch.uint8, device="cuda")
+    for Bsz, L in ((3, 700), (1, 40), (2, 513), (3, 700)):
+        q = synth.query_inputs(wl, device="cuda", batch=Bsz, step=L)
+        out = aatc.decode_attention(g, q, kpt[:Bsz], vpt[:Bsz], L, workspace=ws).cpu().numpy()
+        ref = oracle.decode_attention(to_np64(q), kp[:Bsz], vp[:Bsz], ocal, seq_lens=[L] * Bsz)
+        assert attn_rel_err(out, ref) <= ATTN_RTOL, (Bsz, L)
 
 
 def test_decode_workspace_and_capacity_errors():
@@ -191,9 +327,8 @@ def _end_to_end(wl, sample, layer=0, seq_len=None, bits=None, decode_step=False)
     gcal = g.export()
     ties = _check_calibration(gcal, ocal, wl.n_kv_heads)
     kc, vc = synth.cache_inputs(wl, layer=layer, device="cuda", seq_len=L)
-    L_cap = L + 1
-    kp = aatc.alloc_cache(g, wl.batch, L_cap)
-    vp = aatc.alloc_cache(g, wl.batch, L_cap)
+    kp = aatc.alloc_cache(g, wl.batch, L + 1)
+    vp = aatc.alloc_cache(g, wl.batch, L + 1)
     aatc.encode(g, kc, vc, kp, vp)
     Ltot = L
     if decode_step:
@@ -206,7 +341,6 @@ def _end_to_end(wl, sample, layer=0, seq_len=None, bits=None, decode_step=False)
     qd = synth.query_inputs(wl, layer=layer, device="cuda")
     out = aatc.decode_attention(g, qd, kp, vp, Ltot).cpu().numpy()
     g.check()
-    kpn, vpn = as_u32(kp), as_u32(vp)
     G = wl.group
     worst = 0.0
     for (b, h) in sample:
@@ -219,8 +353,8 @@ def _end_to_end(wl, sample, layer=0, seq_len=None, bits=None, decode_step=False)
         xv = to_np64(vc[b:b + 1, h:h + 1, :Ltot])
         rk, ck, pk = oracle.encode_cache(xk, sub, "k", want_codes=True, want_pre=True)
         rv, cv, pv = oracle.encode_cache(xv, sub, "v", want_codes=True, want_pre=True)
-        compare_codes(kpn[b:b + 1, h:h + 1, :Ltot], ck, pk, sub["bits_k"][0])
-        compare_codes(vpn[b:b + 1, h:h + 1, :Ltot], cv, pv, sub["bits_v"][0])
+        compare_codes(_records(kp[b:b + 1, h:h + 1], ocal["W"], oracle.KEYS, Ltot), ck, pk, sub["bits_k"][0])
+        compare_codes(_records(vp[b:b + 1, h:h + 1], ocal["W"], oracle.VALUES, Ltot), cv, pv, sub["bits_v"][0])
         qq = to_np64(qd[b:b + 1, h * G:(h + 1) * G])
         ref = oracle.decode_attention(qq, rk, rv, sub)
         err = attn_rel_err(out[b, h * G:(h + 1) * G], ref[0])
