@@ -142,8 +142,13 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
  * applied once per head.  workspace: device scratch of at least
  * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned, contents
  * need not be initialized (the call sets up what it needs, on `stream`);
- * calls that share a workspace must be ordered on one stream.  Up to three
- * kernels are launched, the second with programmatic dependent launch.
+ * calls that share a workspace must be ordered on one stream.  Two kernels
+ * are launched on `stream`: a split kernel that writes one partial result per
+ * (row, KV head, split) to the workspace, and a combine kernel (programmatic
+ * dependent launch: its prologue overlaps the split kernel's tail) that
+ * merges the splits and writes `out`.  Records above 16 words or layouts
+ * whose bytes hold more than four code pieces take a slower general path of
+ * three kernels.
  * Errors: CAPACITY if L > L_cap; INVALID_ARG if the workspace is too small or
  * L_cap is not a multiple of 32. */
 aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,

@@ -21,7 +21,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Sizes of the arena pieces, in the order they are carved.
 struct Layout {
-    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, total;
+    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, t3, cols, total;
 };
 
 Layout layout_for(int H)
@@ -35,8 +35,10 @@ Layout layout_for(int H)
     L.f32_mat = up((size_t)H * D * D * sizeof(float));
     L.tabs = up((size_t)H * 2 * sizeof(CodecTables));
     L.plans = up((size_t)H * 2 * sizeof(HeadPlan));
+    L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
+    L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
     L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
-              L.plans + 256;
+              L.plans + L.t3 + L.cols + 1024;
     return L;
 }
 
@@ -79,6 +81,9 @@ aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib 
     h->UvT32 = (float *)take(L.f32_mat);
     h->tab = (CodecTables *)take(L.tabs);
     h->plan = (HeadPlan *)take(L.plans);
+    p = (char *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);   // T3: TMA source, keep it well aligned
+    h->T3 = take(L.t3);
+    h->enc_cols = (EncCol *)take(L.cols);
     h->status = (uint32_t *)take(256);
     e = cudaMemset(h->status, 0, sizeof(uint32_t));
     if (e != cudaSuccess) { cudaFree(h->arena); delete h; return aatc_cuda_fail(e, "cudaMemset"); }

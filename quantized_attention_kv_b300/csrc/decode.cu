@@ -12,20 +12,25 @@
 // each packed record is streamed once.
 //
 // Fast path (record words <= 16, at most 4 code pieces per record byte):
-//   k_qprep_fast   per (batch row, KV head, head group): q' for the group's
-//                  query heads, expanded to one fp16 hi/lo weight per record
-//                  piece in mma.sync B-fragment order; zeroes the merge ticket.
-//   k_decode_fast  per (split, KV head, batch row x head group): 4 warps, each
-//                  streaming its own 32-token tiles into shared memory with
-//                  cp.async.bulk, unpacking pieces with one AND per two fp16
-//                  operands, scores and P.V on mma.sync (fp16 hi/lo operands,
-//                  fp32 accumulation), online softmax in exp2 form.  Warps and
-//                  splits merge by log-sum-exp; the last CTA of a (batch row,
-//                  KV head, head group) applies Uv and writes the output.
+//   k_decode_fast   one persistent CTA per SM over a balanced share of all
+//                   (batch row, KV head, head group, 32-token tile) work.  Per
+//                   segment it computes q' for the head group and expands it
+//                   to one fp16 hi/lo weight per record piece in mma.sync
+//                   B-fragment order; each warp streams its own tiles into
+//                   shared memory with cp.async.bulk, unpacks pieces with one
+//                   AND per two fp16 operands, runs scores and P.V on mma.sync
+//                   (fp16 hi/lo operands, fp32 accumulation) with an exp2
+//                   online softmax; warps merge by log-sum-exp into one
+//                   partial per segment.
+//   k_decode_combine_fast  per (batch row, KV head, head group), launched
+//                   with programmatic dependent launch: merges the partials
+//                   and applies Uv once per head.
 // General path (any shape): one thread per token, codes read by offset.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "internal.h"
 
@@ -57,15 +62,11 @@ constexpr int FSTAGES = 3;       // tiles in flight per warp
 constexpr int PSTRIDE = 40;      // halfs per row of the per-warp P buffer (32 tokens + pad)
 constexpr int FAST_MAX_W = 16;
 constexpr int PROW = 4 + D;      // floats per partial: m, l, 2 pad, acc[D] (acc 16-byte aligned)
-constexpr size_t FINAL_SMEM = (size_t)D * D * 4 + 2 * 8 * D * 4;   // Uv^T + channel sums + cbar
 
 // Work split: every (batch row, KV head, head group) is a "unit" of
-// n_tiles = ceil(L/32) tiles.  The units' tiles are laid end to end and
-// cut into C equal contiguous ranges, one per CTA (C = resident CTAs), so
-// the load is balanced whatever the batch.  A CTA works through the units
-// its range touches one "segment" at a time and leaves one partial per
-// segment; CTA c covers unit u iff its range meets the unit's tiles, and
-// the CTA holding global tile x is c(x) = ((x + 1) C - 1) / T.
+// n_tiles = ceil(L/32) tiles, cut into S = max(1, resident CTAs / units)
+// equal contiguous ranges; CTA (unit u, split s) streams range s of unit u
+// and leaves partial slot s.
 struct FastGeom {
     int NT;          // 8-column n-tiles (each: 4 query heads x hi/lo)
     int HPG;         // query heads per head group (4 NT)
@@ -76,15 +77,10 @@ struct FastGeom {
     int ksteps;      // 4 rows
     int n_tiles;     // tiles per unit
     int units;       // B * Hkv * HG
-    int C;           // CTAs
-    int PMAX;        // partial slots per unit
-    size_t stage_bytes, smem, qtab_words, ws_qtab, ws_qsc, ws_part, ws_cnt, ws_total;
+    int S;           // splits (CTAs, partial slots) per unit
+    int tiles_per;   // tiles per split
+    size_t stage_bytes, smem, ws_part, ws_total;
 };
-
-__host__ __device__ __forceinline__ int cta_of_tile(long long x, int C, long long T)
-{
-    return (int)(((x + 1) * C - 1) / T);
-}
 
 size_t fast_smem(int FW, int W, int groups, int HPG, int NT, int ksteps, int rows)
 {
@@ -93,13 +89,10 @@ size_t fast_smem(int FW, int W, int groups, int HPG, int NT, int ksteps, int row
     const size_t merge = (size_t)FW * (rows_tot + 2) * HPG * 4 + (size_t)D * HPG * 4;
     size_t big = (size_t)FW * FSTAGES * SB;
     big = big > merge ? big : merge;
-    big = big > FINAL_SMEM ? big : FINAL_SMEM;
     big = (big + 127) & ~(size_t)127;
     return big + (size_t)FW * FSTAGES * 8 + (size_t)FW * 16 * PSTRIDE * 2 + (size_t)ksteps * NT * 32 * 8 +
-           (size_t)rows * 4 * 8 * 4 + (size_t)groups * 64 * 4 + 256 * 2 + 8 * 4 + 16;
+           (size_t)rows * 4 * 8 * 4 + (size_t)groups * 64 * 4 + 256 * 2 + 8 * 4 + 2 * 8 * D * 4 + 256 * 2 + 16;
 }
-
-template <int GMAX, int NT, int FW> __global__ void k_decode_fast(struct FastArgs a);
 
 int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem);
 
@@ -117,20 +110,14 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.units = B * h->Hkv * f.HG;
     f.smem = fast_smem(f.FW, h->W, f.groups, f.HPG, f.NT, f.ksteps, f.rows);
     const int per_sm = fast_ctas_per_sm(f.groups, f.NT, f.FW, f.smem);
-    const long long T = (long long)f.units * f.n_tiles;
-    long long C = (long long)sm_count() * per_sm;
-    if (C > T) C = T > 0 ? T : 1;
-    f.C = (int)C;
-    f.PMAX = (int)((f.C + f.units - 1) / f.units) + 1;
+    const int C = sm_count() * per_sm;
+    f.S = C / f.units > 1 ? C / f.units : 1;
+    if (f.S > f.n_tiles) f.S = f.n_tiles > 0 ? f.n_tiles : 1;
+    f.tiles_per = f.n_tiles > 0 ? (f.n_tiles + f.S - 1) / f.S : 1;
+    f.S = f.n_tiles > 0 ? (f.n_tiles + f.tiles_per - 1) / f.tiles_per : 1;
     f.stage_bytes = 256 * (size_t)h->W + 512;
-    f.qtab_words = (size_t)f.ksteps * f.NT * 32 * 2;
-    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-    const size_t uz = (size_t)f.units;
-    f.ws_qtab = up(uz * f.qtab_words * 4);
-    f.ws_qsc = up(uz * 8 * 4);
-    f.ws_part = up(uz * f.PMAX * f.HPG * PROW * 4);
-    f.ws_cnt = up(uz * 4);
-    f.ws_total = f.ws_qtab + f.ws_qsc + f.ws_part + f.ws_cnt;
+    f.ws_part = (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
+    f.ws_total = f.ws_part;
     return f;
 }
 
@@ -158,13 +145,14 @@ __device__ __forceinline__ void mbar_arrive_expect(uint64_t *mb, uint32_t bytes)
 __device__ __forceinline__ bool mbar_wait(uint64_t *mb, uint32_t parity)
 {
     const uint32_t a = smem_u32(mb);
-    for (int it = 0; it < (1 << 22); ++it) {
+    // each try may suspend the thread for up to ~20 us until the phase completes
+    for (int it = 0; it < (1 << 16); ++it) {
         uint32_t done;
         asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
             " selp.u32 %0, 1, 0, p;\n}\n"
             : "=r"(done)
-            : "r"(a), "r"(parity)
+            : "r"(a), "r"(parity), "r"(20000)
             : "memory");
         if (__all_sync(0xffffffffu, done)) return true;
     }
@@ -199,139 +187,20 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 struct FastArgs {
     const uint32_t *kp, *vp;
     const int32_t *seq_lens;
-    int L, L_cap, W, rows, groups, Hkv, G, HG, HPG, n_tiles, units, C, PMAX;
+    int L, L_cap, W, rows, groups, Hkv, G, HG, HPG, n_tiles, units, S, tiles_per;
     const HeadPlan *plan;
-    const uint32_t *qtab;   // [units][ksteps][NT][32] uint2
-    const float *qsc;       // [units][8]
-    float *part;            // [units][PMAX][HPG][PROW]
-    uint32_t *cnt;          // [units]
+    const void *q;          // [B][Hq][D] of the handle's dtype
+    const float *AkT;       // [Hkv][D][D]
+    float *part;            // [units][S][HPG][PROW]
     const CodecTables *tab;
-    const float *UvT, *muv;
-    float *out;
     uint32_t *status;
 };
 
-// q' of the head group's query heads, expanded to per-piece fp16 hi/lo
-// weights in B-fragment order: entry (kstep, n-tile t, lane) = (b0, b1) with
-// column n = 8t + lane/4 = (head n/2, hi if n even else lo), rows of k-step
-// (r, s) from record word 4r + lane%4, slots 2s (b0) and 2s+1 (b1), low half
-// first.  Weight of a piece = q'_ch * 2^ex * S, S a power of two per head
-// keeping every weight below 2^13; qsc[head] = 2^24 / S * log2(e) turns the
-// accumulated score back into log2 units.  Also zeroes the unit's merge
-// ticket and pulls the unit's Uv^T into L2 for the final merge.
-// One block of 256 threads per unit; A_k^T arrives in shared memory by one
-// bulk copy, thread j (+128) sums half of its rows for channel j.
-constexpr int QP_THREADS = 2 * D;
-constexpr size_t QP_SMEM = (size_t)D * D * 4 + 16;
-template <typename T>
-__global__ void __launch_bounds__(QP_THREADS) k_qprep_fast(
-    const T *__restrict__ q, const float *__restrict__ AkT, const float *__restrict__ UvT,
-    const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans, int Hkv, int G, int HG, int HPG,
-    int NT, int ksteps, uint32_t *__restrict__ qtab, float *__restrict__ qsc, uint32_t *__restrict__ cnt,
-    uint32_t *status)
-{
-    asm volatile("griddepcontrol.launch_dependents;");
-    extern __shared__ __align__(128) unsigned char qsm[];
-    float *As = reinterpret_cast<float *>(qsm);          // [D][D] = AkT of this head
-    __shared__ float qs[8][D];
-    __shared__ float pa[2][8][D];
-    __shared__ float S[8];
-    __shared__ int16_t slot_s[AATC_PLAN_SLOTS / 2][8][2];   // key words 0..15: ch | (ex + 64) << 8
-    __shared__ __align__(8) uint64_t bar;
-    const int b = blockIdx.x, h = blockIdx.y, hg = blockIdx.z, tid = threadIdx.x;
-    const int j = tid & (D - 1), kh = tid >> 7;
-    const int unit = (b * Hkv + h) * HG + hg;
-    const int Hq = Hkv * G;
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive_expect(&bar, D * D * 4);
-        bulk_g2s(As, AkT + (size_t)h * D * D, D * D * 4, &bar);
-        if (hg == 0 && b == 0)
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(UvT + (size_t)h * D * D), "r"(D * D * 4)
-                         : "memory");
-        cnt[unit] = 0u;
-    }
-    for (int e = tid; e < 8 * D; e += QP_THREADS) {
-        const int i = e >> 7, cc = e & (D - 1), gi = hg * HPG + i;
-        qs[i][cc] = (i < HPG && gi < G) ? to_f32(q[((size_t)b * Hq + h * G + gi) * D + cc]) : 0.f;
-    }
-    const HeadPlan &pk = plans[h * 2 + 0];
-    for (int e = tid; e < (AATC_PLAN_SLOTS / 2) * 16; e += QP_THREADS) {
-        const int w = e >> 4, k = (e >> 1) & 7, half = e & 1;
-        const int ch = pk.ch[w][k][half];
-        slot_s[w][k][half] = (int16_t)(ch < 0 ? -1 : (ch | ((pk.ex[w][k][half] + 64) << 8)));
-    }
-    __syncthreads();
-    if (!mbar_wait(&bar, 0)) {
-        if (tid == 0) atomicOr(status, AATC_DEV_TIMEOUT);
-        return;
-    }
-    float acc[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int k = kh * 64; k < kh * 64 + 64; ++k) {
-        const float av = As[k * D + j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(av, qs[i][k], acc[i]);
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) pa[kh][i][j] = acc[i];
-    __syncthreads();
-    const CodecTables &tk = tabs[h * 2 + 0];
-    if (tid < D) {
-        const float scale = tk.bits[j] ? tk.step[j] * 0.08838834764831845f : 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pa[0][i][j] = (pa[0][i][j] + pa[1][i][j]) * scale;
-    }
-    __syncthreads();
-    {   // warp i: largest |q'| of head i
-        const int wi = tid >> 5, ln = tid & 31;
-        if (wi < HPG) {
-            float mx = 0.f;
-            for (int k = ln; k < D; k += 32) mx = fmaxf(mx, fabsf(pa[0][wi][k]));
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (ln == 0) {
-                // pieces carry 2^ex with ex <= 7: keep mx * 2^7 * S below 2^13
-                int e = 0;
-                if (mx > 0.f) frexpf(mx, &e);
-                S[wi] = mx > 0.f ? ldexpf(1.f, 6 - e) : 1.f;
-                qsc[unit * 8 + wi] = ldexpf(1.f, 24) / S[wi] * LOG2E;
-            }
-        }
-    }
-    __syncthreads();
-    const int entries = ksteps * NT * 32;
-    uint2 *dst = reinterpret_cast<uint2 *>(qtab) + (size_t)unit * entries;
-    for (int en = tid; en < entries; en += QP_THREADS) {
-        const int lane = en & 31, t = (en >> 5) % NT, ks = (en >> 5) / NT;
-        const int r = ks >> 2, s4 = ks & 3;
-        const int n = 8 * t + (lane >> 2), i = n >> 1, part = n & 1;
-        const int w = 4 * r + (lane & 3);
-        uint32_t o2[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int k = 2 * s4 + rr;
-            float v2[2];
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int sl = slot_s[w][k][half];
-                float val = 0.f;
-                if (sl >= 0 && hg * HPG + i < G) val = ldexpf(pa[0][i][sl & 255] * S[i], (sl >> 8) - 64);
-                const float hi = __half2float(__float2half_rn(val));
-                v2[half] = part ? val - hi : hi;
-            }
-            o2[rr] = pack_half2(v2[0], v2[1]);
-        }
-        dst[en] = make_uint2(o2[0], o2[1]);
-    }
-}
-
-template <int GMAX, int NT, int FW>
+template <int GMAX, int NT, int FW, typename QT>
 __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
+    asm volatile("griddepcontrol.launch_dependents;");   // the combine kernel may start its prologue
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int g = lane >> 2, c = lane & 3;
@@ -344,7 +213,6 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
     const size_t merge = (size_t)FW * (rows_tot + 2) * HPG * 4 + (size_t)D * HPG * 4;
     size_t big = (size_t)FW * FSTAGES * SB;
     big = big > merge ? big : merge;
-    big = big > FINAL_SMEM ? big : FINAL_SMEM;
     big = (big + 127) & ~(size_t)127;
     unsigned char *stage_base = smem;
     uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + big);
@@ -354,10 +222,12 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
     uint32_t *vmask_s = kmask_s + rows * 4 * 8;
     int16_t *vrow_s = reinterpret_cast<int16_t *>(vmask_s + groups * 64);   // [groups*64] (ch << 8 | ex + 64)
     float *sc_s = reinterpret_cast<float *>(vrow_s + 256);
-    __shared__ int s_last;
-    __shared__ float red[NTH];
+    float *qs = sc_s + 8;                     // [8][D] query rows of the head group
+    float *pa = qs + 8 * D;                   // [8][D] q' of the head group
+    int16_t *slot_s = reinterpret_cast<int16_t *>(pa + 8 * D);   // [16][8][2] key piece: ch | (ex + 64) << 8
     __shared__ float cm[8], cl[8], cs[8][FW];
-    __shared__ __align__(8) uint64_t ubar;     // Uv^T bulk copy of the final merge
+    __shared__ float S_s[8];
+    __shared__ float ksc_s[D];                 // Delta_K / sqrt(d), 0 for pruned channels
     __shared__ float vmid_s[256];              // value piece midpoints (2^w-1)/2 * 2^(p-24), per row
 
     uint64_t *my_mbar = mbar + warp * FSTAGES;
@@ -365,25 +235,17 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
     const uint32_t tile_bytes = 128u * W;
     if (lane == 0) {
         for (int s = 0; s < FSTAGES; ++s) mbar_init(&my_mbar[s], 1);
-        if (warp == 0) mbar_init(&ubar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    int n_final = 0;   // final merges done by this CTA (phases of ubar)
     // The warp's n-th tile (over all its segments) goes through stage n % FSTAGES
     // and completes phase n / FSTAGES of that stage's barrier.
     int n_issued = 0, n_done = 0;
 
-    const long long T = (long long)a.units * a.n_tiles;
-    const long long lo = (long long)blockIdx.x * T / a.C, hi = (long long)(blockIdx.x + 1) * T / a.C;
-    bool waited = false;
-    for (long long x = lo; x < hi;) {
-        // ---- next segment: unit u, tiles [ta, tb) of the unit
-        const int u = (int)(x / a.n_tiles);
-        const int ta = (int)(x - (long long)u * a.n_tiles);
-        const long long uend = (long long)(u + 1) * a.n_tiles;
-        const int tb = (int)((hi < uend ? hi : uend) - (long long)u * a.n_tiles);
-        x = (long long)u * a.n_tiles + tb;
+    {
+        // ---- this CTA: unit u, split sp, tiles [ta, tb) of the unit
+        const int u = blockIdx.x / a.S, sp = blockIdx.x % a.S;
+        const int ta = sp * a.tiles_per, tb = min(ta + a.tiles_per, a.n_tiles);
         const int b = u / (a.Hkv * a.HG), h = (u / a.HG) % a.Hkv, hg = u % a.HG;
         const int len = a.seq_lens ? min(max(a.seq_lens[b], 0), a.L) : a.L;
         const int t0 = ta, t1 = min(tb, (len + TILE - 1) / TILE);
@@ -403,29 +265,159 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
             }
         }
 
-        // tables of this unit
+        // ---- tables of this unit and its query weights.  All global loads of
+        // the prologue are issued before any is used: one round trip.
         const HeadPlan &pk = a.plan[h * 2 + 0];
         const HeadPlan &pv = a.plan[h * 2 + 1];
-        for (int e = tid; e < rows * 4 * 8; e += NTH) kmask_s[e] = pk.mask[e >> 3][e & 7];
-        for (int e = tid; e < groups * 64; e += NTH) vmask_s[e] = pv.mask[e >> 3][e & 7];
-        for (int e = tid; e < groups * 64; e += NTH) {
-            // row e = (group, m4, rr): half-word 8 group + rr%8, slot 2 m4 + rr/8
-            const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
-            const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
-            const int ch = pv.ch[hw][k][0];
-            vrow_s[e] = (int16_t)(ch < 0 ? -1 : (ch << 8) | (pv.ex[hw][k][0] + 64));
-            // the mask holds (2^w - 1) << p in each half: its low half / 2 is the
-            // piece's midpoint times 2^p
-            vmid_s[e] = ldexpf((float)(pv.mask[hw][k] & 0xFFFFu), -25);
-        }
-        if (!waited) {   // query weights and tickets come from k_qprep_fast
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            waited = true;
-        }
         {
-            const uint2 *src = reinterpret_cast<const uint2 *>(a.qtab) + (size_t)u * ksteps * NT * 32;
-            for (int e = tid; e < ksteps * NT * 32; e += NTH) qtab_s[e] = src[e];
-            if (tid < 8) sc_s[tid] = a.qsc[u * 8 + tid];
+            // A_k^T: thread (k-set kq, channel quad j4) holds rows k = kq + NTH/32 * m
+            constexpr int KSTEP = NTH / 32;
+            constexpr int KPER = (D + KSTEP - 1) / KSTEP;
+            const int j4 = tid & 31, kq = tid >> 5;
+            float4 av[KPER];
+            const float4 *Ag = reinterpret_cast<const float4 *>(a.AkT + (size_t)h * D * D) + j4;
+#pragma unroll
+            for (int m = 0; m < KPER; ++m) {
+                const int k = kq + KSTEP * m;
+                av[m] = k < D ? __ldg(Ag + (size_t)k * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            const QT *qg = reinterpret_cast<const QT *>(a.q);
+            const int Hq = a.Hkv * a.G;
+            // every global load of the prologue is issued before any result is stored
+            constexpr int QPER = (8 * D + NTH - 1) / NTH;
+            float qv[QPER];
+#pragma unroll
+            for (int r = 0; r < QPER; ++r) {
+                const int e = tid + r * NTH;
+                const int i = e >> 7, cc = e & (D - 1), gi = hg * HPG + i;
+                qv[r] = (e < 8 * D && i < HPG && gi < a.G) ? to_f32(qg[((size_t)b * Hq + h * a.G + gi) * D + cc]) : 0.f;
+            }
+            const int ek = tid;                       // rows * 32 <= NTH
+            const uint32_t km = ek < rows * 32 ? pk.mask[ek >> 3][ek & 7] : 0u;
+            constexpr int VPER = (4 * 64 + NTH - 1) / NTH;
+            uint32_t vm[VPER];
+            int vch[VPER], vex[VPER];
+#pragma unroll
+            for (int r = 0; r < VPER; ++r) {
+                const int e = tid + r * NTH;
+                const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
+                const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
+                const bool in = e < groups * 64;
+                vm[r] = in ? pv.mask[e >> 3][e & 7] : 0u;
+                vch[r] = in ? pv.ch[hw][k][0] : -1;
+                vex[r] = in ? pv.ex[hw][k][0] : 0;
+            }
+            const int es = tid;                       // 16 * 16 <= NTH
+            int sch = -1, sex = 0;
+            if (es < 256) {
+                sch = pk.ch[es >> 4][(es >> 1) & 7][es & 1];
+                sex = pk.ex[es >> 4][(es >> 1) & 7][es & 1];
+            }
+            const CodecTables &tk = a.tab[h * 2 + 0];
+            const float ksc = tid < D ? (tk.bits[tid] ? tk.step[tid] * 0.08838834764831845f : 0.f) : 0.f;
+            // ... then stored
+#pragma unroll
+            for (int r = 0; r < QPER; ++r) {
+                const int e = tid + r * NTH;
+                if (e < 8 * D) {
+                    qs[e] = qv[r];
+                    pa[e] = 0.f;
+                }
+            }
+            if (ek < rows * 32) kmask_s[ek] = km;
+#pragma unroll
+            for (int r = 0; r < VPER; ++r) {
+                const int e = tid + r * NTH;
+                if (e < groups * 64) {
+                    vmask_s[e] = vm[r];
+                    // row e = (group, m4, rr): half-word 8 group + rr%8, slot 2 m4 + rr/8; the
+                    // slot's mask holds (2^w - 1) << p per half: low half / 2 = midpoint * 2^p
+                    const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
+                    const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
+                    (void)hw;
+                    (void)k;
+                    vrow_s[e] = (int16_t)(vch[r] < 0 ? -1 : (vch[r] << 8) | (vex[r] + 64));
+                    vmid_s[e] = 0.f;
+                }
+            }
+            if (es < 256) slot_s[es] = (int16_t)(sch < 0 ? -1 : (sch | ((sex + 64) << 8)));
+            if (tid < D) ksc_s[tid] = ksc;
+            __syncthreads();
+            for (int e = tid; e < groups * 64; e += NTH) {
+                const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
+                const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
+                vmid_s[e] = ldexpf((float)(vmask_s[hw * 8 + k] & 0xFFFFu), -25);
+            }
+            // q'_i[j] = sum_k A_k[j][k] q_i[k]: partial sums over this thread's rows
+            float4 acc4[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int m = 0; m < KPER; ++m) {
+                const int k = kq + KSTEP * m;
+                if (k >= D) break;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    if (i >= HPG) break;
+                    const float qv = qs[i * D + k];
+                    acc4[i].x = fmaf(av[m].x, qv, acc4[i].x);
+                    acc4[i].y = fmaf(av[m].y, qv, acc4[i].y);
+                    acc4[i].z = fmaf(av[m].z, qv, acc4[i].z);
+                    acc4[i].w = fmaf(av[m].w, qv, acc4[i].w);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (i >= HPG) break;
+                float *d = pa + i * D + 4 * j4;
+                atomicAdd(d + 0, acc4[i].x);
+                atomicAdd(d + 1, acc4[i].y);
+                atomicAdd(d + 2, acc4[i].z);
+                atomicAdd(d + 3, acc4[i].w);
+            }
+            __syncthreads();
+            for (int e = tid; e < HPG * D; e += NTH) pa[e] *= ksc_s[e & (D - 1)];
+            __syncthreads();
+            if (warp < HPG) {   // warp i: largest |q'| of head i -> power-of-two scale
+                float mx = 0.f;
+                for (int k = lane; k < D; k += 32) mx = fmaxf(mx, fabsf(pa[warp * D + k]));
+                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                if (lane == 0) {
+                    // pieces carry 2^ex with ex <= 7: keep mx * 2^7 * S below 2^13
+                    int e = 0;
+                    if (mx > 0.f) frexpf(mx, &e);
+                    const float S = mx > 0.f ? ldexpf(1.f, 6 - e) : 1.f;
+                    S_s[warp] = S;
+                    sc_s[warp] = ldexpf(1.f, 24) / S * LOG2E;
+                }
+            }
+            __syncthreads();
+            // B fragments: entry (kstep, n-tile t, lane) = (b0, b1), column n = 8t + lane/4 =
+            // (head n/2, hi if n even else lo), k-step (r, s) from record word 4r + lane%4,
+            // slots 2s (b0) and 2s+1 (b1), low half first; weight = q'_ch * 2^ex * S
+            for (int en = tid; en < ksteps * NT * 32; en += NTH) {
+                const int ln = en & 31, t = (en >> 5) % NT, ks = (en >> 5) / NT;
+                const int r = ks >> 2, s4 = ks & 3;
+                const int n = 8 * t + (ln >> 2), i = n >> 1, part = n & 1;
+                const int w = 4 * r + (ln & 3);
+                uint32_t o2[2];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int k = 2 * s4 + rr;
+                    float v2[2];
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int sl = slot_s[(w * 8 + k) * 2 + half];
+                        float val = 0.f;
+                        if (sl >= 0 && i < HPG && hg * HPG + i < a.G)
+                            val = ldexpf(pa[i * D + (sl & 255)] * S_s[i], (sl >> 8) - 64);
+                        const float hi = __half2float(__float2half_rn(val));
+                        v2[half] = part ? val - hi : hi;
+                    }
+                    o2[rr] = pack_half2(v2[0], v2[1]);
+                }
+                qtab_s[en] = make_uint2(o2[0], o2[1]);
+            }
         }
         __syncthreads();
 
@@ -460,36 +452,58 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
             const uint32_t *Kt = reinterpret_cast<const uint32_t *>(my_stage + s * SB);
             const uint32_t *Vt = Kt + TILE * W;
 
-            // ---- scores: rows = tokens (row g: 2g, row g+8: 2g+1 of the half), k = record pieces
+            // ---- scores: rows = tokens (row g: 2g, row g+8: 2g+1 of the half), k = record pieces;
+            // one accumulator chain per (half, record row) for independent MMAs
             float C[2][NT][4];
+            {
+                float Cr[2][4][NT][4];
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+                for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
-                for (int t = 0; t < NT; ++t)
+                    for (int r = 0; r < 4; ++r)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) C[hf][t][k] = 0.f;
+                        for (int t = 0; t < NT; ++t)
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) Cr[hf][r][t][k] = 0.f;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     if (r >= rows) break;
                     const int nr = min(4, W - 4 * r);
-                    const uint2 kw =
-                        *reinterpret_cast<const uint2 *>(Kt + hf * 16 * W + 64 * r + g * 2 * nr + 2 * c);
                     const uint4 mA = *reinterpret_cast<const uint4 *>(kmask_s + (4 * r + c) * 8);
                     const uint4 mB = *reinterpret_cast<const uint4 *>(kmask_s + (4 * r + c) * 8 + 4);
                     const uint32_t mk[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
-                    const uint32_t x0 = kw.x, x1 = kw.y, y0 = x0 >> 8, y1 = x1 >> 8;
+                    uint32_t x0[2], x1[2], y0[2], y1[2];
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const uint2 kw =
+                            *reinterpret_cast<const uint2 *>(Kt + hf * 16 * W + 64 * r + g * 2 * nr + 2 * c);
+                        x0[hf] = kw.x;
+                        x1[hf] = kw.y;
+                        y0[hf] = kw.x >> 8;
+                        y1[hf] = kw.y >> 8;
+                    }
 #pragma unroll
                     for (int s4 = 0; s4 < 4; ++s4) {
-                        const uint32_t sa = s4 < 2 ? x0 : y0, sb = s4 < 2 ? x1 : y1;
-                        const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
-                        const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
+                        uint2 bq[NT];
 #pragma unroll
-                        for (int t = 0; t < NT; ++t) {
-                            const uint2 bq = qtab_s[((r * 4 + s4) * NT + t) * 32 + lane];
-                            mma16816(C[hf][t], A0, A1, A2, A3, bq.x, bq.y);
+                        for (int t = 0; t < NT; ++t) bq[t] = qtab_s[((r * 4 + s4) * NT + t) * 32 + lane];
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            const uint32_t sa = s4 < 2 ? x0[hf] : y0[hf], sb = s4 < 2 ? x1[hf] : y1[hf];
+                            const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
+                            const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
+#pragma unroll
+                            for (int t = 0; t < NT; ++t) mma16816(Cr[hf][r][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
                         }
                     }
                 }
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            C[hf][t][k] = (Cr[hf][0][t][k] + Cr[hf][1][t][k]) + (Cr[hf][2][t][k] + Cr[hf][3][t][k]);
             }
 
             // ---- online softmax (log2 domain); thread owns head 4t+c of tokens 16hf+2g, +1
@@ -670,134 +684,138 @@ __global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
             atomicAdd(&ach[(rv >> 8) * HPG + i], ldexpf(v, (rv & 255) - 64 + 10));
         }
         __syncthreads();
-        const int c_first = cta_of_tile((long long)u * a.n_tiles, a.C, T);
-        const int c_last = cta_of_tile((long long)(u + 1) * a.n_tiles - 1, a.C, T);
-        const int slot = blockIdx.x - c_first;
         {
-            float *P = a.part + ((size_t)u * a.PMAX + slot) * HPG * PROW;
+            float *P = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
             for (int e = tid; e < HPG * PROW; e += NTH) {
                 const int i = e / PROW, j = e % PROW;
                 P[e] = j == 0 ? cm[i] : (j == 1 ? cl[i] : (j < 4 ? 0.f : ach[(j - 4) * HPG + i]));
             }
         }
+    }
+}
 
-        // ---- last CTA of this unit merges the slots and leaves the transform domain
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) s_last = atomicAdd(&a.cnt[u], 1u) == (unsigned)(c_last - c_first);
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-            const int nslots = c_last - c_first + 1;
-            const float *Pu = a.part + (size_t)u * a.PMAX * HPG * PROW;
-            // per-head maximum and weighted sum over the slots
-            {
-                const int i = tid % HPG;
-                float M = -INFINITY;
-                for (int sp = tid / HPG; sp < nslots; sp += NTH / HPG)
-                    M = fmaxf(M, __ldcg(Pu + ((size_t)sp * HPG + i) * PROW));
-                red[tid] = M;
-            }
-            __syncthreads();
-            if (tid < HPG) {
-                float M = -INFINITY;
-                for (int k = tid; k < NTH; k += HPG) M = fmaxf(M, red[k]);
-                cm[tid] = M;
-            }
-            __syncthreads();
-            {
-                const int i = tid % HPG;
-                const float M = cm[i];
-                float Ls = 0.f;
-                for (int sp = tid / HPG; sp < nslots; sp += NTH / HPG) {
-                    const float *Ps = Pu + ((size_t)sp * HPG + i) * PROW;
-                    const float ms = __ldcg(Ps);
-                    if (ms != -INFINITY) Ls = fmaf(__ldcg(Ps + 1), exp2f(ms - M), Ls);
-                }
-                red[tid] = Ls;
-            }
-            __syncthreads();
-            if (tid < HPG) {
-                float Ls = 0.f;
-                for (int k = tid; k < NTH; k += HPG) Ls += red[k];
-                cl[tid] = Ls;
-            }
-            __syncthreads();
-            // Uv^T of this head into shared memory (one bulk copy, usually from L2)
-            float *UT = reinterpret_cast<float *>(stage_base);       // [D][D]
-            float *cacc = UT + D * D;                                // [HPG][D]
-            float *cbar = cacc + 8 * D;                              // [HPG][D]
-            if (tid == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect(&ubar, D * D * 4);
-                bulk_g2s(UT, a.UvT + (size_t)h * D * D, D * D * 4, &ubar);
-            }
-            // channel sums: thread (i, j4) sums float4 channel block j4 of head i over
-            // a share of the slots; shares are added in shared memory
-            for (int e = tid; e < HPG * D; e += NTH) cacc[e] = 0.f;
-            __syncthreads();
-            {
-                const int outs = HPG * (D / 4);           // float4 outputs
-                const int reps = NTH / outs > 0 ? NTH / outs : 1;
-                const int o = tid % outs, rep = tid / outs;
-                if (rep < reps) {
-                    const int i = o / (D / 4), j4 = o % (D / 4);
-                    const float M = cm[i];
-                    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int sp = rep; sp < nslots; sp += reps) {
-                        const float *Ps = Pu + ((size_t)sp * HPG + i) * PROW;
-                        const float ms = __ldcg(Ps);
-                        const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-                        const float4 v = __ldcg(reinterpret_cast<const float4 *>(Ps + 4) + j4);
-                        s4.x = fmaf(v.x, f, s4.x);
-                        s4.y = fmaf(v.y, f, s4.y);
-                        s4.z = fmaf(v.z, f, s4.z);
-                        s4.w = fmaf(v.w, f, s4.w);
-                    }
-                    float *dst = cacc + i * D + 4 * j4;
-                    atomicAdd(dst + 0, s4.x);
-                    atomicAdd(dst + 1, s4.y);
-                    atomicAdd(dst + 2, s4.z);
-                    atomicAdd(dst + 3, s4.w);
-                }
-            }
-            __syncthreads();
-            // the channel sums are centred: sum_i p_i (u_ij - mid_j)
-            const CodecTables &tv = a.tab[h * 2 + 1];
-            for (int e = tid; e < HPG * D; e += NTH) {
-                const int i = e / D, j = e % D;
-                const float Ls = cl[i];
-                cbar[e] = (Ls > 0.f && tv.bits[j]) ? tv.step[j] * (cacc[e] / Ls) : 0.f;
-            }
-            const bool have_u = mbar_wait(&ubar, (uint32_t)(n_final & 1));
-            ++n_final;
-            if (!have_u && tid == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
-            __syncthreads();
-            // o = Uv cbar + mu_v
-            const int Hq = a.Hkv * a.G;
-            for (int e = tid; e < HPG * D; e += NTH) {
-                const int i = e / D, j = e % D;
-                const int gi = hg * HPG + i;
-                if (gi >= a.G) continue;
-                float o = 0.f;
-                if (cl[i] > 0.f && have_u) {
-                    const float *cb = cbar + i * D;
-#pragma unroll 8
-                    for (int k = 0; k < D; ++k) o = fmaf(UT[k * D + j], cb[k], o);
-                    o += a.muv[h * D + j];
-                }
-                a.out[((size_t)b * Hq + h * a.G + gi) * D + j] = o;
-            }
-            if (tid == 0) a.cnt[u] = 0u;
+
+// Merge the slots of one unit and leave the transform domain:
+//   o = Uv (Delta_V o sum_i p_i (u_i - mid) / sum_i p_i) + mu_v
+// (the slots hold centred sums).  Launched after k_decode_fast with
+// programmatic dependent launch: Uv^T and the tables are staged before the
+// wait for the split kernel's partials.
+constexpr int CB_THREADS = 256;
+constexpr size_t CB_SMEM = (size_t)D * D * 4;
+__global__ void __launch_bounds__(CB_THREADS) k_decode_combine_fast(
+    const float *__restrict__ part, int S, int Hkv, int G, int HG, int HPG,
+    const CodecTables *__restrict__ tabs, const float *__restrict__ UvT, const float *__restrict__ muv,
+    float *__restrict__ out)
+{
+    extern __shared__ __align__(16) float UT[];          // [D][D]
+    __shared__ float cacc[8][D], cbar[8][D];
+    __shared__ float sM[8], sL[8];
+    __shared__ float step_s[D], muv_s[D];
+    __shared__ float ml_s[2][CB_THREADS];
+    const int u = blockIdx.x, tid = threadIdx.x;
+    const int b = u / (Hkv * HG), h = (u / HG) % Hkv, hg = u % HG;
+    {
+        // every load of the prologue in flight at once
+        const float4 *src = reinterpret_cast<const float4 *>(UvT + (size_t)h * D * D);
+        float4 ut[D * D / 4 / CB_THREADS];
+#pragma unroll
+        for (int r = 0; r < D * D / 4 / CB_THREADS; ++r) ut[r] = __ldg(src + tid + r * CB_THREADS);
+        const CodecTables &tv = tabs[h * 2 + 1];
+        float st = 0.f, mv = 0.f;
+        if (tid < D) {
+            st = tv.bits[tid] ? tv.step[tid] : 0.f;
+            mv = muv[h * D + tid];
         }
-        __syncthreads();   // shared memory (tables, merge area) is reused by the next segment
+        float4 *dst = reinterpret_cast<float4 *>(UT);
+#pragma unroll
+        for (int r = 0; r < D * D / 4 / CB_THREADS; ++r) dst[tid + r * CB_THREADS] = ut[r];
+        if (tid < D) {
+            step_s[tid] = st;
+            muv_s[tid] = mv;
+        }
+        for (int e = tid; e < 8 * D; e += CB_THREADS) (&cacc[0][0])[e] = 0.f;
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // partials of k_decode_fast
+    const int nslots = S;
+    const float *Pu = part + (size_t)u * S * HPG * PROW;
+    // per-head maximum and weighted sum over the slots; (slot, head) pairs in parallel
+    float Mh = -INFINITY;
+    for (int e0 = 0; e0 < nslots * HPG; e0 += CB_THREADS) {
+        const int e = e0 + tid;
+        float m = -INFINITY, l = 0.f;
+        if (e < nslots * HPG) {
+            m = __ldcg(Pu + (size_t)e * PROW);
+            l = __ldcg(Pu + (size_t)e * PROW + 1);
+        }
+        __syncthreads();
+        ml_s[0][tid] = m;
+        ml_s[1][tid] = l;
+        __syncthreads();
+        if (tid < HPG) {
+            const int cnt = min(CB_THREADS, nslots * HPG - e0);
+            float M = Mh, Ls = e0 == 0 ? 0.f : sL[tid];
+            for (int k = tid; k < cnt; k += HPG) {
+                const float mk = ml_s[0][k];
+                if (mk == -INFINITY) continue;
+                if (mk > M) {
+                    Ls = (M == -INFINITY) ? 0.f : Ls * exp2f(M - mk);
+                    M = mk;
+                }
+                Ls = fmaf(ml_s[1][k], exp2f(mk - M), Ls);
+            }
+            Mh = M;
+            sM[tid] = M;
+            sL[tid] = Ls;
+        }
+    }
+    __syncthreads();
+    {   // thread (rep, i, j4): float4 block j4 of head i over every reps-th slot
+        const int outs = HPG * (D / 4);
+        const int reps = CB_THREADS / outs;
+        const int o = tid % outs, rep = tid / outs;
+        const int i = o / (D / 4), j4 = o % (D / 4);
+        const float M = sM[i];
+        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int sp = rep; sp < nslots; sp += reps) {
+            const float *Ps = Pu + ((size_t)sp * HPG + i) * PROW;
+            const float ms = __ldcg(Ps);
+            const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(Ps + 4) + j4);
+            s4.x = fmaf(v.x, f, s4.x);
+            s4.y = fmaf(v.y, f, s4.y);
+            s4.z = fmaf(v.z, f, s4.z);
+            s4.w = fmaf(v.w, f, s4.w);
+        }
+        atomicAdd(&cacc[i][4 * j4 + 0], s4.x);
+        atomicAdd(&cacc[i][4 * j4 + 1], s4.y);
+        atomicAdd(&cacc[i][4 * j4 + 2], s4.z);
+        atomicAdd(&cacc[i][4 * j4 + 3], s4.w);
+    }
+    __syncthreads();
+    for (int e = tid; e < HPG * D; e += CB_THREADS) {
+        const int i = e / D, j = e % D;
+        cbar[i][j] = sL[i] > 0.f ? step_s[j] * (cacc[i][j] / sL[i]) : 0.f;
+    }
+    __syncthreads();
+    const int Hq = Hkv * G;
+    for (int e = tid; e < HPG * D; e += CB_THREADS) {
+        const int i = e / D, j = e % D, gi = hg * HPG + i;
+        if (gi >= G) continue;
+        float o = 0.f;
+        if (sL[i] > 0.f) {
+#pragma unroll 8
+            for (int k = 0; k < D; ++k) o = fmaf(UT[k * D + j], cbar[i][k], o);
+            o += muv_s[j];
+        }
+        out[((size_t)b * Hq + h * G + gi) * D + j] = o;
     }
 }
 
 template <int GMAX, int NT, int FW>
 int occupancy_of(size_t smem)
 {
-    auto kern = k_decode_fast<GMAX, NT, FW>;
+    auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 1;
     int n = 0;
@@ -805,9 +823,8 @@ int occupancy_of(size_t smem)
     return n;
 }
 
-int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem)
+int fast_ctas_per_sm_uncached(int groups, int NT, size_t smem)
 {
-    (void)FW;
     if (NT == 1) {
         if (groups <= 2) return occupancy_of<2, 1, 12>(smem);
         if (groups <= 3) return occupancy_of<3, 1, 12>(smem);
@@ -816,6 +833,21 @@ int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem)
     if (groups <= 2) return occupancy_of<2, 2, 8>(smem);
     if (groups <= 3) return occupancy_of<3, 2, 8>(smem);
     return occupancy_of<4, 2, 8>(smem);
+}
+
+int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem)
+{
+    // the answer depends only on the kernel variant and its shared memory
+    static struct { int groups, NT, FW; size_t smem; int n; } cache[16];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].groups == groups && cache[i].NT == NT && cache[i].FW == FW && cache[i].smem == smem)
+            return cache[i].n;
+    const int n = fast_ctas_per_sm_uncached(groups, NT, smem);
+    if (used < 16) cache[used++] = {groups, NT, FW, smem, n};
+    return n;
 }
 
 // ============================================================ general path
@@ -1027,22 +1059,59 @@ size_t general_ws_bytes(const aatc_calib *h, int B, int L)
     return ((qp + 255) / 256) * 256 + part;
 }
 
-template <int GMAX, int NT, int FW>
-aatc_status launch_fast(const FastGeom &f, const FastArgs &a, cudaStream_t s)
+// Raise a kernel's dynamic shared memory limit once per kernel (and per
+// larger size seen).  Keyed by the kernel's address: every instance of a
+// template has the same function type.
+aatc_status smem_limit(const void *kern, size_t bytes)
 {
-    auto kern = k_decode_fast<GMAX, NT, FW>;
-    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)f.smem));
+    static struct { const void *k; size_t set; } seen[32];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    while (i < used && seen[i].k != kern) ++i;
+    if (i < used && seen[i].set >= bytes) return AATC_OK;
+    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+    if (i == used && used < 32) seen[used++] = {kern, 0};
+    if (i < used) seen[i].set = bytes;
+    return AATC_OK;
+}
+
+template <int GMAX, int NT, int FW>
+aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s)
+{
+    if (dt == AATC_BF16) {
+        auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16>;
+        aatc_status st = smem_limit((const void *)kern, f.smem);
+        if (st != AATC_OK) return st;
+        kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
+    } else {
+        auto kern = k_decode_fast<GMAX, NT, FW, float>;
+        aatc_status st = smem_limit((const void *)kern, f.smem);
+        if (st != AATC_OK) return st;
+        kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
+    }
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}
+
+aatc_status launch_combine(const FastGeom &f, const aatc_calib *h, const float *part, float *out, cudaStream_t s)
+{
+    aatc_status st0 = smem_limit((const void *)k_decode_combine_fast, CB_SMEM);
+    if (st0 != AATC_OK) return st0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(f.C);
-    cfg.blockDim = dim3(FW * 32);
-    cfg.dynamicSmemBytes = f.smem;
+    cfg.gridDim = dim3(f.units);
+    cfg.blockDim = dim3(CB_THREADS);
+    cfg.dynamicSmemBytes = CB_SMEM;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, a));
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, k_decode_combine_fast, part, f.S, h->Hkv, h->G, f.HG, f.HPG,
+                                 (const CodecTables *)h->tab, (const float *)h->UvT32, (const float *)h->muv32,
+                                 out));
     return AATC_OK;
 }
 
@@ -1068,27 +1137,7 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
             AATC_CUDA(cudaMemsetAsync(out, 0, (size_t)B * h->Hq * D * sizeof(float), s));
             return AATC_OK;
         }
-        char *w = (char *)ws;
-        uint32_t *qtab = (uint32_t *)w;
-        float *qsc = (float *)(w + f.ws_qtab);
-        float *part = (float *)(w + f.ws_qtab + f.ws_qsc);
-        uint32_t *cnt = (uint32_t *)(w + f.ws_qtab + f.ws_qsc + f.ws_part);
-        const dim3 pg(B, h->Hkv, f.HG);
-        if (h->dtype == AATC_BF16)
-        {
-            auto kq = k_qprep_fast<__nv_bfloat16>;
-            AATC_CUDA(cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QP_SMEM));
-            kq<<<pg, QP_THREADS, QP_SMEM, s>>>((const __nv_bfloat16 *)q, h->AkT32, h->UvT32, h->tab, h->plan,
-                                               h->Hkv, h->G, f.HG, f.HPG, f.NT, f.ksteps, qtab, qsc, cnt,
-                                               h->status);
-        }
-        else {
-            auto kq = k_qprep_fast<float>;
-            AATC_CUDA(cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)QP_SMEM));
-            kq<<<pg, QP_THREADS, QP_SMEM, s>>>((const float *)q, h->AkT32, h->UvT32, h->tab, h->plan, h->Hkv,
-                                               h->G, f.HG, f.HPG, f.NT, f.ksteps, qtab, qsc, cnt, h->status);
-        }
-        AATC_CUDA(cudaGetLastError());
+        float *part = (float *)ws;
         FastArgs a;
         a.kp = kp;
         a.vp = vp;
@@ -1104,26 +1153,26 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.HPG = f.HPG;
         a.n_tiles = f.n_tiles;
         a.units = f.units;
-        a.C = f.C;
-        a.PMAX = f.PMAX;
+        a.S = f.S;
+        a.tiles_per = f.tiles_per;
         a.plan = h->plan;
-        a.qtab = qtab;
-        a.qsc = qsc;
+        a.q = q;
+        a.AkT = h->AkT32;
         a.part = part;
-        a.cnt = cnt;
         a.tab = h->tab;
-        a.UvT = h->UvT32;
-        a.muv = h->muv32;
-        a.out = out;
         a.status = h->status;
+        aatc_status st;
         if (f.NT == 1) {
-            if (f.groups <= 2) return launch_fast<2, 1, 12>(f, a, s);
-            if (f.groups <= 3) return launch_fast<3, 1, 12>(f, a, s);
-            return launch_fast<4, 1, 12>(f, a, s);
+            if (f.groups <= 2) st = launch_fast<2, 1, 12>(f, a, h->dtype, s);
+            else if (f.groups <= 3) st = launch_fast<3, 1, 12>(f, a, h->dtype, s);
+            else st = launch_fast<4, 1, 12>(f, a, h->dtype, s);
+        } else {
+            if (f.groups <= 2) st = launch_fast<2, 2, 8>(f, a, h->dtype, s);
+            else if (f.groups <= 3) st = launch_fast<3, 2, 8>(f, a, h->dtype, s);
+            else st = launch_fast<4, 2, 8>(f, a, h->dtype, s);
         }
-        if (f.groups <= 2) return launch_fast<2, 2, 8>(f, a, s);
-        if (f.groups <= 3) return launch_fast<3, 2, 8>(f, a, s);
-        return launch_fast<4, 2, 8>(f, a, s);
+        if (st != AATC_OK) return st;
+        return launch_combine(f, h, part, out, s);
     }
     if (h->W > GEN_MAX_W) return aatc_fail(AATC_ERR_UNSUPPORTED, "record of %d words", h->W);
     SplitPlan p = plan_splits(B, h->Hkv, L);

@@ -130,6 +130,8 @@ aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B,
                        int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
 {
     if (L_new == 0 || B == 0) return AATC_OK;
+    if (h->dtype == AATC_BF16 && h->tmap_ok && h->W <= 16)
+        return encode_tc_run(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
     const size_t smem = (size_t)D * D * 4 + (size_t)ENC_TILE * (D + 1) * 4 +
                         (size_t)ENC_TILE * (h->W + 1) * 4;
     const dim3 grid((L_new + ENC_TILE - 1) / ENC_TILE, h->Hkv, 2 * B);

@@ -1,0 +1,484 @@
+// encode_tc.cu -- tensor-core encoder for bf16 keys/values.
+//
+// Transform, quantize and bit-pack ("Attention-Aware Transform Coding Guide:
+// KV Compression", section "End-to-End Implementation": rotate into the
+// calibrated basis, quantize each channel at its allocated width; "Spend
+// Bits Where Queries Look", Abstract: fixed per-token bit count).
+//
+// The transform c = T x of a 128-token block is a dense 128 x 128 x 128
+// contraction, done by tcgen05.mma: A = the bf16 token rows (exact), B = T
+// split in three bf16 terms T1 + T2 + T3 (about 24 significant bits, so c is
+// as accurate as an fp32 product), accumulated in fp32 in tensor memory.
+// T's rows are stored in record order, so accumulator column n is the code
+// at record position n and the epilogue packs codes front to back.
+//
+// One persistent CTA per SM works through a contiguous range of (head,
+// tensor, batch row, 128-token block) items:
+//   warp 4, one thread: TMA loads (x tiles: 3 stages; T: once per head and
+//       tensor) and MMA issue into two tensor-memory accumulators;
+//   warps 0-3: epilogue, thread = token = tensor-memory lane: read the 128
+//       accumulators, quantize (v = c inv + off, clamp, round half to even),
+//       pack LSB-first into the record and place the words in the tiled
+//       cache layout in shared memory; full aligned blocks leave by one bulk
+//       store, other blocks by per-token stores.
+// Every wait is bounded; a wait that gives up sets the handle's TIMEOUT bit.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace {
+
+constexpr int D = AATC_D;
+constexpr int EB = 128;                 // tokens per block (MMA M)
+constexpr int ESTAGES = 3;
+constexpr int EPI = 4;                  // epilogue warps
+constexpr int ETHREADS = (EPI + 1) * 32;
+constexpr uint32_t XBYTES = EB * D * 2; // 32 KB per x tile
+constexpr uint32_t TBYTES = 3 * D * D * 2;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *mb, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mb)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect(uint64_t *mb, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mb)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *mb)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mb)) : "memory");
+}
+
+// bounded wait of one thread on a phase; false if it gave up
+__device__ __forceinline__ bool mbar_wait1(uint64_t *mb, uint32_t parity)
+{
+    const uint32_t a = smem_u32(mb);
+    // each try may suspend the thread for up to ~20 us until the phase completes
+    for (int it = 0; it < (1 << 16); ++it) {
+        uint32_t done;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(a), "r"(parity), "r"(20000)
+            : "memory");
+        if (done) return true;
+    }
+    return false;
+}
+
+__device__ __forceinline__ void tma2d(void *dst, const void *map, int x, int y, uint64_t *mb)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_u32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(smem_u32(mb))
+        : "memory");
+}
+
+// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the layout a {64, rows} TMA box with 128B swizzle writes)
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// kind::f16 instruction descriptor: bf16 A and B, fp32 accumulator, K-major
+// operands, M = 128, N = 128
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(EB >> 4) << 24);
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t ad, uint64_t bd, uint32_t acc)
+{
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(ad), "l"(bd), "r"(IDESC), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *mb)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mb))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ int key_word_pos(int i, int w, int W)
+{
+    const int r = w >> 2, nr = min(4, W - 4 * r), ii = i & 15;
+    return 16 * W * (i >> 4) + 64 * r + (ii >> 1) * 2 * nr + 2 * (w - 4 * r) + (ii & 1);
+}
+
+struct EncArgs {
+    int B, H, L_new, start_pos, L_cap, W, nblk, n_items;
+    const EncCol *cols;     // [H][2][D]
+    uint32_t *kp, *vp;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(ETHREADS, 1)
+    k_encode_tc(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxv,
+                const __grid_constant__ CUtensorMap mt, EncArgs a)
+{
+    extern __shared__ unsigned char sm_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    unsigned char *Ts = sm;                              // 3 splits x 2 k-halves x 16 KB
+    unsigned char *Xs = Ts + TBYTES;                     // ESTAGES x 32 KB
+    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // 2 x 128 W words (tiled)
+    const int W = a.W;
+    EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + 2 * EB * W);        // [D]
+    __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[2], d_empty[2];
+    __shared__ uint32_t tmem_base;
+    __shared__ int s_fail;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                     "r"(2 * D));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == EPI * 32) {
+        for (int s = 0; s < ESTAGES; ++s) {
+            mbar_init(&x_full[s], 1);
+            mbar_init(&x_empty[s], 1);
+        }
+        mbar_init(&t_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&mma_done[b], 1);
+            mbar_init(&d_empty[b], EPI);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        s_fail = 0;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;");
+    const uint32_t tmem = tmem_base;
+
+    const int per_ht = a.B * a.nblk;
+    const int i0 = (int)((long long)blockIdx.x * a.n_items / gridDim.x);
+    const int i1 = (int)((long long)(blockIdx.x + 1) * a.n_items / gridDim.x);
+    const int count = i1 - i0;
+
+    if (warp == EPI) {
+        if (lane == 0 && count > 0) {
+            // ------------------------------------------------ producer + MMA issue
+            auto issue_x = [&](int n) {
+                const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
+                const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
+                const int row = (b * a.H + h) * a.L_new + blk * EB;
+                const CUtensorMap *map = t ? &mxv : &mxk;
+                const int s = n % ESTAGES;
+                mbar_expect(&x_full[s], XBYTES);
+                tma2d(Xs + s * XBYTES, map, 0, row, &x_full[s]);
+                tma2d(Xs + s * XBYTES + XBYTES / 2, map, 64, row, &x_full[s]);
+            };
+            bool ok = true;
+            for (int n = 0; n < ESTAGES && n < count; ++n) issue_x(n);
+            int ht_loaded = -1, t_uses = 0;
+            for (int n = 0; n < count && ok; ++n) {
+                const int item = i0 + n, ht = item / per_ht;
+                if (ht != ht_loaded) {
+                    // the MMAs reading the old T are done once the previous item's commit arrived
+                    if (n > 0) ok = ok && mbar_wait1(&mma_done[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1));
+                    mbar_expect(&t_full, TBYTES);
+                    for (int sp = 0; sp < 3; ++sp)
+                        for (int kh = 0; kh < 2; ++kh)
+                            tma2d(Ts + (sp * 2 + kh) * (XBYTES / 2), &mt, kh * 64, (ht * 3 + sp) * D, &t_full);
+                    ok = ok && mbar_wait1(&t_full, (uint32_t)(t_uses & 1));
+                    ++t_uses;
+                    ht_loaded = ht;
+                }
+                const int s = n % ESTAGES, buf = n & 1;
+                ok = ok && mbar_wait1(&x_full[s], (uint32_t)((n / ESTAGES) & 1));
+                if (n >= 2) ok = ok && mbar_wait1(&d_empty[buf], (uint32_t)(((n >> 1) - 1) & 1));
+                if (!ok) break;
+                asm volatile("tcgen05.fence::after_thread_sync;");
+                const uint32_t xa = smem_u32(Xs + s * XBYTES), ta = smem_u32(Ts);
+                const uint32_t dcol = tmem + buf * D;
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t koff = (ks >> 2) * (XBYTES / 2) + (ks & 3) * 32;
+                        mma_bf16(dcol, desc_sw128(xa + koff), desc_sw128(ta + sp * XBYTES + koff),
+                                 (uint32_t)(sp > 0 || ks > 0));
+                    }
+                mma_commit(&mma_done[buf]);
+                mma_commit(&x_empty[s]);
+                // refill the stage the previous item used
+                if (n >= 1 && n - 1 + ESTAGES < count) {
+                    const int sp = (n - 1) % ESTAGES;
+                    ok = ok && mbar_wait1(&x_empty[sp], (uint32_t)(((n - 1) / ESTAGES) & 1));
+                    if (ok) issue_x(n - 1 + ESTAGES);
+                }
+            }
+            if (!ok) {
+                atomicOr(a.status, AATC_DEV_TIMEOUT);
+                s_fail = 1;
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue warps
+        int ht_cols = -1;
+        const int i = warp * 32 + lane;     // token within the block = tensor-memory lane
+        for (int n = 0; n < count; ++n) {
+            const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
+            const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
+            if (ht != ht_cols) {
+                asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+                for (int e = tid; e < D; e += EPI * 32) cols_s[e] = a.cols[(size_t)ht * D + e];
+                asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+                ht_cols = ht;
+            }
+            const int buf = n & 1;
+            const bool ok = mbar_wait1(&mma_done[buf], (uint32_t)((n >> 1) & 1));
+            if (!ok || *(volatile int *)&s_fail) {
+                if (!ok) atomicOr(a.status, AATC_DEV_TIMEOUT);
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;");
+            uint32_t *R = Rs + buf * EB * W;
+            // the store of item n-2 read this staging buffer; it has drained
+            // once the issuing thread waited on it (below) and the barrier passed
+            const int tl = i >> 5, ii = i & 31;
+            uint32_t *Rt = R + tl * 32 * W;
+            uint16_t *Rt16 = reinterpret_cast<uint16_t *>(Rt);
+            float fin = 0.f;
+            uint32_t lo = 0;
+            int nb = 0, w = 0;
+            const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16) + buf * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(row_addr + c0, r);
+                EncCol cc[16];   // this chunk's constants, loaded before any store of the chunk
+#pragma unroll
+                for (int q = 0; q < 16; ++q) cc[q] = cols_s[c0 + q];
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const EncCol col = cc[q];
+                    if (col.bits == 0) continue;
+                    const float c = __uint_as_float(r[q]);
+                    fin += c;
+                    float v = fmaf(c, col.inv, col.off);
+                    v = fminf(fmaxf(v, 0.f), col.top);
+                    // adding 1.5 * 2^23 rounds to the nearest integer, ties to even
+                    const uint32_t u = __float_as_uint(v + 12582912.f) & 0xFFu;
+                    lo |= u << nb;
+                    const int nb2 = nb + col.bits;
+                    if (nb2 >= 32) {
+                        if (t == 0) {
+                            Rt[key_word_pos(ii, w, W)] = lo;
+                        } else {
+                            Rt16[2 * (16 * (2 * w) + (ii >> 1)) + (ii & 1)] = (uint16_t)lo;
+                            Rt16[2 * (16 * (2 * w + 1) + (ii >> 1)) + (ii & 1)] = (uint16_t)(lo >> 16);
+                        }
+                        lo = nb2 > 32 ? (u >> (32 - nb)) : 0u;
+                        nb = nb2 - 32;
+                        ++w;
+                    } else {
+                        nb = nb2;
+                    }
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&d_empty[buf]);
+            const int tok = blk * EB + i;
+            if (!(fabsf(fin) <= 3.4e38f) && tok < a.L_new) atomicOr(a.status, AATC_DEV_NONFINITE);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staging -> bulk store
+            asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+            // ---- store the block's records
+            uint32_t *out = (t ? a.vp : a.kp) + ((size_t)b * a.H + h) * (size_t)a.L_cap * W;
+            const int p0 = a.start_pos + blk * EB;
+            const int ntok = min(EB, a.L_new - blk * EB);
+            if (ntok == EB && (p0 & 31) == 0) {
+                if (tid == 0) {
+                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                                     out + (size_t)p0 * W),
+                                 "r"(smem_u32(R)), "r"((uint32_t)(EB * W * 4))
+                                 : "memory");
+                    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+                    // the next use of the other buffer is allowed while this one drains;
+                    // before this buffer is written again (item n+2) at most one group may be pending
+                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                }
+            } else if (t == 0) {
+                // partial block: per-token words (keys)
+                for (int e = tid; e < ntok * W; e += EPI * 32) {
+                    const int ti = e / W, ww = e % W, pos = p0 + ti;
+                    const uint32_t word = R[(ti >> 5) * 32 * W + key_word_pos(ti & 31, ww, W)];
+                    out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, ww, W)] = word;
+                }
+            } else {
+                // partial block: per-token half-words (values)
+                const uint16_t *R16 = reinterpret_cast<const uint16_t *>(R);
+                uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
+                for (int e = tid; e < ntok * 2 * W; e += EPI * 32) {
+                    const int ti = e / (2 * W), q = e % (2 * W), pos = p0 + ti;
+                    const uint16_t hw = R16[2 * ((ti >> 5) * 32 * W + 16 * q + ((ti & 31) >> 1)) + (ti & 1)];
+                    o16[2 * ((size_t)(pos >> 5) * 32 * W + 16 * q + ((pos & 31) >> 1)) + (pos & 1)] = hw;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+        }
+        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;");
+    __syncthreads();
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * D));
+}
+
+// T3 (three bf16 terms of T, rows in record order) and the epilogue columns
+__global__ void k_enc_build(const double *__restrict__ T_k, const double *__restrict__ T_v,
+                            const float *__restrict__ bk32, const float *__restrict__ bv32,
+                            const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
+                            __nv_bfloat16 *__restrict__ T3, EncCol *__restrict__ cols)
+{
+    const int h = blockIdx.x, t = blockIdx.y, n = blockIdx.z, k = threadIdx.x;
+    const HeadPlan &pl = plans[h * 2 + t];
+    const CodecTables &tb = tabs[h * 2 + t];
+    const int j = n < pl.n_coded ? pl.order[n] : -1;
+    const double *T = (t ? T_v : T_k) + (size_t)h * D * D;
+    const double x = j >= 0 ? T[(size_t)j * D + k] : 0.0;
+    const __nv_bfloat16 a1 = __double2bfloat16(x);
+    const double r1 = x - (double)__bfloat162float(a1);
+    const __nv_bfloat16 a2 = __double2bfloat16(r1);
+    const double r2 = r1 - (double)__bfloat162float(a2);
+    const __nv_bfloat16 a3 = __double2bfloat16(r2);
+    __nv_bfloat16 *dst = T3 + (((size_t)(h * 2 + t) * 3) * D + n) * D + k;
+    dst[0] = a1;
+    dst[(size_t)D * D] = a2;
+    dst[(size_t)2 * D * D] = a3;
+    if (k == 0) {
+        EncCol c;
+        if (j >= 0) {
+            const float bias = (t ? bv32 : bk32)[h * D + j];
+            c.inv = tb.inv_step[j];
+            c.off = fmaf(-bias, tb.inv_step[j], tb.mid[j]);
+            c.top = tb.top[j];
+            c.bits = tb.bits[j];
+        } else {
+            c.inv = 0.f;
+            c.off = 0.f;
+            c.top = 0.f;
+            c.bits = 0;
+        }
+        cols[(size_t)(h * 2 + t) * D + n] = c;
+    }
+}
+
+// The driver's tensor-map encoder, found through the runtime so that the
+// library does not link against the driver library itself.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)p;
+    }
+    return fn;
+}
+
+bool encode_tma(CUtensorMap *m, const void *base, unsigned long long rows)
+{
+    const EncodeTiledFn fn = encode_tiled_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t enc_smem(int W) { return 1024 + TBYTES + ESTAGES * XBYTES + 2 * (size_t)EB * W * 4 + D * sizeof(EncCol); }
+
+int sm_count_enc()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        n = (cudaGetDevice(&dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+                ? v
+                : 148;
+    }
+    return n;
+}
+
+}  // namespace
+
+aatc_status enc_build(aatc_calib *h, cudaStream_t s)
+{
+    k_enc_build<<<dim3(h->Hkv, 2, D), D, 0, s>>>(h->T_k, h->T_v, h->bk32, h->bv32, h->tab, h->plan,
+                                                 (__nv_bfloat16 *)h->T3, h->enc_cols);
+    AATC_CUDA(cudaGetLastError());
+    CUtensorMap m;
+    h->tmap_ok = encode_tma(&m, h->T3, (unsigned long long)h->Hkv * 2 * 3 * D);
+    static_assert(sizeof(CUtensorMap) <= sizeof(h->tmap_T3), "tensor map storage");
+    memcpy(h->tmap_T3, &m, sizeof(m));
+    return AATC_OK;
+}
+
+aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new, int start_pos,
+                          int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+{
+    const unsigned long long rows = (unsigned long long)B * h->Hkv * L_new;
+    CUtensorMap mk, mv, mt;
+    if (!encode_tma(&mk, k, rows) || !encode_tma(&mv, v, rows))
+        return aatc_fail(AATC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the encoder inputs");
+    memcpy(&mt, h->tmap_T3, sizeof(mt));
+    EncArgs a;
+    a.B = B;
+    a.H = h->Hkv;
+    a.L_new = L_new;
+    a.start_pos = start_pos;
+    a.L_cap = L_cap;
+    a.W = h->W;
+    a.nblk = (L_new + EB - 1) / EB;
+    a.n_items = h->Hkv * 2 * B * a.nblk;
+    a.cols = h->enc_cols;
+    a.kp = kp;
+    a.vp = vp;
+    a.status = h->status;
+    const size_t smem = enc_smem(h->W);
+    AATC_CUDA(cudaFuncSetAttribute(k_encode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    int grid = sm_count_enc();
+    if (grid > a.n_items) grid = a.n_items;
+    k_encode_tc<<<grid, ETHREADS, smem, s>>>(mk, mv, mt, a);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}

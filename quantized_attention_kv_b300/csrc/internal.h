@@ -43,10 +43,20 @@ struct CodecTables {
 #define AATC_PLAN_SLOTS 32    // record words (keys) or half-words (values) covered
 struct HeadPlan {
     int16_t off[AATC_D];                  // record bit offset of each code, -1 if pruned
+    int16_t order[AATC_D];                // channels in record order (first n_coded entries)
+    int32_t n_coded;                      // channels with b_j > 0
     int32_t max_pieces;                   // largest number of pieces in one byte
     uint32_t mask[AATC_PLAN_SLOTS][8];    // keys: per record word; values: per half-word
     int8_t ch[AATC_PLAN_SLOTS][8][2];     // channel of the piece in the low/high half, -1 = none
     int8_t ex[AATC_PLAN_SLOTS][8][2];     // code bit offset of the piece minus p
+};
+
+// Encoder epilogue constants of one record-order column n (channel order[n]):
+// v = c * inv + off is the quantizer input c/Delta + mid with the bias T mu
+// folded in; codes are clamp(rint(v), 0, top); bits = 0 past n_coded.
+struct __align__(16) EncCol {
+    float inv, off, top;
+    int32_t bits;
 };
 
 struct aatc_calib {
@@ -67,6 +77,13 @@ struct aatc_calib {
     float *muv32;             // [H][d]
     CodecTables *tab;         // [H][2]
     HeadPlan *plan;           // [H][2] record layout and decode masks
+    // tensor-core encoder operands (bf16 inputs): T split in three bf16 terms
+    // T = T1 + T2 + T3 with rows in record order, [H][2][3][d][d]; and the
+    // epilogue columns [H][2][d]
+    void *T3;
+    EncCol *enc_cols;
+    alignas(64) unsigned char tmap_T3[128];   // CUtensorMap over T3 (rows x 128 bf16)
+    bool tmap_ok;
     bool fast_layout;         // every record byte of every head holds <= AATC_PIECES pieces
     uint32_t *status;         // device status word
 };
@@ -97,7 +114,12 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
 // Host-side plan of one bit allocation (exposed for the ABI tests).
 void plan_one(const int32_t *bits, int W, HeadPlan *out);
 
-// ---- encode (encode.cu) ----
+// Build T3, enc_cols and the T3 tensor map (after the plans are on the device).
+aatc_status enc_build(aatc_calib *h, cudaStream_t s);
+
+// ---- encode (encode.cu, encode_tc.cu) ----
+aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
+                          int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s);
 aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
                        int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s);
 

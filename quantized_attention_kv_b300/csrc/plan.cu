@@ -64,6 +64,8 @@ void plan_one(const int32_t *bits, int W, HeadPlan *out)
 
     int order[D];
     const int n = record_order(bits, order);
+    out->n_coded = n;
+    for (int a = 0; a < D; ++a) out->order[a] = (int16_t)(a < n ? order[a] : -1);
     const int nbytes = 4 * W;
     std::vector<std::vector<Piece>> by(nbytes);
     int pos = 0;
@@ -138,5 +140,7 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
     }
     h->fast_layout = fast;
     AATC_CUDA(cudaMemcpy(h->plan, plans.data(), sizeof(HeadPlan) * plans.size(), cudaMemcpyHostToDevice));
-    return AATC_OK;
+    aatc_status st = enc_build(h, 0);
+    if (st == AATC_OK) AATC_CUDA(cudaDeviceSynchronize());
+    return st;
 }

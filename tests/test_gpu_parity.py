@@ -132,6 +132,45 @@ def test_encode_matches_oracle_with_imported_calibration(L_new, start, L_cap):
     g.check()
 
 
+_bf16_cache = {}
+
+
+def _bf16_two_heads():
+    """Llama-shaped bf16 calibration of two KV heads (oracle), for the tensor-core encoder."""
+    if not _bf16_cache:
+        wl = synth.dataclasses.replace(WL["llama_32k"], n_kv_heads=2, n_q_heads=8)
+        k, v, q = synth.calib_inputs(wl, device="cuda")
+        _bf16_cache.update(wl=wl, ocal=_oracle_cal(k, v, q, wl.bits))
+    return _bf16_cache
+
+
+@pytest.mark.parametrize("L_new,start,L_cap,B", [(1024, 0, 1024, 2), (1000, 24, 1056, 2), (1, 7, 32, 1),
+                                                 (300, 64, 384, 3), (257, 0, 288, 1)])
+def test_encode_bf16_tensor_core_path(L_new, start, L_cap, B):
+    """bf16 inputs go through the tensor-core encoder: full aligned 128-token
+    blocks leave by bulk store, ragged or unaligned ones by per-token stores."""
+    c = _bf16_two_heads()
+    wl, ocal = c["wl"], c["ocal"]
+    W = ocal["W"]
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=L_new, batch=B)
+    kp = torch.full((B, 2, L_cap, W), -1, dtype=torch.int32, device="cuda")
+    vp = kp.clone()
+    aatc.encode(g, kc, vc, kp, vp, start_pos=start)
+    torch.cuda.synchronize()
+    for t, kind, x, p in (("k", oracle.KEYS, kc, kp), ("v", oracle.VALUES, vc, vp)):
+        _, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
+        got = _records(p, W, kind, L_new, start)
+        for h in range(2):
+            compare_codes(got[:, h], codes[:, h], pre[:, h], ocal["bits_" + t][h])
+        cc = as_u32(p).reshape(B * 2, -1).copy()
+        ones = np.full((L_new, W), 0xFFFFFFFF, dtype=np.uint32)
+        for r in range(B * 2):
+            oracle.cache_put(ones, kind, cache=cc[r], start=start)
+        assert np.all(cc == 0xFFFFFFFF), t
+    g.check()
+
+
 def test_encode_writes_the_oracle_cache_bit_for_bit():
     """Away from rounding ties the whole tiled cache equals the oracle's."""
     c = _tiny()
