@@ -21,7 +21,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Sizes of the arena pieces, in the order they are carved.
 struct Layout {
-    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, t3, cols, total;
+    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, dblob, t3, cols, total;
 };
 
 Layout layout_for(int H)
@@ -35,10 +35,11 @@ Layout layout_for(int H)
     L.f32_mat = up((size_t)H * D * D * sizeof(float));
     L.tabs = up((size_t)H * 2 * sizeof(CodecTables));
     L.plans = up((size_t)H * 2 * sizeof(HeadPlan));
+    L.dblob = up((size_t)H * sizeof(DecBlob));
     L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
     L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
     L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
-              L.plans + L.t3 + L.cols + 1024;
+              L.plans + L.dblob + L.f32_vec + L.t3 + L.cols + 1024;
     return L;
 }
 
@@ -81,6 +82,8 @@ aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib 
     h->UvT32 = (float *)take(L.f32_mat);
     h->tab = (CodecTables *)take(L.tabs);
     h->plan = (HeadPlan *)take(L.plans);
+    h->dblob = (DecBlob *)take(L.dblob);
+    h->vcst = (float *)take(L.f32_vec);
     p = (char *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);   // T3: TMA source, keep it well aligned
     h->T3 = take(L.t3);
     h->enc_cols = (EncCol *)take(L.cols);

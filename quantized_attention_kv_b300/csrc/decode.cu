@@ -58,10 +58,11 @@ int sm_count()
 }
 
 // =============================================================== fast path
-constexpr int FSTAGES = 3;       // tiles in flight per warp
 constexpr int PSTRIDE = 40;      // halfs per row of the per-warp P buffer (32 tokens + pad)
 constexpr int FAST_MAX_W = 16;
 constexpr int PROW = 4 + D;      // floats per partial: m, l, 2 pad, acc[D] (acc 16-byte aligned)
+constexpr int PSH = 6;           // P operands carry p * 2^PSH
+constexpr float RESCALE_T = 8.f; // the running maximum is raised once a score exceeds it by this (log2)
 
 // Work split: every (batch row, KV head, head group) is a "unit" of
 // n_tiles = ceil(L/32) tiles, cut into S = max(1, resident CTAs / units)
@@ -71,7 +72,9 @@ struct FastGeom {
     int NT;          // 8-column n-tiles (each: 4 query heads x hi/lo)
     int HPG;         // query heads per head group (4 NT)
     int HG;          // head groups per KV head
+    int GMAX;        // value groups the kernel variant holds (>= groups)
     int FW;          // warps per CTA
+    int FST;         // tiles in flight per warp
     int rows;        // key rows of 4 record words
     int groups;      // value groups of 8 half-words
     int ksteps;      // 4 rows
@@ -79,22 +82,38 @@ struct FastGeom {
     int units;       // B * Hkv * HG
     int S;           // splits (CTAs, partial slots) per unit
     int tiles_per;   // tiles per split
-    size_t stage_bytes, smem, ws_part, ws_total;
+    size_t stage_bytes, stage_region, uv_off, smem, ws_total;
 };
 
-size_t fast_smem(int FW, int W, int groups, int HPG, int NT, int ksteps, int rows)
+// Shared memory of k_decode_fast, in carve order.
+struct FastSmem {
+    size_t stages, mat, blob, qtab, pbuf, mbar, scr, total;
+    size_t uv_off;
+};
+
+FastSmem fast_smem_layout(int FW, int FST, int W, int NT, int ksteps, int groups)
 {
-    const size_t SB = 256 * (size_t)W + 512;
-    const size_t rows_tot = 64 * (size_t)groups;
-    const size_t merge = (size_t)FW * (rows_tot + 2) * HPG * 4 + (size_t)D * HPG * 4;
-    size_t big = (size_t)FW * FSTAGES * SB;
-    big = big > merge ? big : merge;
-    big = (big + 127) & ~(size_t)127;
-    return big + (size_t)FW * FSTAGES * 8 + (size_t)FW * 16 * PSTRIDE * 2 + (size_t)ksteps * NT * 32 * 8 +
-           (size_t)rows * 4 * 8 * 4 + (size_t)groups * 64 * 4 + 256 * 2 + 8 * 4 + 2 * 8 * D * 4 + 256 * 2 + 16;
+    FastSmem m;
+    const int HPG = 4 * NT;
+    const size_t tiles = (size_t)FW * FST * 256 * W;
+    // epilogue: the warps' piece sums, then Delta_V o channel sums [D][8], partial outputs [4][8][D]
+    m.uv_off = ((size_t)FW * 64 * groups * HPG * 4 + 127) & ~(size_t)127;
+    const size_t epi_region = m.uv_off + (size_t)D * 8 * 4 + (size_t)4 * 8 * D * 4;
+    m.stages = tiles > epi_region ? tiles : epi_region;
+    m.mat = (size_t)D * D * 4;   // A_k^T, then Uv^T
+    m.blob = sizeof(DecBlob);
+    m.qtab = (size_t)ksteps * NT * 32 * 8;
+    m.pbuf = (size_t)FW * 8 * NT * PSTRIDE * 2;
+    m.mbar = (((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15;
+    const size_t pro = ((size_t)D * 8 + (size_t)HPG * D) * 4;   // query rows, q'
+    const size_t epi = (size_t)2 * FW * HPG * 4;                 // warp maxima and sums
+    m.scr = pro > epi ? pro : epi;
+    m.total = m.stages + m.mat + m.blob + m.qtab + m.pbuf + m.mbar + m.scr;
+    return m;
 }
 
-int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem);
+int fast_ctas_per_sm(int GMAX, int NT, int FW, size_t smem);
+int sm_limit_bytes();
 
 FastGeom fast_geom(const aatc_calib *h, int B, int L)
 {
@@ -102,22 +121,30 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.NT = h->G <= 4 ? 1 : 2;
     f.HPG = 4 * f.NT;
     f.HG = (h->G + f.HPG - 1) / f.HPG;
-    f.FW = f.NT == 1 ? 12 : 8;
     f.rows = (h->W + 3) / 4;
     f.groups = (2 * h->W + 7) / 8;
+    f.GMAX = f.groups <= 2 ? 2 : (f.groups <= 3 ? 3 : 4);
+    f.FW = f.NT == 2 ? 8 : (f.GMAX <= 3 ? 16 : 12);
     f.ksteps = 4 * f.rows;
+    f.FST = 3;
+    FastSmem m = fast_smem_layout(f.FW, f.FST, h->W, f.NT, f.ksteps, f.groups);
+    if (m.total > (size_t)sm_limit_bytes()) {
+        f.FST = 2;
+        m = fast_smem_layout(f.FW, f.FST, h->W, f.NT, f.ksteps, f.groups);
+    }
+    f.smem = m.total;
+    f.stage_region = m.stages;
+    f.uv_off = m.uv_off;
+    f.stage_bytes = (size_t)256 * h->W;
     f.n_tiles = L > 0 ? (L + TILE - 1) / TILE : 0;
     f.units = B * h->Hkv * f.HG;
-    f.smem = fast_smem(f.FW, h->W, f.groups, f.HPG, f.NT, f.ksteps, f.rows);
-    const int per_sm = fast_ctas_per_sm(f.groups, f.NT, f.FW, f.smem);
+    const int per_sm = fast_ctas_per_sm(f.GMAX, f.NT, f.FW, f.smem);
     const int C = sm_count() * per_sm;
     f.S = C / f.units > 1 ? C / f.units : 1;
     if (f.S > f.n_tiles) f.S = f.n_tiles > 0 ? f.n_tiles : 1;
     f.tiles_per = f.n_tiles > 0 ? (f.n_tiles + f.S - 1) / f.S : 1;
     f.S = f.n_tiles > 0 ? (f.n_tiles + f.tiles_per - 1) / f.tiles_per : 1;
-    f.stage_bytes = 256 * (size_t)h->W + 512;
-    f.ws_part = (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
-    f.ws_total = f.ws_part;
+    f.ws_total = (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
     return f;
 }
 
@@ -184,631 +211,687 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^x for x = -inf or a finite value in the normal range (hardware exp2).
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Exact power of two 2^e, e in [-126, 127].
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
+
 struct FastArgs {
     const uint32_t *kp, *vp;
     const int32_t *seq_lens;
-    int L, L_cap, W, rows, groups, Hkv, G, HG, HPG, n_tiles, units, S, tiles_per;
-    const HeadPlan *plan;
+    int L, L_cap, W, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;
+    uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
+    uint32_t uv_off;        // epilogue: offset of Uv^T in the stage region (after the warp sums)
+    const DecBlob *blob;    // [Hkv]
+    const float *UvT;       // [Hkv][D][D]
     const void *q;          // [B][Hq][D] of the handle's dtype
     const float *AkT;       // [Hkv][D][D]
     float *part;            // [units][S][HPG][PROW]
-    const CodecTables *tab;
     uint32_t *status;
 };
 
+// One CTA = one split of one unit.  Every warp streams its own tiles
+// (tile ta + warp + i FW of the split) through FST shared-memory stages.
+//
+// Scores (per half-tile of 16 tokens): A = key pieces (rows = tokens 2g and
+// 2g+1 of the half, k = record pieces), B = query weights (8 columns = 4
+// heads x hi/lo fp16 parts of q'), fp32 accumulation on mma.sync.  P.V: A =
+// value pieces (rows = pieces of 8 half-words), B = P (k = tokens, columns =
+// heads x hi/lo fp16 parts of p * 2^PSH).  The softmax maximum is raised
+// only when a score exceeds it by RESCALE_T, so p * 2^PSH stays below 2^14.
+// Each tile's P.V starts from zero and is added to the running sums in
+// fp32, so the tensor-core accumulation (which does not round to nearest)
+// never carries more than one tile.
 template <int GMAX, int NT, int FW, typename QT>
-__global__ void __launch_bounds__(FW * 32) k_decode_fast(FastArgs a)
+__global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
+    constexpr int HPG = 4 * NT;
     asm volatile("griddepcontrol.launch_dependents;");   // the combine kernel may start its prologue
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int g = lane >> 2, c = lane & 3;
-    const int W = a.W, rows = a.rows, groups = a.groups, HPG = a.HPG;
+    const int W = a.W, rows = a.rows, groups = a.groups, FST = a.FST;
     const int ksteps = rows * 4;
+    const uint32_t SB = 256u * W, tile_bytes = 128u * W;
 
-    // shared memory carve-up (sizes as in fast_smem)
-    const size_t SB = 256 * (size_t)W + 512;
-    const size_t rows_tot = 64 * (size_t)groups;
-    const size_t merge = (size_t)FW * (rows_tot + 2) * HPG * 4 + (size_t)D * HPG * 4;
-    size_t big = (size_t)FW * FSTAGES * SB;
-    big = big > merge ? big : merge;
-    big = (big + 127) & ~(size_t)127;
+    // shared memory carve-up (as in fast_smem_layout)
     unsigned char *stage_base = smem;
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(smem + big);
-    __half *pbuf = reinterpret_cast<__half *>(mbar + FW * FSTAGES);
-    uint2 *qtab_s = reinterpret_cast<uint2 *>(pbuf + FW * 16 * PSTRIDE);
-    uint32_t *kmask_s = reinterpret_cast<uint32_t *>(qtab_s + ksteps * NT * 32);
-    uint32_t *vmask_s = kmask_s + rows * 4 * 8;
-    int16_t *vrow_s = reinterpret_cast<int16_t *>(vmask_s + groups * 64);   // [groups*64] (ch << 8 | ex + 64)
-    float *sc_s = reinterpret_cast<float *>(vrow_s + 256);
-    float *qs = sc_s + 8;                     // [8][D] query rows of the head group
-    float *pa = qs + 8 * D;                   // [8][D] q' of the head group
-    int16_t *slot_s = reinterpret_cast<int16_t *>(pa + 8 * D);   // [16][8][2] key piece: ch | (ex + 64) << 8
-    __shared__ float cm[8], cl[8], cs[8][FW];
-    __shared__ float S_s[8];
-    __shared__ float ksc_s[D];                 // Delta_K / sqrt(d), 0 for pruned channels
-    __shared__ float vmid_s[256];              // value piece midpoints (2^w-1)/2 * 2^(p-24), per row
+    float *mat_s = reinterpret_cast<float *>(smem + a.stage_region);   // [D][D]: A_k^T, then Uv^T
+    DecBlob *blob_s = reinterpret_cast<DecBlob *>(mat_s + D * D);
+    uint2 *qtab_s = reinterpret_cast<uint2 *>(blob_s + 1);
+    __half *pbuf = reinterpret_cast<__half *>(qtab_s + ksteps * NT * 32);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(pbuf + FW * 8 * NT * PSTRIDE);   // [FW][FST], blob, mat
+    float *scr = reinterpret_cast<float *>(
+        reinterpret_cast<unsigned char *>(mbar) + ((((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15));
+    __shared__ int mxi[8];
+    __shared__ float cm[8], cl[8];
 
-    uint64_t *my_mbar = mbar + warp * FSTAGES;
-    unsigned char *my_stage = stage_base + (size_t)warp * FSTAGES * SB;
-    const uint32_t tile_bytes = 128u * W;
+    // ---- this CTA: unit u, split sp, tiles [ta, tb) of the unit
+    const int u = blockIdx.x / a.S, sp = blockIdx.x % a.S;
+    const int b = u / (a.Hkv * a.HG), h = (u / a.HG) % a.Hkv, hg = u % a.HG;
+    const int ta = sp * a.tiles_per, tb = min(ta + a.tiles_per, a.n_tiles);
+    const size_t slab = ((size_t)b * a.Hkv + h) * (size_t)a.L_cap * W;
+    uint64_t *my_mbar = mbar + warp * FST;
+    uint64_t *blob_bar = mbar + FW * FST;
+    uint64_t *mat_bar = blob_bar + 1;   // phase 0: A_k^T, phase 1: Uv^T
+    unsigned char *my_stage = stage_base + (size_t)warp * FST * SB;
+
+    // Barriers first (the init fence waits for the thread's outstanding memory
+    // operations), then the copies the prologue needs, ahead of the tile burst.
+    // The one-shot code here is kept short: it runs from a cold instruction cache.
     if (lane == 0) {
-        for (int s = 0; s < FSTAGES; ++s) mbar_init(&my_mbar[s], 1);
+        for (int s = 0; s < FST; ++s) mbar_init(&my_mbar[s], 1);
+        if (warp == 0) {
+            mbar_init(blob_bar, 1);
+            mbar_init(mat_bar, 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    __syncthreads();
-    // The warp's n-th tile (over all its segments) goes through stage n % FSTAGES
-    // and completes phase n / FSTAGES of that stage's barrier.
-    int n_issued = 0, n_done = 0;
-
+    __syncwarp();
+    if (tid == 0) {
+        mbar_arrive_expect(blob_bar, (uint32_t)sizeof(DecBlob));
+        bulk_g2s(blob_s, a.blob + h, (uint32_t)sizeof(DecBlob), blob_bar);
+        mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
+        bulk_g2s(mat_s, a.AkT + (size_t)h * D * D, (uint32_t)(D * D * 4), mat_bar);
+    }
+    // query rows of the head group: element e = (head e / D, k = e % D)
+    constexpr int QPER = (HPG * D + NTH - 1) / NTH;
+    float qv[QPER];
     {
-        // ---- this CTA: unit u, split sp, tiles [ta, tb) of the unit
-        const int u = blockIdx.x / a.S, sp = blockIdx.x % a.S;
-        const int ta = sp * a.tiles_per, tb = min(ta + a.tiles_per, a.n_tiles);
-        const int b = u / (a.Hkv * a.HG), h = (u / a.HG) % a.Hkv, hg = u % a.HG;
-        const int len = a.seq_lens ? min(max(a.seq_lens[b], 0), a.L) : a.L;
-        const int t0 = ta, t1 = min(tb, (len + TILE - 1) / TILE);
-        const size_t slab = ((size_t)b * a.Hkv + h) * (size_t)a.L_cap * W;
-
-        auto issue = [&](int tile, int s) {
-            unsigned char *dst = my_stage + s * SB;
-            mbar_arrive_expect(&my_mbar[s], 2 * tile_bytes);
-            bulk_g2s(dst, a.kp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
-            bulk_g2s(dst + tile_bytes, a.vp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
-        };
-        for (int i = 0; i < FSTAGES; ++i) {
-            const int tile = t0 + warp + i * FW;
-            if (tile < t1) {
-                if (lane == 0) issue(tile, n_issued % FSTAGES);
-                ++n_issued;
-            }
+        const QT *qg = reinterpret_cast<const QT *>(a.q);
+        const int Hq = a.Hkv * a.G;
+#pragma unroll
+        for (int r = 0; r < QPER; ++r) {
+            const int e = tid + r * NTH, gi = hg * HPG + (e >> 7);
+            qv[r] = (e < HPG * D && gi < a.G) ? to_f32(qg[((size_t)b * Hq + h * a.G + gi) * D + (e & (D - 1))]) : 0.f;
         }
+    }
+    const int len = a.seq_lens ? min(max(a.seq_lens[b], 0), a.L) : a.L;
 
-        // ---- tables of this unit and its query weights.  All global loads of
-        // the prologue are issued before any is used: one round trip.
-        const HeadPlan &pk = a.plan[h * 2 + 0];
-        const HeadPlan &pv = a.plan[h * 2 + 1];
+    auto issue = [&](int tile, int s) {
+        unsigned char *dst = my_stage + s * SB;
+        mbar_arrive_expect(&my_mbar[s], 2 * tile_bytes);
+        bulk_g2s(dst, a.kp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
+        bulk_g2s(dst + tile_bytes, a.vp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
+    };
+    // The warp's n-th tile goes through stage n % FST and completes phase
+    // n / FST of that stage's barrier.  The first tiles are requested up to
+    // tb, before the row length has arrived (tiles below tb are inside the
+    // cache); copies past the row's length are drained at the end.
+    int n_issued = 0, n_done = 0;
+    int st_next = 0;          // stage of the next tile to consume
+    uint32_t ph_next = 0;     // its barrier phase parity
+    for (int i = 0; i < FST; ++i) {
+        const int tile = ta + warp + i * FW;
+        if (tile < tb) {
+            if (lane == 0) issue(tile, i);
+            ++n_issued;
+        }
+    }
+    const int t1 = min(tb, (len + TILE - 1) / TILE);
+
+    // ---- query weights of the head group: q' = (A_k q) o Delta_K / sqrt(d),
+    // scaled per head by a power of two S_i, split into fp16 hi/lo parts and
+    // laid out as mma.sync B fragments.
+    float sc[NT];   // log2-domain score scale of head 4t + c: 2^24 / S_i * log2(e)
+    bool ok;
+    {
+        float *q_s = scr;              // [D][8] query rows, transposed
+        float *pa = scr + D * 8;       // [HPG][D] q'
+#pragma unroll
+        for (int r = 0; r < QPER; ++r) {
+            const int e = tid + r * NTH;
+            if (e < HPG * D) q_s[(e & (D - 1)) * 8 + (e >> 7)] = qv[r];
+        }
+        if (tid < 8) mxi[tid] = 0;
+        __syncthreads();
+        ok = mbar_wait(mat_bar, 0);
+        ok = mbar_wait(blob_bar, 0) && ok;
+        // thread (k-split ks, channel j): sum over rows k = ks, ks + KS, ... of A_k^T[k][j] q_i[k]
+        constexpr int KS = NTH / D;
+        float *red = reinterpret_cast<float *>(pbuf);   // [KS][HPG][D], the P buffers are free until the loop
         {
-            // A_k^T: thread (k-set kq, channel quad j4) holds rows k = kq + NTH/32 * m
-            constexpr int KSTEP = NTH / 32;
-            constexpr int KPER = (D + KSTEP - 1) / KSTEP;
-            const int j4 = tid & 31, kq = tid >> 5;
-            float4 av[KPER];
-            const float4 *Ag = reinterpret_cast<const float4 *>(a.AkT + (size_t)h * D * D) + j4;
-#pragma unroll
-            for (int m = 0; m < KPER; ++m) {
-                const int k = kq + KSTEP * m;
-                av[m] = k < D ? __ldg(Ag + (size_t)k * (D / 4)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            const QT *qg = reinterpret_cast<const QT *>(a.q);
-            const int Hq = a.Hkv * a.G;
-            // every global load of the prologue is issued before any result is stored
-            constexpr int QPER = (8 * D + NTH - 1) / NTH;
-            float qv[QPER];
-#pragma unroll
-            for (int r = 0; r < QPER; ++r) {
-                const int e = tid + r * NTH;
-                const int i = e >> 7, cc = e & (D - 1), gi = hg * HPG + i;
-                qv[r] = (e < 8 * D && i < HPG && gi < a.G) ? to_f32(qg[((size_t)b * Hq + h * a.G + gi) * D + cc]) : 0.f;
-            }
-            const int ek = tid;                       // rows * 32 <= NTH
-            const uint32_t km = ek < rows * 32 ? pk.mask[ek >> 3][ek & 7] : 0u;
-            constexpr int VPER = (4 * 64 + NTH - 1) / NTH;
-            uint32_t vm[VPER];
-            int vch[VPER], vex[VPER];
-#pragma unroll
-            for (int r = 0; r < VPER; ++r) {
-                const int e = tid + r * NTH;
-                const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
-                const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
-                const bool in = e < groups * 64;
-                vm[r] = in ? pv.mask[e >> 3][e & 7] : 0u;
-                vch[r] = in ? pv.ch[hw][k][0] : -1;
-                vex[r] = in ? pv.ex[hw][k][0] : 0;
-            }
-            const int es = tid;                       // 16 * 16 <= NTH
-            int sch = -1, sex = 0;
-            if (es < 256) {
-                sch = pk.ch[es >> 4][(es >> 1) & 7][es & 1];
-                sex = pk.ex[es >> 4][(es >> 1) & 7][es & 1];
-            }
-            const CodecTables &tk = a.tab[h * 2 + 0];
-            const float ksc = tid < D ? (tk.bits[tid] ? tk.step[tid] * 0.08838834764831845f : 0.f) : 0.f;
-            // ... then stored
-#pragma unroll
-            for (int r = 0; r < QPER; ++r) {
-                const int e = tid + r * NTH;
-                if (e < 8 * D) {
-                    qs[e] = qv[r];
-                    pa[e] = 0.f;
-                }
-            }
-            if (ek < rows * 32) kmask_s[ek] = km;
-#pragma unroll
-            for (int r = 0; r < VPER; ++r) {
-                const int e = tid + r * NTH;
-                if (e < groups * 64) {
-                    vmask_s[e] = vm[r];
-                    // row e = (group, m4, rr): half-word 8 group + rr%8, slot 2 m4 + rr/8; the
-                    // slot's mask holds (2^w - 1) << p per half: low half / 2 = midpoint * 2^p
-                    const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
-                    const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
-                    (void)hw;
-                    (void)k;
-                    vrow_s[e] = (int16_t)(vch[r] < 0 ? -1 : (vch[r] << 8) | (vex[r] + 64));
-                    vmid_s[e] = 0.f;
-                }
-            }
-            if (es < 256) slot_s[es] = (int16_t)(sch < 0 ? -1 : (sch | ((sex + 64) << 8)));
-            if (tid < D) ksc_s[tid] = ksc;
-            __syncthreads();
-            for (int e = tid; e < groups * 64; e += NTH) {
-                const int gr = e >> 6, m4 = (e >> 4) & 3, rr = e & 15;
-                const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
-                vmid_s[e] = ldexpf((float)(vmask_s[hw * 8 + k] & 0xFFFFu), -25);
-            }
-            // q'_i[j] = sum_k A_k[j][k] q_i[k]: partial sums over this thread's rows
-            float4 acc4[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int m = 0; m < KPER; ++m) {
-                const int k = kq + KSTEP * m;
-                if (k >= D) break;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    if (i >= HPG) break;
-                    const float qv = qs[i * D + k];
-                    acc4[i].x = fmaf(av[m].x, qv, acc4[i].x);
-                    acc4[i].y = fmaf(av[m].y, qv, acc4[i].y);
-                    acc4[i].z = fmaf(av[m].z, qv, acc4[i].z);
-                    acc4[i].w = fmaf(av[m].w, qv, acc4[i].w);
+            const int j = tid & (D - 1), ks = tid >> 7;
+            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+            for (int k = ks; k < D; k += KS) {
+                const float av = mat_s[k * D + j];
+                const float4 q0 = *reinterpret_cast<const float4 *>(&q_s[k * 8]);
+                o[0] = fmaf(av, q0.x, o[0]);
+                o[1] = fmaf(av, q0.y, o[1]);
+                o[2] = fmaf(av, q0.z, o[2]);
+                o[3] = fmaf(av, q0.w, o[3]);
+                if (HPG > 4) {
+                    const float4 q1 = *reinterpret_cast<const float4 *>(&q_s[k * 8 + 4]);
+                    o[4] = fmaf(av, q1.x, o[4]);
+                    o[5] = fmaf(av, q1.y, o[5]);
+                    o[6] = fmaf(av, q1.z, o[6]);
+                    o[7] = fmaf(av, q1.w, o[7]);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (i >= HPG) break;
-                float *d = pa + i * D + 4 * j4;
-                atomicAdd(d + 0, acc4[i].x);
-                atomicAdd(d + 1, acc4[i].y);
-                atomicAdd(d + 2, acc4[i].z);
-                atomicAdd(d + 3, acc4[i].w);
-            }
-            __syncthreads();
-            for (int e = tid; e < HPG * D; e += NTH) pa[e] *= ksc_s[e & (D - 1)];
-            __syncthreads();
-            if (warp < HPG) {   // warp i: largest |q'| of head i -> power-of-two scale
-                float mx = 0.f;
-                for (int k = lane; k < D; k += 32) mx = fmaxf(mx, fabsf(pa[warp * D + k]));
-                for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                if (lane == 0) {
-                    // pieces carry 2^ex with ex <= 7: keep mx * 2^7 * S below 2^13
-                    int e = 0;
-                    if (mx > 0.f) frexpf(mx, &e);
-                    const float S = mx > 0.f ? ldexpf(1.f, 6 - e) : 1.f;
-                    S_s[warp] = S;
-                    sc_s[warp] = ldexpf(1.f, 24) / S * LOG2E;
-                }
-            }
-            __syncthreads();
-            // B fragments: entry (kstep, n-tile t, lane) = (b0, b1), column n = 8t + lane/4 =
-            // (head n/2, hi if n even else lo), k-step (r, s) from record word 4r + lane%4,
-            // slots 2s (b0) and 2s+1 (b1), low half first; weight = q'_ch * 2^ex * S
-            for (int en = tid; en < ksteps * NT * 32; en += NTH) {
-                const int ln = en & 31, t = (en >> 5) % NT, ks = (en >> 5) / NT;
-                const int r = ks >> 2, s4 = ks & 3;
-                const int n = 8 * t + (ln >> 2), i = n >> 1, part = n & 1;
-                const int w = 4 * r + (ln & 3);
-                uint32_t o2[2];
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int k = 2 * s4 + rr;
-                    float v2[2];
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const int sl = slot_s[(w * 8 + k) * 2 + half];
-                        float val = 0.f;
-                        if (sl >= 0 && i < HPG && hg * HPG + i < a.G)
-                            val = ldexpf(pa[i * D + (sl & 255)] * S_s[i], (sl >> 8) - 64);
-                        const float hi = __half2float(__float2half_rn(val));
-                        v2[half] = part ? val - hi : hi;
-                    }
-                    o2[rr] = pack_half2(v2[0], v2[1]);
-                }
-                qtab_s[en] = make_uint2(o2[0], o2[1]);
-            }
+            for (int i = 0; i < HPG; ++i) red[(ks * HPG + i) * D + j] = o[i];
         }
         __syncthreads();
-
-        float m_run[NT], l_run[NT], sc[NT];
-        float acc[GMAX][4][NT][4];
+        // A_k^T is used up: Uv^T for the epilogue comes into the same buffer
+        if (tid == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
+            bulk_g2s(mat_s, a.UvT + (size_t)h * D * D, (uint32_t)(D * D * 4), mat_bar);
+        }
+        // q' = sum over the k-splits, times Delta_K / sqrt(d); largest |q'| per head
+        for (int e = tid; e < HPG * D; e += NTH) {   // a warp's 32 entries share one head
+            const int i = e >> 7, j = e & (D - 1);
+            float v = 0.f;
+            for (int ks = 0; ks < KS; ++ks) v += red[(ks * HPG + i) * D + j];
+            v = ok ? v * blob_s->ksc[j] : 0.f;
+            pa[e] = v;
+            float mx = fabsf(v);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            m_run[t] = -INFINITY;
-            l_run[t] = 0.f;
-            sc[t] = sc_s[4 * t + c];
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) atomicMax(&mxi[i], __float_as_int(mx));
+        }
+        __syncthreads();
+        // S_i = 2^(6 - e_i) with max|q'_i| = f 2^e_i, f in [0.5, 1): weights below 2^(6 + 7)
+        auto s_exp = [&](int i) -> int {
+            const int bits = mxi[i];
+            const int e = bits > 0 ? ((bits >> 23) & 255) - 126 : 6;
+            return max(-100, min(100, 6 - e));
+        };
+        // B fragments: entry (kstep, n-tile t, lane) = (b0, b1), column n = 8t + lane/4 =
+        // (head n/2, hi if n even else lo), k-step (r, s4) from record word 4r + lane%4,
+        // slots 2 s4 (b0) and 2 s4 + 1 (b1), low half first; weight = q'_ch * 2^ex * S
+        for (int en = tid; en < ksteps * NT * 32; en += NTH) {
+            const int ln = en & 31, t = (en >> 5) % NT, ks = (en >> 5) / NT;
+            const int r = ks >> 2, s4 = ks & 3;
+            const int n = 8 * t + (ln >> 2), i = n >> 1, part = n & 1;
+            const int w = 4 * r + (ln & 3);
+            const bool live = hg * HPG + i < a.G;
+            const int se = s_exp(i);
+            uint32_t o2[2];
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int k = 2 * s4 + rr;
+                float v2[2];
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int sl = blob_s->kslot[w][k][half];
+                    float val = 0.f;
+                    if (sl >= 0 && live) val = pa[i * D + (sl & 255)] * pow2i(se + (sl >> 8) - 64);
+                    const float hi = __half2float(__float2half_rn(val));
+                    v2[half] = part ? val - hi : hi;
+                }
+                o2[rr] = pack_half2(v2[0], v2[1]);
+            }
+            qtab_s[en] = make_uint2(o2[0], o2[1]);
         }
 #pragma unroll
-        for (int gr = 0; gr < GMAX; ++gr)
+        for (int t = 0; t < NT; ++t) sc[t] = LOG2E * pow2i(24 - s_exp(4 * t + c));
+    }
+    __syncthreads();
+
+    float m_run[NT], l_run[NT];
+    float acc[GMAX][4][NT][2];   // rows g / g + 8 of each value m-tile, hi + lo columns summed
 #pragma unroll
-            for (int m4 = 0; m4 < 4; ++m4)
+    for (int t = 0; t < NT; ++t) {
+        m_run[t] = -INFINITY;
+        l_run[t] = 0.f;
+    }
+#pragma unroll
+    for (int gr = 0; gr < GMAX; ++gr)
+#pragma unroll
+        for (int m4 = 0; m4 < 4; ++m4)
+#pragma unroll
+            for (int t = 0; t < NT; ++t) acc[gr][m4][t][0] = acc[gr][m4][t][1] = 0.f;
+
+    __half *pw = pbuf + warp * 8 * NT * PSTRIDE;
+    bool failed = !ok;
+    for (int it = 0; !failed; ++it) {
+        const int tile = ta + warp + it * FW;
+        if (tile >= t1) break;
+        const int s = st_next;
+        if (!mbar_wait(&my_mbar[s], ph_next)) {
+            failed = true;
+            break;
+        }
+        ++n_done;
+        if (++st_next == FST) {
+            st_next = 0;
+            ph_next ^= 1u;
+        }
+        const uint32_t *Kt = reinterpret_cast<const uint32_t *>(my_stage + s * SB);
+        const uint32_t *Vt = Kt + TILE * W;
+
+        // ---- scores: C[hf][r & 1] rows g / g+8 = tokens 16 hf + 2g / +1, columns 2c / 2c+1 =
+        // head c hi / lo; two chains per half-tile (even and odd key rows)
+        float C[2][2][NT][4];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+            for (int rp = 0; rp < 2; ++rp)
 #pragma unroll
                 for (int t = 0; t < NT; ++t)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[gr][m4][t][k] = 0.f;
-
-        __half *pw = pbuf + warp * 16 * PSTRIDE;
-        bool failed = false;
-        for (int it = 0;; ++it) {
-            const int tile = t0 + warp + it * FW;
-            if (tile >= t1) break;
-            const int s = n_done % FSTAGES;
-            if (!mbar_wait(&my_mbar[s], (uint32_t)((n_done / FSTAGES) & 1))) {
-                failed = true;
-                break;
+                    for (int k = 0; k < 4; ++k) C[hf][rp][t][k] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            if (r >= rows) break;
+            const int nr = min(4, W - 4 * r);
+            const uint4 mA = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][0]);
+            const uint4 mB = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][4]);
+            const uint32_t mk[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
+            uint32_t x0[2], x1[2], y0[2], y1[2];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const uint2 kw = *reinterpret_cast<const uint2 *>(Kt + hf * 16 * W + 64 * r + g * 2 * nr + 2 * c);
+                x0[hf] = kw.x;
+                x1[hf] = kw.y;
+                y0[hf] = kw.x >> 8;
+                y1[hf] = kw.y >> 8;
             }
-            ++n_done;
-            const uint32_t *Kt = reinterpret_cast<const uint32_t *>(my_stage + s * SB);
-            const uint32_t *Vt = Kt + TILE * W;
-
-            // ---- scores: rows = tokens (row g: 2g, row g+8: 2g+1 of the half), k = record pieces;
-            // one accumulator chain per (half, record row) for independent MMAs
-            float C[2][NT][4];
-            {
-                float Cr[2][4][NT][4];
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
+            for (int s4 = 0; s4 < 4; ++s4) {
+                uint2 bq[NT];
 #pragma unroll
-                    for (int r = 0; r < 4; ++r)
+                for (int t = 0; t < NT; ++t) bq[t] = qtab_s[((r * 4 + s4) * NT + t) * 32 + lane];
 #pragma unroll
-                        for (int t = 0; t < NT; ++t)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) Cr[hf][r][t][k] = 0.f;
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    if (r >= rows) break;
-                    const int nr = min(4, W - 4 * r);
-                    const uint4 mA = *reinterpret_cast<const uint4 *>(kmask_s + (4 * r + c) * 8);
-                    const uint4 mB = *reinterpret_cast<const uint4 *>(kmask_s + (4 * r + c) * 8 + 4);
-                    const uint32_t mk[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
-                    uint32_t x0[2], x1[2], y0[2], y1[2];
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const uint2 kw =
-                            *reinterpret_cast<const uint2 *>(Kt + hf * 16 * W + 64 * r + g * 2 * nr + 2 * c);
-                        x0[hf] = kw.x;
-                        x1[hf] = kw.y;
-                        y0[hf] = kw.x >> 8;
-                        y1[hf] = kw.y >> 8;
-                    }
-#pragma unroll
-                    for (int s4 = 0; s4 < 4; ++s4) {
-                        uint2 bq[NT];
-#pragma unroll
-                        for (int t = 0; t < NT; ++t) bq[t] = qtab_s[((r * 4 + s4) * NT + t) * 32 + lane];
-#pragma unroll
-                        for (int hf = 0; hf < 2; ++hf) {
-                            const uint32_t sa = s4 < 2 ? x0[hf] : y0[hf], sb = s4 < 2 ? x1[hf] : y1[hf];
-                            const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
-                            const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
-#pragma unroll
-                            for (int t = 0; t < NT; ++t) mma16816(Cr[hf][r][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf)
+                for (int hf = 0; hf < 2; ++hf) {
+                    const uint32_t sa = s4 < 2 ? x0[hf] : y0[hf], sb = s4 < 2 ? x1[hf] : y1[hf];
+                    const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
+                    const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
 #pragma unroll
                     for (int t = 0; t < NT; ++t)
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            C[hf][t][k] = (Cr[hf][0][t][k] + Cr[hf][1][t][k]) + (Cr[hf][2][t][k] + Cr[hf][3][t][k]);
-            }
-
-            // ---- online softmax (log2 domain); thread owns head 4t+c of tokens 16hf+2g, +1
-            const int tb0 = tile * TILE;
-            float psh[NT], psl[NT];   // this tile's sums of the fp16 P operands (hi, lo) per head
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                float z[2][2];
-                float mt = -INFINITY;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int tau = tb0 + 16 * hf + 2 * g;
-                    z[hf][0] = tau < len ? (C[hf][t][0] + C[hf][t][1]) * sc[t] : -INFINITY;
-                    z[hf][1] = tau + 1 < len ? (C[hf][t][2] + C[hf][t][3]) * sc[t] : -INFINITY;
-                    mt = fmaxf(mt, fmaxf(z[hf][0], z[hf][1]));
+                        mma16816(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
                 }
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 4));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 8));
-                mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 16));
-                const float mn = fmaxf(m_run[t], mt);
-                const float alpha = (mn == -INFINITY) ? 1.f : exp2f(m_run[t] - mn);
-                m_run[t] = mn;
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    l_run[t] *= alpha;
-#pragma unroll
-                    for (int gr = 0; gr < GMAX; ++gr)
-#pragma unroll
-                        for (int m4 = 0; m4 < 4; ++m4)
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) acc[gr][m4][t][k] *= alpha;
-                }
-                psh[t] = 0.f;
-                psl[t] = 0.f;
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const float p0 = z[hf][0] == -INFINITY ? 0.f : exp2f(z[hf][0] - mn);
-                    const float p1 = z[hf][1] == -INFINITY ? 0.f : exp2f(z[hf][1] - mn);
-                    l_run[t] += p0 + p1;
-                    // P scaled by 2^14: hi/lo fp16 pair per token (hi in column 2c, lo in 2c+1)
-                    const float s0 = p0 * 16384.f, s1 = p1 * 16384.f;
-                    const __half2 hi2 = __floats2half2_rn(s0, s1);
-                    const float2 hif = __half22float2(hi2);
-                    const __half2 lo2 = __floats2half2_rn(s0 - hif.x, s1 - hif.y);
-                    const float2 lof = __half22float2(lo2);
-                    psh[t] += hif.x + hif.y;
-                    psl[t] += lof.x + lof.y;
-                    const int tau = 16 * hf + 2 * g;
-                    *reinterpret_cast<__half2 *>(pw + (8 * t + 2 * c) * PSTRIDE + tau) = hi2;
-                    *reinterpret_cast<__half2 *>(pw + (8 * t + 2 * c + 1) * PSTRIDE + tau) = lo2;
-                }
-            }
-            __syncwarp();
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    psh[t] += __shfl_xor_sync(0xffffffffu, psh[t], o);
-                    psl[t] += __shfl_xor_sync(0xffffffffu, psl[t], o);
-                }
-            }
-
-            // ---- P.V: rows = value pieces (half-word 8 gr + g, slot 2 m4 / 2 m4 + 1), k = tokens
-            uint2 bp[2][NT];
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-#pragma unroll
-                for (int t = 0; t < NT; ++t)
-                    bp[kk][t] = *reinterpret_cast<const uint2 *>(pw + (8 * t + g) * PSTRIDE + 8 * c + 4 * kk);
-#pragma unroll
-            for (int gr = 0; gr < GMAX; ++gr) {
-                if (gr >= groups) break;
-                const int e = 8 * gr + g;
-                const uint4 pq = *reinterpret_cast<const uint4 *>(Vt + e * 16 + 4 * c);
-                const uint4 mA = *reinterpret_cast<const uint4 *>(vmask_s + e * 8);
-                const uint4 mB = *reinterpret_cast<const uint4 *>(vmask_s + e * 8 + 4);
-                const uint32_t mv[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
-                const uint32_t xs[4] = {pq.x, pq.y, pq.z, pq.w};
-                const uint32_t ys[4] = {pq.x >> 8, pq.y >> 8, pq.z >> 8, pq.w >> 8};
-#pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-#pragma unroll
-                    for (int kk = 0; kk < 2; ++kk) {
-                        const uint32_t u0 = m4 < 2 ? xs[2 * kk] : ys[2 * kk];
-                        const uint32_t u1 = m4 < 2 ? xs[2 * kk + 1] : ys[2 * kk + 1];
-                        const uint32_t A0 = u0 & mv[2 * m4], A1 = u0 & mv[2 * m4 + 1];
-                        const uint32_t A2 = u1 & mv[2 * m4], A3 = u1 & mv[2 * m4 + 1];
-#pragma unroll
-                        for (int t = 0; t < NT; ++t)
-                            mma16816(acc[gr][m4][t], A0, A1, A2, A3, bp[kk][t].x, bp[kk][t].y);
-                    }
-                    // keep the sums centred: subtract each piece's midpoint times the
-                    // tile's P mass, so the tensor-core accumulation (which does not
-                    // round to nearest) only ever carries small values
-                    const float c0 = vmid_s[(gr * 4 + m4) * 16 + g], c1 = vmid_s[(gr * 4 + m4) * 16 + g + 8];
-#pragma unroll
-                    for (int t = 0; t < NT; ++t) {
-                        acc[gr][m4][t][0] = fmaf(-c0, psh[t], acc[gr][m4][t][0]);
-                        acc[gr][m4][t][1] = fmaf(-c0, psl[t], acc[gr][m4][t][1]);
-                        acc[gr][m4][t][2] = fmaf(-c1, psh[t], acc[gr][m4][t][2]);
-                        acc[gr][m4][t][3] = fmaf(-c1, psl[t], acc[gr][m4][t][3]);
-                    }
-                }
-            }
-            __syncwarp();
-            const int nt = tile + FSTAGES * FW;
-            if (nt < t1) {
-                if (lane == 0) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue(nt, n_issued % FSTAGES);
-                }
-                ++n_issued;
             }
         }
-        if (failed) {
-            if (lane == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
-            // let copies still in flight land before the shared memory is reused
-            for (; n_done < n_issued; ++n_done)
-                mbar_wait(&my_mbar[n_done % FSTAGES], (uint32_t)((n_done / FSTAGES) & 1));
-#pragma unroll
-            for (int t = 0; t < NT; ++t) { m_run[t] = -INFINITY; l_run[t] = 0.f; }
-        }
 
-        // ---- warp partials -> shared memory (the stage area is free now)
-        __syncthreads();
-        float *wm = reinterpret_cast<float *>(stage_base);          // [FW][HPG]
-        float *wl = wm + FW * HPG;                                   // [FW][HPG]
-        float *wacc = wl + FW * HPG;                                 // [FW][rows_tot][HPG]
-        float *ach = wacc + (size_t)FW * rows_tot * HPG;             // [D][HPG]
+        // ---- online softmax (log2 domain); thread owns head 4t+c of tokens 16hf+2g, +1
+        const int tb0 = tile * TILE;
+        const bool full = tb0 + TILE <= len;
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            float l = l_run[t];
-            l += __shfl_xor_sync(0xffffffffu, l, 4);
-            l += __shfl_xor_sync(0xffffffffu, l, 8);
-            l += __shfl_xor_sync(0xffffffffu, l, 16);
-            const int i = 4 * t + c;
-            if (g == 0) {
-                wm[warp * HPG + i] = m_run[t];
-                wl[warp * HPG + i] = l;
+            float sv[4];
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                sv[2 * hf] = (C[hf][0][t][0] + C[hf][0][t][1]) + (C[hf][1][t][0] + C[hf][1][t][1]);
+                sv[2 * hf + 1] = (C[hf][0][t][2] + C[hf][0][t][3]) + (C[hf][1][t][2] + C[hf][1][t][3]);
             }
+            if (!full) {
 #pragma unroll
-            for (int gr = 0; gr < GMAX; ++gr) {
-                if (gr >= groups) break;
+                for (int j = 0; j < 4; ++j)
+                    if (tb0 + 16 * (j >> 1) + 2 * g + (j & 1) >= len) sv[j] = -INFINITY;
+            }
+            const float mt = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3])) * sc[t];
+            if (__any_sync(0xffffffffu, mt > m_run[t] + RESCALE_T)) {
+                float mw = mt;
+                mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 4));
+                mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 8));
+                mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, 16));
+                const float mn = fmaxf(m_run[t], mw);
+                const float alpha = ex2(m_run[t] - mn);   // 0 while nothing was seen yet
+                m_run[t] = mn;
+                l_run[t] *= alpha;
 #pragma unroll
-                for (int m4 = 0; m4 < 4; ++m4) {
-                    const int row = (gr * 4 + m4) * 16 + g;
-                    float *dst = wacc + ((size_t)warp * rows_tot + row) * HPG + i;
-                    dst[0] = failed ? 0.f : acc[gr][m4][t][0] + acc[gr][m4][t][1];
-                    dst[8 * HPG] = failed ? 0.f : acc[gr][m4][t][2] + acc[gr][m4][t][3];
+                for (int gr = 0; gr < GMAX; ++gr)
+#pragma unroll
+                    for (int m4 = 0; m4 < 4; ++m4) {
+                        acc[gr][m4][t][0] *= alpha;
+                        acc[gr][m4][t][1] *= alpha;
+                    }
+            }
+            const float mb = m_run[t] - (float)PSH;
+            float p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) p[j] = ex2(fmaf(sv[j], sc[t], -mb));
+            l_run[t] += (p[0] + p[1]) + (p[2] + p[3]);
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                // hi/lo fp16 pair per token (hi in column 2c, lo in 2c+1)
+                const __half2 hi2 = __floats2half2_rn(p[2 * hf], p[2 * hf + 1]);
+                const float2 hif = __half22float2(hi2);
+                const __half2 lo2 = __floats2half2_rn(p[2 * hf] - hif.x, p[2 * hf + 1] - hif.y);
+                const int tau = 16 * hf + 2 * g;
+                *reinterpret_cast<__half2 *>(pw + (8 * t + 2 * c) * PSTRIDE + tau) = hi2;
+                *reinterpret_cast<__half2 *>(pw + (8 * t + 2 * c + 1) * PSTRIDE + tau) = lo2;
+            }
+        }
+        __syncwarp();
+
+        // ---- P.V: rows = value pieces (half-word 8 gr + g, slot 2 m4 / 2 m4 + 1), k = tokens
+        uint2 bp[2][NT];
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+                bp[kk][t] = *reinterpret_cast<const uint2 *>(pw + (8 * t + g) * PSTRIDE + 8 * c + 4 * kk);
+#pragma unroll
+        for (int gr = 0; gr < GMAX; ++gr) {
+            if (gr >= groups) break;
+            const int e = 8 * gr + g;
+            const uint4 pq = *reinterpret_cast<const uint4 *>(Vt + e * 16 + 4 * c);
+            const uint4 mA = *reinterpret_cast<const uint4 *>(&blob_s->vmask[e][0]);
+            const uint4 mB = *reinterpret_cast<const uint4 *>(&blob_s->vmask[e][4]);
+            const uint32_t mv[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
+            const uint32_t xs[4] = {pq.x, pq.y, pq.z, pq.w};
+            const uint32_t ys[4] = {pq.x >> 8, pq.y >> 8, pq.z >> 8, pq.w >> 8};
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+                float ta4[NT][4];
+#pragma unroll
+                for (int t = 0; t < NT; ++t) ta4[t][0] = ta4[t][1] = ta4[t][2] = ta4[t][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const uint32_t u0 = m4 < 2 ? xs[2 * kk] : ys[2 * kk];
+                    const uint32_t u1 = m4 < 2 ? xs[2 * kk + 1] : ys[2 * kk + 1];
+                    const uint32_t A0 = u0 & mv[2 * m4], A1 = u0 & mv[2 * m4 + 1];
+                    const uint32_t A2 = u1 & mv[2 * m4], A3 = u1 & mv[2 * m4 + 1];
+#pragma unroll
+                    for (int t = 0; t < NT; ++t) mma16816(ta4[t], A0, A1, A2, A3, bp[kk][t].x, bp[kk][t].y);
+                }
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    acc[gr][m4][t][0] += ta4[t][0] + ta4[t][1];
+                    acc[gr][m4][t][1] += ta4[t][2] + ta4[t][3];
                 }
             }
         }
-        for (int e = tid; e < D * HPG; e += NTH) ach[e] = 0.f;
-        __syncthreads();
-
-        // ---- merge the warps, map pieces to channels: sum_i p_i u_ij (p unscaled)
-        if (tid < HPG) {
-            const int i = tid;
-            float M = -INFINITY;
-            for (int w = 0; w < FW; ++w) M = fmaxf(M, wm[w * HPG + i]);
-            float Ls = 0.f;
-            for (int w = 0; w < FW; ++w) {
-                const float f = (M == -INFINITY || wm[w * HPG + i] == -INFINITY) ? 0.f : exp2f(wm[w * HPG + i] - M);
-                cs[i][w] = f;
-                Ls += wl[w * HPG + i] * f;
+        __syncwarp();
+        const int nt = tile + FST * FW;
+        if (nt < t1) {
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(nt, s);
             }
+            ++n_issued;
+        }
+    }
+    // copies still in flight (requested past the row's length, or left by a
+    // failed wait) land before the shared memory is reused
+    if (failed && lane == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
+    for (; n_done < n_issued; ++n_done) {
+        if (!mbar_wait(&my_mbar[st_next], ph_next)) failed = true;
+        if (++st_next == FST) {
+            st_next = 0;
+            ph_next ^= 1u;
+        }
+    }
+    if (failed) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) { m_run[t] = -INFINITY; l_run[t] = 0.f; }
+    }
+
+    // ---- merge the warps in piece space, gather the pieces into channels and
+    // leave the transform domain for this split: y_i = Uv (Delta_V o sum_t p_it u_t)
+    // (the midpoint and mu_v terms are the same for every split: the combine adds them)
+    const int rows_tot = 64 * groups;
+    float *wm = scr;                                          // [FW][HPG]
+    float *wl = wm + FW * HPG;                                // [FW][HPG]
+    float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG]
+    const float *UT = mat_s;                                  // [D][D] Uv^T (prefetched)
+    float *cbarT = reinterpret_cast<float *>(stage_base + a.uv_off);   // [D][8] Delta_V o channel sums
+    float *red = cbarT + D * 8;                               // [4][8][D] k-quarter partial outputs
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        float l = l_run[t];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (g == 0) {
+            wm[warp * HPG + 4 * t + c] = m_run[t];
+            wl[warp * HPG + 4 * t + c] = l;
+        }
+    }
+    __syncthreads();   // every warp is out of its loop: the stages are free
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+        const int i = 4 * t + c;
+        float M = -INFINITY;
+#pragma unroll 4
+        for (int w = 0; w < FW; ++w) M = fmaxf(M, wm[w * HPG + i]);
+        const float f = m_run[t] == -INFINITY ? 0.f : ex2(m_run[t] - M);
+#pragma unroll
+        for (int gr = 0; gr < GMAX; ++gr) {
+            if (gr >= groups) break;
+#pragma unroll
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const int row = (gr * 4 + m4) * 16 + g;
+                wacc[((size_t)warp * rows_tot + row) * HPG + i] = acc[gr][m4][t][0] * f;
+                wacc[((size_t)warp * rows_tot + row + 8) * HPG + i] = acc[gr][m4][t][1] * f;
+            }
+        }
+    }
+    if (warp < HPG) {   // warp i: maximum and sum of head i over the warps (FW <= 32)
+        const int i = warp;
+        const float mw = lane < FW ? wm[lane * HPG + i] : -INFINITY;
+        float M = mw;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float Ls = mw == -INFINITY ? 0.f : wl[lane * HPG + i] * ex2(mw - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+        if (lane == 0) {
             cm[i] = M;
             cl[i] = Ls;
         }
-        __syncthreads();
-        for (int e = tid; e < (int)rows_tot * HPG; e += NTH) {
-            const int row = e / HPG, i = e % HPG;
-            const int rv = vrow_s[row];
-            if (rv < 0) continue;
-            float v = 0.f;
-#pragma unroll 4
-            for (int w = 0; w < FW; ++w) v = fmaf(wacc[((size_t)w * rows_tot + row) * HPG + i], cs[i][w], v);
-            // fp16 operands: piece value * 2^(p-24) and P * 2^14; piece * 2^ex is the code part
-            atomicAdd(&ach[(rv >> 8) * HPG + i], ldexpf(v, (rv & 255) - 64 + 10));
-        }
-        __syncthreads();
-        {
-            float *P = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
-            for (int e = tid; e < HPG * PROW; e += NTH) {
-                const int i = e / PROW, j = e % PROW;
-                P[e] = j == 0 ? cm[i] : (j == 1 ? cl[i] : (j < 4 ? 0.f : ach[(j - 4) * HPG + i]));
+    }
+    __syncthreads();
+    // channel sums sum_t p_t u_tj (both sides carry 2^PSH), times Delta_V,j
+    for (int e = tid; e < HPG * D; e += NTH) {
+        const int i = e >> 7, j = e & (D - 1);
+        float v = 0.f;
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+            const int vg = blob_s->vgat[j][q2];
+            if (vg >= 0) {
+                const float *src = wacc + (size_t)(vg & 255) * HPG + i;
+                float s0 = 0.f, s1 = 0.f;
+                int w = 0;
+                for (; w + 2 <= FW; w += 2) {
+                    s0 += src[(size_t)w * rows_tot * HPG];
+                    s1 += src[(size_t)(w + 1) * rows_tot * HPG];
+                }
+                if (w < FW) s0 += src[(size_t)w * rows_tot * HPG];
+                // fp16 operands: piece * 2^(p - 24); piece * 2^ex is the code part
+                v = fmaf(s0 + s1, pow2i((vg >> 8) - 64 + 24), v);
             }
+        }
+        cbarT[j * 8 + i] = v * blob_s->vstep[j];
+    }
+    __syncthreads();
+    if (!mbar_wait(mat_bar, 1)) failed = true;
+    {   // thread (k-quarter kq, output j) for every head
+        const int j = tid & (D - 1);
+        for (int kq = tid >> 7; kq < 4; kq += NTH / D) {
+            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k = 32 * kq; k < 32 * kq + 32; ++k) {
+                const float uv = UT[k * D + j];
+                const float4 c0 = *reinterpret_cast<const float4 *>(&cbarT[k * 8]);
+                o[0] = fmaf(uv, c0.x, o[0]);
+                o[1] = fmaf(uv, c0.y, o[1]);
+                o[2] = fmaf(uv, c0.z, o[2]);
+                o[3] = fmaf(uv, c0.w, o[3]);
+                if (HPG > 4) {
+                    const float4 c1 = *reinterpret_cast<const float4 *>(&cbarT[k * 8 + 4]);
+                    o[4] = fmaf(uv, c1.x, o[4]);
+                    o[5] = fmaf(uv, c1.y, o[5]);
+                    o[6] = fmaf(uv, c1.z, o[6]);
+                    o[7] = fmaf(uv, c1.w, o[7]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < HPG; ++i) red[(kq * 8 + i) * D + j] = o[i];
+        }
+    }
+    __syncthreads();
+    {
+        float *P = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
+        for (int e = tid; e < HPG * D; e += NTH) {
+            const int i = e >> 7, j = e & (D - 1);
+            const float y = (red[(0 * 8 + i) * D + j] + red[(1 * 8 + i) * D + j]) +
+                            (red[(2 * 8 + i) * D + j] + red[(3 * 8 + i) * D + j]);
+            P[i * PROW + 4 + j] = failed ? 0.f : y;
+        }
+        if (tid < HPG) {
+            P[tid * PROW + 0] = failed ? -INFINITY : cm[tid];
+            P[tid * PROW + 1] = failed ? 0.f : cl[tid];
+            P[tid * PROW + 2] = 0.f;
+            P[tid * PROW + 3] = 0.f;
         }
     }
 }
 
-
-// Merge the slots of one unit and leave the transform domain:
-//   o = Uv (Delta_V o sum_i p_i (u_i - mid) / sum_i p_i) + mu_v
-// (the slots hold centred sums).  Launched after k_decode_fast with
-// programmatic dependent launch: Uv^T and the tables are staged before the
-// wait for the split kernel's partials.
-constexpr int CB_THREADS = 256;
-constexpr size_t CB_SMEM = (size_t)D * D * 4;
-__global__ void __launch_bounds__(CB_THREADS) k_decode_combine_fast(
-    const float *__restrict__ part, int S, int Hkv, int G, int HG, int HPG,
-    const CodecTables *__restrict__ tabs, const float *__restrict__ UvT, const float *__restrict__ muv,
-    float *__restrict__ out)
+// Merge the splits of one unit:
+//   o = sum_s w_s y_s / sum_s w_s l_s + (mu_v - Uv (Delta_V o mid)),  w_s = 2^(m_s - M)
+// where y_s = Uv (Delta_V o sum_t p_t u_t) over split s.  Launched after
+// k_decode_fast with programmatic dependent launch.  The unit's partial slots
+// are contiguous: they come in by bulk copies of up to CS slots, and each
+// slot's weight is kept in its spare word 2.  The code is a few short loops
+// (it runs once per launch, from a cold instruction cache).
+constexpr int CB_THREADS = 512;
+constexpr size_t CB_STAGE_BYTES = 96 * 1024;
+int cb_chunk(int HPG) { return (int)(CB_STAGE_BYTES / ((size_t)HPG * PROW * 4)); }
+size_t cb_smem(int S, int HPG)
 {
-    extern __shared__ __align__(16) float UT[];          // [D][D]
-    __shared__ float cacc[8][D], cbar[8][D];
-    __shared__ float sM[8], sL[8];
-    __shared__ float step_s[D], muv_s[D];
-    __shared__ float ml_s[2][CB_THREADS];
-    const int u = blockIdx.x, tid = threadIdx.x;
+    const int cs = cb_chunk(HPG);
+    return (size_t)(S < cs ? S : cs) * HPG * PROW * 4;
+}
+__global__ void __launch_bounds__(CB_THREADS) k_decode_combine_fast(
+    const float *__restrict__ part, int S, int CS, int Hkv, int G, int HG, int HPG,
+    const float *__restrict__ vcst, float *__restrict__ out, uint32_t *status)
+{
+    extern __shared__ __align__(128) float Ps[];           // [CS][HPG][PROW]
+    __shared__ float Mh[8], Lh[8], Rh[8];
+    __shared__ uint64_t bar;
+    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = u / (Hkv * HG), h = (u / HG) % Hkv, hg = u % HG;
-    {
-        // every load of the prologue in flight at once
-        const float4 *src = reinterpret_cast<const float4 *>(UvT + (size_t)h * D * D);
-        float4 ut[D * D / 4 / CB_THREADS];
-#pragma unroll
-        for (int r = 0; r < D * D / 4 / CB_THREADS; ++r) ut[r] = __ldg(src + tid + r * CB_THREADS);
-        const CodecTables &tv = tabs[h * 2 + 1];
-        float st = 0.f, mv = 0.f;
-        if (tid < D) {
-            st = tv.bits[tid] ? tv.step[tid] : 0.f;
-            mv = muv[h * D + tid];
-        }
-        float4 *dst = reinterpret_cast<float4 *>(UT);
-#pragma unroll
-        for (int r = 0; r < D * D / 4 / CB_THREADS; ++r) dst[tid + r * CB_THREADS] = ut[r];
-        if (tid < D) {
-            step_s[tid] = st;
-            muv_s[tid] = mv;
-        }
-        for (int e = tid; e < 8 * D; e += CB_THREADS) (&cacc[0][0])[e] = 0.f;
+    const float cst = vcst[h * D + (tid & (D - 1))];
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (tid < 8) {
+        Mh[tid] = -INFINITY;
+        Lh[tid] = 0.f;
+    }
+    __syncthreads();
     asm volatile("griddepcontrol.wait;" ::: "memory");   // partials of k_decode_fast
-    const int nslots = S;
+
     const float *Pu = part + (size_t)u * S * HPG * PROW;
-    // per-head maximum and weighted sum over the slots; (slot, head) pairs in parallel
-    float Mh = -INFINITY;
-    for (int e0 = 0; e0 < nslots * HPG; e0 += CB_THREADS) {
-        const int e = e0 + tid;
-        float m = -INFINITY, l = 0.f;
-        if (e < nslots * HPG) {
-            m = __ldcg(Pu + (size_t)e * PROW);
-            l = __ldcg(Pu + (size_t)e * PROW + 1);
+    float A[2] = {0.f, 0.f};   // pairs e = tid + q CB_THREADS: head e / D, channel e % D
+    bool ok = true;
+    for (int c0 = 0, k = 0; c0 < S; c0 += CS, ++k) {
+        const int n = min(CS, S - c0);
+        if (tid == 0) {
+            const uint32_t bytes = (uint32_t)((size_t)n * HPG * PROW * 4);
+            mbar_arrive_expect(&bar, bytes);
+            bulk_g2s(Ps, Pu + (size_t)c0 * HPG * PROW, bytes, &bar);
         }
-        __syncthreads();
-        ml_s[0][tid] = m;
-        ml_s[1][tid] = l;
-        __syncthreads();
-        if (tid < HPG) {
-            const int cnt = min(CB_THREADS, nslots * HPG - e0);
-            float M = Mh, Ls = e0 == 0 ? 0.f : sL[tid];
-            for (int k = tid; k < cnt; k += HPG) {
-                const float mk = ml_s[0][k];
-                if (mk == -INFINITY) continue;
-                if (mk > M) {
-                    Ls = (M == -INFINITY) ? 0.f : Ls * exp2f(M - mk);
-                    M = mk;
-                }
-                Ls = fmaf(ml_s[1][k], exp2f(mk - M), Ls);
+        ok = mbar_wait(&bar, (uint32_t)(k & 1)) && ok;
+        if (warp < HPG) {   // warp i: running maximum and sum of head i, slot weights
+            const int i = warp;
+            float mc = -INFINITY;
+            for (int s = lane; s < n; s += 32) mc = fmaxf(mc, Ps[(s * HPG + i) * PROW]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+            const float Mo = Mh[i], M = fmaxf(Mo, mc);
+            float Lc = 0.f;
+            for (int s = lane; s < n; s += 32) {
+                float *P = Ps + (s * HPG + i) * PROW;
+                const float w = P[0] == -INFINITY ? 0.f : ex2(P[0] - M);
+                P[2] = w;
+                Lc = fmaf(P[1], w, Lc);
             }
-            Mh = M;
-            sM[tid] = M;
-            sL[tid] = Ls;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) Lc += __shfl_xor_sync(0xffffffffu, Lc, o);
+            __syncwarp();
+            if (lane == 0) {
+                const float r = Mo == -INFINITY ? 0.f : ex2(Mo - M);
+                Rh[i] = r;
+                Lh[i] = Lh[i] * r + Lc;
+                Mh[i] = M;
+            }
         }
-    }
-    __syncthreads();
-    {   // thread (rep, i, j4): float4 block j4 of head i over every reps-th slot
-        const int outs = HPG * (D / 4);
-        const int reps = CB_THREADS / outs;
-        const int o = tid % outs, rep = tid / outs;
-        const int i = o / (D / 4), j4 = o % (D / 4);
-        const float M = sM[i];
-        float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int sp = rep; sp < nslots; sp += reps) {
-            const float *Ps = Pu + ((size_t)sp * HPG + i) * PROW;
-            const float ms = __ldcg(Ps);
-            const float f = ms == -INFINITY ? 0.f : exp2f(ms - M);
-            const float4 v = __ldcg(reinterpret_cast<const float4 *>(Ps + 4) + j4);
-            s4.x = fmaf(v.x, f, s4.x);
-            s4.y = fmaf(v.y, f, s4.y);
-            s4.z = fmaf(v.z, f, s4.z);
-            s4.w = fmaf(v.w, f, s4.w);
+        __syncthreads();
+        for (int q = 0; q < 2; ++q) {
+            const int e = tid + q * CB_THREADS;
+            if (e >= HPG * D) break;
+            const int i = e >> 7, j = e & (D - 1);
+            float a0 = A[q] * Rh[i], a1 = 0.f;
+            const float *P = Ps + i * PROW;
+            int s = 0;
+            for (; s + 2 <= n; s += 2) {
+                a0 = fmaf(P[(s * HPG) * PROW + 2], P[(s * HPG) * PROW + 4 + j], a0);
+                a1 = fmaf(P[((s + 1) * HPG) * PROW + 2], P[((s + 1) * HPG) * PROW + 4 + j], a1);
+            }
+            if (s < n) a0 = fmaf(P[(s * HPG) * PROW + 2], P[(s * HPG) * PROW + 4 + j], a0);
+            A[q] = a0 + a1;
         }
-        atomicAdd(&cacc[i][4 * j4 + 0], s4.x);
-        atomicAdd(&cacc[i][4 * j4 + 1], s4.y);
-        atomicAdd(&cacc[i][4 * j4 + 2], s4.z);
-        atomicAdd(&cacc[i][4 * j4 + 3], s4.w);
+        __syncthreads();   // the stage is refilled by the next chunk
     }
-    __syncthreads();
-    for (int e = tid; e < HPG * D; e += CB_THREADS) {
-        const int i = e / D, j = e % D;
-        cbar[i][j] = sL[i] > 0.f ? step_s[j] * (cacc[i][j] / sL[i]) : 0.f;
-    }
-    __syncthreads();
+    if (!ok && tid == 0) atomicOr(status, AATC_DEV_TIMEOUT);
     const int Hq = Hkv * G;
-    for (int e = tid; e < HPG * D; e += CB_THREADS) {
-        const int i = e / D, j = e % D, gi = hg * HPG + i;
-        if (gi >= G) continue;
-        float o = 0.f;
-        if (sL[i] > 0.f) {
-#pragma unroll 8
-            for (int k = 0; k < D; ++k) o = fmaf(UT[k * D + j], cbar[i][k], o);
-            o += muv_s[j];
+    for (int q = 0; q < 2; ++q) {
+        const int e = tid + q * CB_THREADS;
+        if (e >= HPG * D) break;
+        const int i = e >> 7, j = e & (D - 1), gi = hg * HPG + i;
+        const float Ls = Lh[i];   // j = tid % D: cst is channel j's
+        if (gi < G) out[((size_t)b * Hq + h * G + gi) * D + j] = (Ls > 0.f && ok) ? A[q] / Ls + cst : 0.f;
+    }
+}
+
+// Per-head fast-decoder tables from the plans and codec tables.
+__global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs, int W,
+                            const double *__restrict__ Uv, const double *__restrict__ muv, DecBlob *__restrict__ out,
+                            float *__restrict__ vcst)
+{
+    const int h = blockIdx.x, tid = threadIdx.x;
+    const HeadPlan &pk = plans[h * 2 + 0];
+    const HeadPlan &pv = plans[h * 2 + 1];
+    const CodecTables &tk = tabs[h * 2 + 0];
+    const CodecTables &tv = tabs[h * 2 + 1];
+    // mu_v - Uv (Delta_V o mid): the part of every output that does not depend on the tokens
+    for (int j = tid; j < D; j += blockDim.x) {
+        double acc = muv[(size_t)h * D + j];
+        for (int k = 0; k < D; ++k)
+            if (tv.bits[k]) acc -= Uv[((size_t)h * D + j) * D + k] * ((double)tv.step[k] * (double)tv.mid[k]);
+        vcst[(size_t)h * D + j] = (float)acc;
+    }
+    DecBlob &o = out[h];
+    const int rows_tot = 64 * ((2 * W + 7) / 8);
+    for (int e = tid; e < 16 * 8; e += blockDim.x) {
+        const int w = e >> 3, k = e & 7;
+        o.kmask[w][k] = w < W ? pk.mask[w][k] : 0u;
+        for (int half = 0; half < 2; ++half) {
+            const int ch = w < W ? pk.ch[w][k][half] : -1;
+            o.kslot[w][k][half] = (int16_t)(ch < 0 ? -1 : (ch | ((pk.ex[w][k][half] + 64) << 8)));
         }
-        out[((size_t)b * Hq + h * G + gi) * D + j] = o;
+    }
+    for (int e = tid; e < 32 * 8; e += blockDim.x) {
+        const int hw = e >> 3, k = e & 7;
+        o.vmask[hw][k] = hw < 2 * W ? pv.mask[hw][k] : 0u;
+    }
+    for (int j = tid; j < D; j += blockDim.x) {
+        o.ksc[j] = tk.bits[j] ? tk.step[j] * 0.08838834764831845f : 0.f;
+        o.vstep[j] = tv.bits[j] ? tv.step[j] : 0.f;
+        // value pieces of channel j: row (gr, m4, rr) holds slot 2 m4 + rr / 8 of half-word 8 gr + rr % 8
+        int n = 0;
+        int16_t got[2] = {-1, -1};
+        for (int row = 0; row < rows_tot && n < 2; ++row) {
+            const int gr = row >> 6, m4 = (row >> 4) & 3, rr = row & 15;
+            const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
+            if (hw < 2 * W && pv.ch[hw][k][0] == j) got[n++] = (int16_t)(row | ((pv.ex[hw][k][0] + 64) << 8));
+        }
+        o.vgat[j][0] = got[0];
+        o.vgat[j][1] = got[1];
     }
 }
 
@@ -823,30 +906,44 @@ int occupancy_of(size_t smem)
     return n;
 }
 
-int fast_ctas_per_sm_uncached(int groups, int NT, size_t smem)
+int fast_ctas_per_sm_uncached(int GMAX, int NT, size_t smem)
 {
     if (NT == 1) {
-        if (groups <= 2) return occupancy_of<2, 1, 12>(smem);
-        if (groups <= 3) return occupancy_of<3, 1, 12>(smem);
+        if (GMAX == 2) return occupancy_of<2, 1, 16>(smem);
+        if (GMAX == 3) return occupancy_of<3, 1, 16>(smem);
         return occupancy_of<4, 1, 12>(smem);
     }
-    if (groups <= 2) return occupancy_of<2, 2, 8>(smem);
-    if (groups <= 3) return occupancy_of<3, 2, 8>(smem);
+    if (GMAX == 2) return occupancy_of<2, 2, 8>(smem);
+    if (GMAX == 3) return occupancy_of<3, 2, 8>(smem);
     return occupancy_of<4, 2, 8>(smem);
 }
 
-int fast_ctas_per_sm(int groups, int NT, int FW, size_t smem)
+int fast_ctas_per_sm(int GMAX, int NT, int FW, size_t smem)
 {
     // the answer depends only on the kernel variant and its shared memory
-    static struct { int groups, NT, FW; size_t smem; int n; } cache[16];
+    static struct { int GMAX, NT, FW; size_t smem; int n; } cache[16];
     static int used = 0;
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
-        if (cache[i].groups == groups && cache[i].NT == NT && cache[i].FW == FW && cache[i].smem == smem)
+        if (cache[i].GMAX == GMAX && cache[i].NT == NT && cache[i].FW == FW && cache[i].smem == smem)
             return cache[i].n;
-    const int n = fast_ctas_per_sm_uncached(groups, NT, smem);
-    if (used < 16) cache[used++] = {groups, NT, FW, smem, n};
+    const int n = fast_ctas_per_sm_uncached(GMAX, NT, smem);
+    if (used < 16) cache[used++] = {GMAX, NT, FW, smem, n};
+    return n;
+}
+
+// Largest dynamic shared memory of one block on this device.
+int sm_limit_bytes()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        n = (cudaGetDevice(&dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && v > 0)
+                ? v
+                : 232448;
+    }
     return n;
 }
 
@@ -1097,25 +1194,32 @@ aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cud
 
 aatc_status launch_combine(const FastGeom &f, const aatc_calib *h, const float *part, float *out, cudaStream_t s)
 {
-    aatc_status st0 = smem_limit((const void *)k_decode_combine_fast, CB_SMEM);
+    const size_t smem = cb_smem(f.S, f.HPG);
+    aatc_status st0 = smem_limit((const void *)k_decode_combine_fast, smem);
     if (st0 != AATC_OK) return st0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(f.units);
     cfg.blockDim = dim3(CB_THREADS);
-    cfg.dynamicSmemBytes = CB_SMEM;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    AATC_CUDA(cudaLaunchKernelEx(&cfg, k_decode_combine_fast, part, f.S, h->Hkv, h->G, f.HG, f.HPG,
-                                 (const CodecTables *)h->tab, (const float *)h->UvT32, (const float *)h->muv32,
-                                 out));
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, k_decode_combine_fast, part, f.S, cb_chunk(f.HPG), h->Hkv, h->G, f.HG,
+                                 f.HPG, (const float *)h->vcst, out, h->status));
     return AATC_OK;
 }
 
 }  // namespace
+
+aatc_status dec_build(aatc_calib *h, cudaStream_t s)
+{
+    k_dec_build<<<h->Hkv, D, 0, s>>>(h->plan, h->tab, h->W, h->U_v, h->mu_v, h->dblob, h->vcst);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}
 
 size_t decode_ws_bytes(const aatc_calib *h, int B, int L)
 {
@@ -1150,25 +1254,27 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.Hkv = h->Hkv;
         a.G = h->G;
         a.HG = f.HG;
-        a.HPG = f.HPG;
+        a.FST = f.FST;
+        a.stage_region = (uint32_t)f.stage_region;
+        a.uv_off = (uint32_t)f.uv_off;
+        a.UvT = h->UvT32;
         a.n_tiles = f.n_tiles;
         a.units = f.units;
         a.S = f.S;
         a.tiles_per = f.tiles_per;
-        a.plan = h->plan;
+        a.blob = h->dblob;
         a.q = q;
         a.AkT = h->AkT32;
         a.part = part;
-        a.tab = h->tab;
         a.status = h->status;
         aatc_status st;
         if (f.NT == 1) {
-            if (f.groups <= 2) st = launch_fast<2, 1, 12>(f, a, h->dtype, s);
-            else if (f.groups <= 3) st = launch_fast<3, 1, 12>(f, a, h->dtype, s);
+            if (f.GMAX == 2) st = launch_fast<2, 1, 16>(f, a, h->dtype, s);
+            else if (f.GMAX == 3) st = launch_fast<3, 1, 16>(f, a, h->dtype, s);
             else st = launch_fast<4, 1, 12>(f, a, h->dtype, s);
         } else {
-            if (f.groups <= 2) st = launch_fast<2, 2, 8>(f, a, h->dtype, s);
-            else if (f.groups <= 3) st = launch_fast<3, 2, 8>(f, a, h->dtype, s);
+            if (f.GMAX == 2) st = launch_fast<2, 2, 8>(f, a, h->dtype, s);
+            else if (f.GMAX == 3) st = launch_fast<3, 2, 8>(f, a, h->dtype, s);
             else st = launch_fast<4, 2, 8>(f, a, h->dtype, s);
         }
         if (st != AATC_OK) return st;

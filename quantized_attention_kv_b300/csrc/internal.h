@@ -51,6 +51,18 @@ struct HeadPlan {
     int8_t ex[AATC_PLAN_SLOTS][8][2];     // code bit offset of the piece minus p
 };
 
+// Per-KV-head tables of the fast decoder, laid out as they sit in shared
+// memory (one bulk copy per CTA).  Built on the device from the plans and
+// codec tables (decode.cu).
+struct __align__(16) DecBlob {
+    uint32_t kmask[16][8];     // key record word w, slot k: AND mask (0 past the record)
+    uint32_t vmask[32][8];     // value half-word e, slot k: AND mask in both halves
+    float ksc[AATC_D];         // Delta_K,j / sqrt(d), 0 for pruned channels
+    float vstep[AATC_D];       // Delta_V,j, 0 for pruned channels
+    int16_t kslot[16][8][2];   // key piece of (word, slot, half): ch | (ex + 64) << 8, -1 = none
+    int16_t vgat[AATC_D][2];   // value channel j: its piece rows, row | (ex + 64) << 8, -1 = none
+};
+
 // Encoder epilogue constants of one record-order column n (channel order[n]):
 // v = c * inv + off is the quantizer input c/Delta + mid with the bias T mu
 // folded in; codes are clamp(rint(v), 0, top); bits = 0 past n_coded.
@@ -77,6 +89,8 @@ struct aatc_calib {
     float *muv32;             // [H][d]
     CodecTables *tab;         // [H][2]
     HeadPlan *plan;           // [H][2] record layout and decode masks
+    DecBlob *dblob;           // [H] fast-decoder tables
+    float *vcst;              // [H][d] mu_v - Uv (Delta_V o mid)
     // tensor-core encoder operands (bf16 inputs): T split in three bf16 terms
     // T = T1 + T2 + T3 with rows in record order, [H][2][3][d][d]; and the
     // epilogue columns [H][2][d]
@@ -116,6 +130,8 @@ void plan_one(const int32_t *bits, int W, HeadPlan *out);
 
 // Build T3, enc_cols and the T3 tensor map (after the plans are on the device).
 aatc_status enc_build(aatc_calib *h, cudaStream_t s);
+// Build the fast decoder's per-head tables (after the plans are on the device).
+aatc_status dec_build(aatc_calib *h, cudaStream_t s);
 
 // ---- encode (encode.cu, encode_tc.cu) ----
 aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,

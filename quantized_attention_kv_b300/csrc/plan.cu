@@ -141,6 +141,7 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
     h->fast_layout = fast;
     AATC_CUDA(cudaMemcpy(h->plan, plans.data(), sizeof(HeadPlan) * plans.size(), cudaMemcpyHostToDevice));
     aatc_status st = enc_build(h, 0);
+    if (st == AATC_OK) st = dec_build(h, 0);
     if (st == AATC_OK) AATC_CUDA(cudaDeviceSynchronize());
     return st;
 }
