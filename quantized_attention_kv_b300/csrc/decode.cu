@@ -205,6 +205,17 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// d = A B with a zero accumulator passed as its own operand (no register to clear).
+__device__ __forceinline__ void mma16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                           uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%10,%10,%10};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
 {
     __half2 v = __floats2half2_rn(lo, hi);
@@ -471,15 +482,15 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 
         // ---- scores: C[hf][r & 1] rows g / g+8 = tokens 16 hf + 2g / +1, columns 2c / 2c+1 =
         // head c hi / lo; two chains per half-tile (even and odd key rows)
-        float C[2][2][NT][4];
+        float C[2][2][NT][4];   // chain (hf, rp) starts at row rp, k-step 0 with a zero accumulator
+        if (rows < 2) {         // one key row: the odd chain stays empty
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-            for (int rp = 0; rp < 2; ++rp)
+            for (int hf = 0; hf < 2; ++hf)
 #pragma unroll
                 for (int t = 0; t < NT; ++t)
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) C[hf][rp][t][k] = 0.f;
+                    for (int k = 0; k < 4; ++k) C[hf][1][t][k] = 0.f;
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             if (r >= rows) break;
@@ -507,8 +518,10 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
                     const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
                     const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
 #pragma unroll
-                    for (int t = 0; t < NT; ++t)
-                        mma16816(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
+                    for (int t = 0; t < NT; ++t) {
+                        if (r < 2 && s4 == 0) mma16816_z(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
+                        else mma16816(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
+                    }
                 }
             }
         }
@@ -586,15 +599,16 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             for (int m4 = 0; m4 < 4; ++m4) {
                 float ta4[NT][4];
 #pragma unroll
-                for (int t = 0; t < NT; ++t) ta4[t][0] = ta4[t][1] = ta4[t][2] = ta4[t][3] = 0.f;
-#pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const uint32_t u0 = m4 < 2 ? xs[2 * kk] : ys[2 * kk];
                     const uint32_t u1 = m4 < 2 ? xs[2 * kk + 1] : ys[2 * kk + 1];
                     const uint32_t A0 = u0 & mv[2 * m4], A1 = u0 & mv[2 * m4 + 1];
                     const uint32_t A2 = u1 & mv[2 * m4], A3 = u1 & mv[2 * m4 + 1];
 #pragma unroll
-                    for (int t = 0; t < NT; ++t) mma16816(ta4[t], A0, A1, A2, A3, bp[kk][t].x, bp[kk][t].y);
+                    for (int t = 0; t < NT; ++t) {
+                        if (kk == 0) mma16816_z(ta4[t], A0, A1, A2, A3, bp[kk][t].x, bp[kk][t].y);
+                        else mma16816(ta4[t], A0, A1, A2, A3, bp[kk][t].x, bp[kk][t].y);
+                    }
                 }
 #pragma unroll
                 for (int t = 0; t < NT; ++t) {
