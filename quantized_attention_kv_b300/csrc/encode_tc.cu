@@ -31,8 +31,9 @@ namespace {
 
 constexpr int D = AATC_D;
 constexpr int EB = 128;                 // tokens per block (MMA M)
-constexpr int ESTAGES = 3;
-constexpr int EPI = 4;                  // epilogue warps
+constexpr int ESTAGES = 2;
+constexpr int NGRP = 4;                 // epilogue groups, one tensor-memory accumulator each
+constexpr int EPI = 4 * NGRP;           // epilogue warps (4 per group: one per tensor-memory lane quarter)
 constexpr int ETHREADS = (EPI + 1) * 32;
 constexpr uint32_t XBYTES = EB * D * 2; // 32 KB per x tile
 constexpr uint32_t TBYTES = 3 * D * D * 2;
@@ -143,17 +144,22 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *Ts = sm;                              // 3 splits x 2 k-halves x 16 KB
     unsigned char *Xs = Ts + TBYTES;                     // ESTAGES x 32 KB
-    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // 2 x 128 W words (tiled)
+    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 W words (tiled)
     const int W = a.W;
-    EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + 2 * EB * W);        // [D]
-    __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[2], d_empty[2];
+    EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + NGRP * EB * W);     // [NGRP][D]
+    __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
+    __shared__ int2 wtab[16];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid < 16) {
+        const int r = tid >> 2, nr = min(4, a.W - 4 * r);
+        wtab[tid] = make_int2(64 * r + 2 * (tid - 4 * r), 2 * nr);
+    }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                     "r"(2 * D));
+                     "r"(NGRP * D));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == EPI * 32) {
@@ -162,9 +168,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             mbar_init(&x_empty[s], 1);
         }
         mbar_init(&t_full, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&mma_done[b], 1);
-            mbar_init(&d_empty[b], EPI);
+        for (int g = 0; g < NGRP; ++g) {
+            mbar_init(&mma_done[g], 1);
+            mbar_init(&d_empty[g], 4);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         s_fail = 0;
@@ -182,6 +188,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     if (warp == EPI) {
         if (lane == 0 && count > 0) {
             // ------------------------------------------------ producer + MMA issue
+            // item n: x stage n % ESTAGES, accumulator (and epilogue group) n % NGRP
             auto issue_x = [&](int n) {
                 const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
                 const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
@@ -199,7 +206,8 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 const int item = i0 + n, ht = item / per_ht;
                 if (ht != ht_loaded) {
                     // the MMAs reading the old T are done once the previous item's commit arrived
-                    if (n > 0) ok = ok && mbar_wait1(&mma_done[(n - 1) & 1], (uint32_t)(((n - 1) >> 1) & 1));
+                    if (n > 0)
+                        ok = ok && mbar_wait1(&mma_done[(n - 1) % NGRP], (uint32_t)(((n - 1) / NGRP) & 1));
                     mbar_expect(&t_full, TBYTES);
                     for (int sp = 0; sp < 3; ++sp)
                         for (int kh = 0; kh < 2; ++kh)
@@ -208,13 +216,14 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                     ++t_uses;
                     ht_loaded = ht;
                 }
-                const int s = n % ESTAGES, buf = n & 1;
+                const int s = n % ESTAGES, g = n % NGRP;
                 ok = ok && mbar_wait1(&x_full[s], (uint32_t)((n / ESTAGES) & 1));
-                if (n >= 2) ok = ok && mbar_wait1(&d_empty[buf], (uint32_t)(((n >> 1) - 1) & 1));
+                // the accumulator is free once its group read the item NGRP back
+                if (n >= NGRP) ok = ok && mbar_wait1(&d_empty[g], (uint32_t)(((n / NGRP) - 1) & 1));
                 if (!ok) break;
                 asm volatile("tcgen05.fence::after_thread_sync;");
                 const uint32_t xa = smem_u32(Xs + s * XBYTES), ta = smem_u32(Ts);
-                const uint32_t dcol = tmem + buf * D;
+                const uint32_t dcol = tmem + g * D;
 #pragma unroll
                 for (int sp = 0; sp < 3; ++sp)
 #pragma unroll
@@ -223,7 +232,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                         mma_bf16(dcol, desc_sw128(xa + koff), desc_sw128(ta + sp * XBYTES + koff),
                                  (uint32_t)(sp > 0 || ks > 0));
                     }
-                mma_commit(&mma_done[buf]);
+                mma_commit(&mma_done[g]);
                 mma_commit(&x_empty[s]);
                 // refill the stage the previous item used
                 if (n >= 1 && n - 1 + ESTAGES < count) {
@@ -238,49 +247,51 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             }
         }
     } else {
-        // ---------------------------------------------------- epilogue warps
+        // ---------------------------------------------------- epilogue groups
+        const int g = warp >> 2, wq = warp & 3;   // group, tensor-memory lane quarter
+        const int gt = wq * 32 + lane;             // thread in group = token in block = lane
+        const int bar_id = 1 + g;
+        EncCol *cols = cols_s + g * D;
+        uint32_t *R = Rs + g * EB * W;
         int ht_cols = -1;
-        const int i = warp * 32 + lane;     // token within the block = tensor-memory lane
-        for (int n = 0; n < count; ++n) {
+        for (int n = g; n < count; n += NGRP) {
             const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
             const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
             if (ht != ht_cols) {
-                asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
-                for (int e = tid; e < D; e += EPI * 32) cols_s[e] = a.cols[(size_t)ht * D + e];
-                asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+                asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
+                for (int e = gt; e < D; e += 128) cols[e] = a.cols[(size_t)ht * D + e];
+                asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
                 ht_cols = ht;
             }
-            const int buf = n & 1;
-            const bool ok = mbar_wait1(&mma_done[buf], (uint32_t)((n >> 1) & 1));
+            const bool ok = mbar_wait1(&mma_done[g], (uint32_t)((n / NGRP) & 1));
             if (!ok || *(volatile int *)&s_fail) {
                 if (!ok) atomicOr(a.status, AATC_DEV_TIMEOUT);
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;");
-            uint32_t *R = Rs + buf * EB * W;
-            // the store of item n-2 read this staging buffer; it has drained
-            // once the issuing thread waited on it (below) and the barrier passed
-            const int tl = i >> 5, ii = i & 31;
+            const int tl = gt >> 5, ii = gt & 31;
             uint32_t *Rt = R + tl * 32 * W;
             uint16_t *Rt16 = reinterpret_cast<uint16_t *>(Rt);
+            // key word w of token ii sits at ka + wtab[w].x + kb * wtab[w].y (the tiled layout)
+            uint32_t *Rk = Rt + 16 * W * (ii >> 4) + (ii & 1);
+            const int kb = (ii & 15) >> 1;
             float fin = 0.f;
             uint32_t lo = 0;
             int nb = 0, w = 0;
-            const uint32_t row_addr = tmem + ((uint32_t)(warp * 32) << 16) + buf * D;
+            const uint32_t row_addr = tmem + ((uint32_t)(wq * 32) << 16) + g * D;
+            // Pruned channels come last in record order with a zero range: they add no
+            // bits.  A non-finite input makes every coefficient non-finite (T is dense),
+            // so two coefficients per token are checked.
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(row_addr + c0, r);
-                EncCol cc[16];   // this chunk's constants, loaded before any store of the chunk
-#pragma unroll
-                for (int q = 0; q < 16; ++q) cc[q] = cols_s[c0 + q];
                 asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                if (c0 == 0) fin = __uint_as_float(r[0]) + __uint_as_float(r[1]);
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
-                    const EncCol col = cc[q];
-                    if (col.bits == 0) continue;
+                    const EncCol col = cols[c0 + q];
                     const float c = __uint_as_float(r[q]);
-                    fin += c;
                     float v = fmaf(c, col.inv, col.off);
                     v = fminf(fmaxf(v, 0.f), col.top);
                     // adding 1.5 * 2^23 rounds to the nearest integer, ties to even
@@ -289,10 +300,11 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                     const int nb2 = nb + col.bits;
                     if (nb2 >= 32) {
                         if (t == 0) {
-                            Rt[key_word_pos(ii, w, W)] = lo;
+                            const int2 wt = wtab[w];
+                            Rk[wt.x + kb * wt.y] = lo;
                         } else {
-                            Rt16[2 * (16 * (2 * w) + (ii >> 1)) + (ii & 1)] = (uint16_t)lo;
-                            Rt16[2 * (16 * (2 * w + 1) + (ii >> 1)) + (ii & 1)] = (uint16_t)(lo >> 16);
+                            Rt16[64 * w + ii] = (uint16_t)lo;   // half-words 2w, 2w+1 of token ii
+                            Rt16[64 * w + 32 + ii] = (uint16_t)(lo >> 16);
                         }
                         lo = nb2 > 32 ? (u >> (32 - nb)) : 0u;
                         nb = nb2 - 32;
@@ -304,29 +316,28 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             }
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[buf]);
-            const int tok = blk * EB + i;
+            if (lane == 0) mbar_arrive(&d_empty[g]);
+            const int tok = blk * EB + gt;
             if (!(fabsf(fin) <= 3.4e38f) && tok < a.L_new) atomicOr(a.status, AATC_DEV_NONFINITE);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staging -> bulk store
-            asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+            asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
             // ---- store the block's records
             uint32_t *out = (t ? a.vp : a.kp) + ((size_t)b * a.H + h) * (size_t)a.L_cap * W;
             const int p0 = a.start_pos + blk * EB;
             const int ntok = min(EB, a.L_new - blk * EB);
             if (ntok == EB && (p0 & 31) == 0) {
-                if (tid == 0) {
+                if (gt == 0) {
                     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
                                      out + (size_t)p0 * W),
                                  "r"(smem_u32(R)), "r"((uint32_t)(EB * W * 4))
                                  : "memory");
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-                    // the next use of the other buffer is allowed while this one drains;
-                    // before this buffer is written again (item n+2) at most one group may be pending
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    // the group writes this staging buffer again with its next item
+                    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                 }
             } else if (t == 0) {
                 // partial block: per-token words (keys)
-                for (int e = tid; e < ntok * W; e += EPI * 32) {
+                for (int e = gt; e < ntok * W; e += 128) {
                     const int ti = e / W, ww = e % W, pos = p0 + ti;
                     const uint32_t word = R[(ti >> 5) * 32 * W + key_word_pos(ti & 31, ww, W)];
                     out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, ww, W)] = word;
@@ -335,19 +346,19 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 // partial block: per-token half-words (values)
                 const uint16_t *R16 = reinterpret_cast<const uint16_t *>(R);
                 uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
-                for (int e = tid; e < ntok * 2 * W; e += EPI * 32) {
+                for (int e = gt; e < ntok * 2 * W; e += 128) {
                     const int ti = e / (2 * W), q = e % (2 * W), pos = p0 + ti;
                     const uint16_t hw = R16[2 * ((ti >> 5) * 32 * W + 16 * q + ((ti & 31) >> 1)) + (ti & 1)];
                     o16[2 * ((size_t)(pos >> 5) * 32 * W + 16 * q + ((pos & 31) >> 1)) + (pos & 1)] = hw;
                 }
             }
-            asm volatile("bar.sync 1, %0;" ::"r"(EPI * 32));
+            asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
         }
-        if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (gt == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
-    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * D));
+    if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NGRP * D));
 }
 
 // T3 (three bf16 terms of T, rows in record order) and the epilogue columns
@@ -424,7 +435,7 @@ bool encode_tma(CUtensorMap *m, const void *base, unsigned long long rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t enc_smem(int W) { return 1024 + TBYTES + ESTAGES * XBYTES + 2 * (size_t)EB * W * 4 + D * sizeof(EncCol); }
+size_t enc_smem(int W) { return 1024 + TBYTES + ESTAGES * XBYTES + NGRP * (size_t)EB * W * 4 + NGRP * D * sizeof(EncCol); }
 
 int sm_count_enc()
 {
