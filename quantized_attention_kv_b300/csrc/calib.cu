@@ -460,6 +460,15 @@ aatc_status launch_stats(const T *k, const T *v, const T *q, aatc_calib *h, int 
     const int nck = (N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
     const long nq = (long)G * N;
     const int nckq = (int)((nq + MOMENT_CHUNK - 1) / MOMENT_CHUNK);
+    if (sizeof(T) == 2) {   // bf16: exact digit-split contraction on the tensor cores
+        const __nv_bfloat16 *kb = reinterpret_cast<const __nv_bfloat16 *>(k);
+        const __nv_bfloat16 *vb = reinterpret_cast<const __nv_bfloat16 *>(v);
+        const __nv_bfloat16 *qb = reinterpret_cast<const __nv_bfloat16 *>(q);
+        aatc_status st = cov_tc_run(kb, H, N, h->mu_k, Sk, N, partial, h->status, s);
+        if (st == AATC_OK) st = cov_tc_run(vb, H, N, h->mu_v, Sv, N, partial, h->status, s);
+        if (st == AATC_OK) st = cov_tc_run(qb, H, nq, nullptr, Sq, nq, partial, h->status, s);
+        return st;
+    }
     k_moment_partial<T><<<dim3(nck, H), 256, 0, s>>>(k, N, h->mu_k, partial);
     k_moment_reduce<<<dim3(D * D / 256, H), 256, 0, s>>>(partial, nck, N, Sk);
     k_moment_partial<T><<<dim3(nck, H), 256, 0, s>>>(v, N, h->mu_v, partial);
@@ -478,7 +487,10 @@ size_t calib_work_bytes(int Hkv, int Hq, int N)
     const size_t mat = (size_t)D * D * sizeof(double);
     const size_t nck = (size_t)(N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
     const size_t nckq = ((size_t)G * N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
-    const size_t partial = (size_t)Hkv * (nck > nckq ? nck : nckq) * mat;
+    size_t partial = (size_t)Hkv * (nck > nckq ? nck : nckq) * mat;
+    const size_t tc = cov_tc_scratch(Hkv, (long)G * N);   // the largest of the three (rows G N >= N)
+    if (tc > partial) partial = tc;
+    partial = (partial + 255) & ~(size_t)255;
     return partial + (size_t)Hkv * 7 * mat;   // Sk Sv Sq Uq Sh Si Mk
 }
 
@@ -492,7 +504,11 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     const size_t nck = (size_t)(N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
     const size_t nckq = ((size_t)G * N + MOMENT_CHUNK - 1) / MOMENT_CHUNK;
     double *partial = base;
-    double *Sk = partial + (size_t)H * (nck > nckq ? nck : nckq) * M;
+    size_t pbytes = (size_t)H * (nck > nckq ? nck : nckq) * M * sizeof(double);
+    const size_t tc = cov_tc_scratch(H, (long)G * N);
+    if (tc > pbytes) pbytes = tc;
+    pbytes = (pbytes + 255) & ~(size_t)255;
+    double *Sk = (double *)((char *)base + pbytes);
     double *Sv = Sk + H * M, *Sq = Sv + H * M, *Uq = Sq + H * M, *Sh = Uq + H * M,
            *Si = Sh + H * M, *Mk = Si + H * M;
     aatc_status st;

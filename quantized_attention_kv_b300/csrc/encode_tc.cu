@@ -26,8 +26,11 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "tc_util.h"
 
 namespace {
+
+using namespace tc;
 
 constexpr int D = AATC_D;
 constexpr int EB = 128;                 // tokens per block (MMA M)
@@ -37,91 +40,6 @@ constexpr int EPI = 4 * NGRP;           // epilogue warps (4 per group: one per 
 constexpr int ETHREADS = (EPI + 1) * 32;
 constexpr uint32_t XBYTES = EB * D * 2; // 32 KB per x tile
 constexpr uint32_t TBYTES = 3 * D * D * 2;
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *mb, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(mb)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect(uint64_t *mb, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mb)), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *mb)
-{
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mb)) : "memory");
-}
-
-// bounded wait of one thread on a phase; false if it gave up
-__device__ __forceinline__ bool mbar_wait1(uint64_t *mb, uint32_t parity)
-{
-    const uint32_t a = smem_u32(mb);
-    // each try may suspend the thread for up to ~20 us until the phase completes
-    for (int it = 0; it < (1 << 16); ++it) {
-        uint32_t done;
-        asm volatile(
-            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-            " selp.u32 %0, 1, 0, p;\n}\n"
-            : "=r"(done)
-            : "r"(a), "r"(parity), "r"(20000)
-            : "memory");
-        if (done) return true;
-    }
-    return false;
-}
-
-__device__ __forceinline__ void tma2d(void *dst, const void *map, int x, int y, uint64_t *mb)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(map), "r"(x), "r"(y), "r"(smem_u32(mb))
-        : "memory");
-}
-
-// shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// 1024 bytes apart (the layout a {64, rows} TMA box with 128B swizzle writes)
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr)
-{
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFF) >> 4);
-    d |= (uint64_t)1 << 16;
-    d |= (uint64_t)(1024 >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
-    return d;
-}
-
-// kind::f16 instruction descriptor: bf16 A and B, fp32 accumulator, K-major
-// operands, M = 128, N = 128
-constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(D >> 3) << 17) | ((uint32_t)(EB >> 4) << 24);
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t ad, uint64_t bd, uint32_t acc)
-{
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(ad), "l"(bd), "r"(IDESC), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *mb)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mb))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
 
 __device__ __forceinline__ int key_word_pos(int i, int w, int W)
 {
@@ -422,12 +340,14 @@ EncodeTiledFn encode_tiled_fn()
     return fn;
 }
 
-bool encode_tma(CUtensorMap *m, const void *base, unsigned long long rows)
+// bf16 rows of `inner` elements (row stride inner * 2 bytes), boxes of 64 x 128
+// with 128-byte swizzle (the K-major operand tile of the kind::f16 MMAs).
+bool encode_tma(CUtensorMap *m, const void *base, unsigned long long inner, unsigned long long rows)
 {
     const EncodeTiledFn fn = encode_tiled_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
     cuuint32_t box[2] = {64, 128};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
@@ -452,13 +372,19 @@ int sm_count_enc()
 
 }  // namespace
 
+bool tma_map_bf16(void *map128, const void *base, unsigned long long inner, unsigned long long rows)
+{
+    static_assert(sizeof(CUtensorMap) <= 128, "tensor map storage");
+    return encode_tma(reinterpret_cast<CUtensorMap *>(map128), base, inner, rows);
+}
+
 aatc_status enc_build(aatc_calib *h, cudaStream_t s)
 {
     k_enc_build<<<dim3(h->Hkv, 2, D), D, 0, s>>>(h->T_k, h->T_v, h->bk32, h->bv32, h->tab, h->plan,
                                                  (__nv_bfloat16 *)h->T3, h->enc_cols);
     AATC_CUDA(cudaGetLastError());
     CUtensorMap m;
-    h->tmap_ok = encode_tma(&m, h->T3, (unsigned long long)h->Hkv * 2 * 3 * D);
+    h->tmap_ok = encode_tma(&m, h->T3, D, (unsigned long long)h->Hkv * 2 * 3 * D);
     static_assert(sizeof(CUtensorMap) <= sizeof(h->tmap_T3), "tensor map storage");
     memcpy(h->tmap_T3, &m, sizeof(m));
     return AATC_OK;
@@ -469,7 +395,7 @@ aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int
 {
     const unsigned long long rows = (unsigned long long)B * h->Hkv * L_new;
     CUtensorMap mk, mv, mt;
-    if (!encode_tma(&mk, k, rows) || !encode_tma(&mv, v, rows))
+    if (!encode_tma(&mk, k, D, rows) || !encode_tma(&mv, v, D, rows))
         return aatc_fail(AATC_ERR_CUDA, "cuTensorMapEncodeTiled failed for the encoder inputs");
     memcpy(&mt, h->tmap_T3, sizeof(mt));
     EncArgs a;

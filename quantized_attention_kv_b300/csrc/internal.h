@@ -1,6 +1,7 @@
 // internal.h -- private declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -118,6 +119,13 @@ aatc_status aatc_cuda_fail(cudaError_t e, const char *what);
 size_t calib_work_bytes(int Hkv, int Hq, int N);
 aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const void *q_cal,
                       int N, int max_sweeps, void *work, cudaStream_t s);
+// Second moments of bf16 rows on the tensor cores (cov_tc.cu):
+// S[h] = (1/count) sum_t (x_t - c_h)(x_t - c_h)^T over the `rows` rows of head
+// h (X: [H][rows][d]; center [H][d] fp64 or NULL), exact up to one rounding of
+// x - c to 28-bit fixed point.  Scratch of cov_tc_scratch(H, rows) bytes.
+size_t cov_tc_scratch(int H, long rows);
+aatc_status cov_tc_run(const __nv_bfloat16 *X, int H, long rows, const double *center, double *S, long count,
+                       void *scratch, uint32_t *status, cudaStream_t s);
 // Rebuild the fp32 operands and codec tables from the fp64 results.
 aatc_status calib_derive(aatc_calib *h, cudaStream_t s);
 
@@ -130,6 +138,10 @@ void plan_one(const int32_t *bits, int W, HeadPlan *out);
 
 // Build T3, enc_cols and the T3 tensor map (after the plans are on the device).
 aatc_status enc_build(aatc_calib *h, cudaStream_t s);
+// 2D tensor map (written to 128 bytes at map128, 64-byte aligned) over bf16
+// rows of `inner` elements: 64 x 128 boxes, 128-byte swizzle.  False if the
+// driver entry point is missing or rejects the layout.
+bool tma_map_bf16(void *map128, const void *base, unsigned long long inner, unsigned long long rows);
 // Build the fast decoder's per-head tables (after the plans are on the device).
 aatc_status dec_build(aatc_calib *h, cudaStream_t s);
 
