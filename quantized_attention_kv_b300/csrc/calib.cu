@@ -130,8 +130,9 @@ __global__ void k_moment_reduce(const double *__restrict__ partial, int nchunks,
 // AATC_DEV_NO_CONVERGENCE.
 constexpr int JAC_THREADS = 512;
 constexpr int TRI = D * (D + 1) / 2;
+constexpr int JAC_BLOCKS = 64 * 65 / 2;   // 2x2 blocks (pair k1 <= pair k2) of one round
 constexpr size_t JAC_SMEM = (size_t)(TRI + D * D) * sizeof(double) + 64 * 2 * sizeof(double) +
-                            64 * 2 * sizeof(int) + 4 * sizeof(int);
+                            64 * 2 * sizeof(int) + 4 * sizeof(int) + (size_t)JAC_BLOCKS * 2 * sizeof(uint16_t);
 
 __device__ __forceinline__ int tri(int i, int j)
 {
@@ -139,9 +140,12 @@ __device__ __forceinline__ int tri(int i, int j)
     return i * D - (i * (i - 1)) / 2 + (j - i);
 }
 
-__global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict__ Ain, int max_sweeps,
-                                                        double *__restrict__ evals,
-                                                        double *__restrict__ evecs,
+// Two independent batches in one launch: blocks m < M0 take (Ain0, evals0,
+// evecs0)[m], the others (Ain1, evals1, evecs1)[m - M0].
+__global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict__ Ain0, double *__restrict__ evals0,
+                                                        double *__restrict__ evecs0, int M0,
+                                                        const double *__restrict__ Ain1, double *__restrict__ evals1,
+                                                        double *__restrict__ evecs1, int max_sweeps,
                                                         uint32_t *status)
 {
     extern __shared__ double smem[];
@@ -150,8 +154,21 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
     double *cs = V + D * D;                // [64][2]
     int *pq = (int *)(cs + 128);           // [64][2]
     int *flag = pq + 128;                  // [0] rotated, [1] nonfinite
-    const int m = blockIdx.x, tid = threadIdx.x;
+    uint16_t *kpair = reinterpret_cast<uint16_t *>(flag + 4);   // [JAC_BLOCKS][2]: block -> (k1, k2)
+    const int tid = threadIdx.x;
+    const bool second = (int)blockIdx.x >= M0;
+    const int m = second ? blockIdx.x - M0 : blockIdx.x;
+    const double *Ain = second ? Ain1 : Ain0;
+    double *evals = second ? evals1 : evals0;
+    double *evecs = second ? evecs1 : evecs0;
     const double *Am = Ain + (size_t)m * D * D;
+    for (int blk = tid; blk < JAC_BLOCKS; blk += JAC_THREADS) {
+        int k2 = (int)((sqrt(8.0 * blk + 1.0) - 1.0) * 0.5);
+        while (k2 * (k2 + 1) / 2 > blk) --k2;
+        while ((k2 + 1) * (k2 + 2) / 2 <= blk) ++k2;
+        kpair[2 * blk] = (uint16_t)(blk - k2 * (k2 + 1) / 2);
+        kpair[2 * blk + 1] = (uint16_t)k2;
+    }
 
     if (tid < 2) flag[tid] = 0;
     __syncthreads();
@@ -196,11 +213,8 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
             }
             __syncthreads();
             // A <- J^T A J, one 2x2 block (pair k1, pair k2) per task, k1 <= k2
-            for (int blk = tid; blk < 64 * 65 / 2; blk += JAC_THREADS) {
-                int k2 = (int)((sqrt(8.0 * blk + 1.0) - 1.0) * 0.5);
-                while (k2 * (k2 + 1) / 2 > blk) --k2;
-                while ((k2 + 1) * (k2 + 2) / 2 <= blk) ++k2;
-                int k1 = blk - k2 * (k2 + 1) / 2;
+            for (int blk = tid; blk < JAC_BLOCKS; blk += JAC_THREADS) {
+                const int k1 = kpair[2 * blk], k2 = kpair[2 * blk + 1];
                 int p1 = pq[2 * k1], q1 = pq[2 * k1 + 1];
                 double c1 = cs[2 * k1], s1 = cs[2 * k1 + 1];
                 if (k1 == k2) {
@@ -312,13 +326,14 @@ __global__ void k_transpose64(const double *__restrict__ X, double *__restrict__
 // Bit allocation and step sizes
 // ---------------------------------------------------------------------------
 
-__device__ double gauss_pdf(double x) { return exp(-0.5 * x * x) * 0.3989422804014327; }
-__device__ double gauss_cdf(double x) { return 0.5 * erfc(-x * 0.7071067811865476); }
+// The step sizes depend only on the width b: computed once on the host.
+double gauss_pdf(double x) { return exp(-0.5 * x * x) * 0.3989422804014327; }
+double gauss_cdf(double x) { return 0.5 * erfc(-x * 0.7071067811865476); }
 
 // Centroid map of a mid-rise uniform quantizer with N levels on N(0,1): given
 // the step D (which fixes the cells), the step whose levels c_u D best fit
 // the cell means in the MSE sense, sum_u c_u E[x; cell_u] / sum_u c_u^2 P_u.
-__device__ double centroid_step(int N, double Dlt)
+double centroid_step(int N, double Dlt)
 {
     double num = 0.0, den = 0.0;
     for (int u = 0; u < N; ++u) {
@@ -334,7 +349,7 @@ __device__ double centroid_step(int N, double Dlt)
 
 // The MSE-optimal step is the fixed point of centroid_step; solved by the
 // secant method on centroid_step(D) - D from D0 = 4/N.
-__device__ double gauss_uniform_step(int b)
+double gauss_uniform_step(int b)
 {
     const int N = 1 << b;
     double x0 = 4.0 / N, x1 = centroid_step(N, x0);
@@ -357,10 +372,26 @@ __device__ double gauss_uniform_step(int b)
 // g* is taken, and gains equal to g* are taken in (j, t) order until the
 // budget is met.  b_j = number of taken gains of channel j.
 // Delta_j = s_{b_j} sqrt(lam_j) rounded to fp32.
+struct StepTable {
+    double s[AATC_MAXB + 1];   // s[b] = MSE-optimal uniform step of N(0,1) at b bits, s[0] = 0
+};
+
+const StepTable &step_table()
+{
+    static const StepTable t = [] {
+        StepTable r;
+        r.s[0] = 0.0;
+        for (int b = 1; b <= AATC_MAXB; ++b) r.s[b] = gauss_uniform_step(b);
+        return r;
+    }();
+    return t;
+}
+
 __global__ void __launch_bounds__(1024) k_waterfill(const double *__restrict__ lam_k,
                                                     const double *__restrict__ lam_v, int Bbits,
                                                     int32_t *__restrict__ bits_k, int32_t *__restrict__ bits_v,
-                                                    float *__restrict__ step_k, float *__restrict__ step_v)
+                                                    float *__restrict__ step_k, float *__restrict__ step_v,
+                                                    StepTable steps)
 {
     __shared__ double gain[D * AATC_MAXB];
     __shared__ double s_tab[AATC_MAXB + 1];
@@ -371,7 +402,7 @@ __global__ void __launch_bounds__(1024) k_waterfill(const double *__restrict__ l
     const int j = t >> 3, tb = t & 7;
     const double g = ldexp(fmax(lam[j], 0.0), -2 * tb);
     gain[t] = g;
-    if (t <= AATC_MAXB) s_tab[t] = (t == 0) ? 0.0 : gauss_uniform_step(t);
+    if (t <= AATC_MAXB) s_tab[t] = steps.s[t];
     if (t < D) nb[t] = 0;
     if (t == 0) mx = 0ull;
     __syncthreads();
@@ -521,17 +552,17 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     if (st != AATC_OK) return st;
 
     AATC_CUDA(cudaFuncSetAttribute(k_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)JAC_SMEM));
-    // query metric: Sq = Uq Lq Uq^T ; Sh = Sq^{1/2}, Si = Sq^{-1/2}
-    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Sq, max_sweeps, h->lam_q, Uq, h->status);
+    // query metric: Sq = Uq Lq Uq^T ; Sh = Sq^{1/2}, Si = Sq^{-1/2}; with it the
+    // value KLT Sv = Uv Lv Uv^T (independent of the key path)
+    k_jacobi<<<2 * H, JAC_THREADS, JAC_SMEM, s>>>(Sq, h->lam_q, Uq, H, Sv, h->lam_v, h->U_v, max_sweeps, h->status);
     const dim3 gg(D * D / 256, H);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_SQRT, Uq, 1, Sh);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_INVSQRT, Uq, 1, Si);
     // whitened key covariance Mk = Sh Sk Sh (Jacobi reads its symmetric part)
     k_gemm64<<<gg, 256, 0, s>>>(Sh, 0, nullptr, DIAG_NONE, Sk, 0, Uq);       // Uq reused as tmp
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, nullptr, DIAG_NONE, Sh, 0, Mk);
-    // KLTs: Mk = Uk Lk Uk^T (Uk kept in Uq), Sv = Uv Lv Uv^T
-    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Mk, max_sweeps, h->lam_k, Uq, h->status);
-    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Sv, max_sweeps, h->lam_v, h->U_v, h->status);
+    // key KLT: Mk = Uk Lk Uk^T (Uk kept in Uq)
+    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Mk, h->lam_k, Uq, H, nullptr, nullptr, nullptr, max_sweeps, h->status);
     // Tk = Uk^T Sh, Ak = Uk^T Si, Tk^{-1} = Si Uk, Tv = Uv^T
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Sh, 0, h->T_k);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Si, 0, h->A_k);
@@ -539,7 +570,7 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     k_transpose64<<<gg, 256, 0, s>>>(h->U_v, h->T_v);
     AATC_CUDA(cudaGetLastError());
     k_waterfill<<<dim3(H, 2), 1024, 0, s>>>(h->lam_k, h->lam_v, h->Bbits, h->bits_k, h->bits_v,
-                                            h->step_k, h->step_v);
+                                            h->step_k, h->step_v, step_table());
     AATC_CUDA(cudaGetLastError());
     return calib_derive(h, s);
 }

@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(128, 1) k_cov_tc(const __grid_constant__ CUten
             for (int c0 = 0; c0 < D; c0 += 16) {
                 uint32_t r[16];
                 tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + k * D + c0, r);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                tmem_wait_ld(r);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
                     *reinterpret_cast<float4 *>(dst + c0 + 4 * q4) =

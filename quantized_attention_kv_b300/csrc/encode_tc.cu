@@ -199,13 +199,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             const uint32_t row_addr = tmem + ((uint32_t)(wq * 32) << 16) + g * D;
             // Pruned channels come last in record order with a zero range: they add no
             // bits.  A non-finite input makes every coefficient non-finite (T is dense),
-            // so two coefficients per token are checked.
-#pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(row_addr + c0, r);
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                if (c0 == 0) fin = __uint_as_float(r[0]) + __uint_as_float(r[1]);
+            // so two coefficients per token are checked.  The next 16 accumulator
+            // columns are in flight while the current 16 are quantized.
+            auto quantize16 = [&](const uint32_t (&r)[16], int c0) {
 #pragma unroll
                 for (int q = 0; q < 16; ++q) {
                     const EncCol col = cols[c0 + q];
@@ -231,6 +227,19 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                         nb = nb2;
                     }
                 }
+            };
+            uint32_t ra[16], rb[16];
+            tmem_ld16(row_addr, ra);
+            tmem_wait_ld(ra);
+            fin = __uint_as_float(ra[0]) + __uint_as_float(ra[1]);
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                tmem_ld16(row_addr + c0 + 16, rb);
+                quantize16(ra, c0);
+                tmem_wait_ld(rb);
+                if (c0 + 32 < D) tmem_ld16(row_addr + c0 + 32, ra);
+                quantize16(rb, c0 + 16);
+                tmem_wait_ld(ra);
             }
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
