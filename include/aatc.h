@@ -84,6 +84,11 @@ typedef struct {
  * (the B largest gains lam_j 4^-t, ties to the smaller j then t), and steps
  * Delta_j = s_{b_j} sqrt(lam_j) with s_b the MSE-optimal uniform step for a
  * unit Gaussian.  On success *out receives a new handle (free with aatc_free).
+ * Precision: fp32 inputs accumulate the moments in fp64.  bf16 inputs compute
+ * them on the tensor cores from x - mean rounded once to 28-bit fixed point
+ * (one power-of-two scale per channel); the contraction itself is exact, so
+ * the moments differ from fp64 ones only by that rounding (relative 2^-27 of
+ * each channel's largest |x - mean|).  Eigensolver and allocation run in fp64.
  * Synchronizes `stream` once.  Returns NO_CONVERGENCE / NONFINITE from the
  * device status; the handle is not created then. */
 aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const void *v_cal,
@@ -144,11 +149,12 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
  * need not be initialized (the call sets up what it needs, on `stream`);
  * calls that share a workspace must be ordered on one stream.  Two kernels
  * are launched on `stream`: a split kernel that writes one partial result per
- * (row, KV head, split) to the workspace, and a combine kernel (programmatic
- * dependent launch: its prologue overlaps the split kernel's tail) that
- * merges the splits and writes `out`.  Records above 16 words or layouts
- * whose bytes hold more than four code pieces take a slower general path of
- * three kernels.
+ * (row, KV head group, split) to the workspace -- its running softmax
+ * maximum and sum, and Uv (Delta_V o sum_i p_i u_i) over its tokens -- and a
+ * combine kernel (programmatic dependent launch) that merges the splits and
+ * adds mu_v - Uv (Delta_V o mid).  Records above 16 words or layouts whose
+ * bytes hold more than four code pieces take a slower general path of three
+ * kernels.
  * Errors: CAPACITY if L > L_cap; INVALID_ARG if the workspace is too small or
  * L_cap is not a multiple of 32. */
 aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
