@@ -147,8 +147,10 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
  * applied once per head.  workspace: device scratch of at least
  * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned, contents
  * need not be initialized (the call sets up what it needs, on `stream`);
- * calls that share a workspace must be ordered on one stream.  Two kernels
- * are launched on `stream`: a split kernel that writes one partial result per
+ * calls that share a workspace must be ordered on one stream.  When the rows
+ * and KV head groups already fill the GPU, each is one CTA of a single kernel
+ * that writes `out` directly (no workspace).  Otherwise two kernels are
+ * launched on `stream`: a split kernel that writes one partial result per
  * (row, KV head group, split) to the workspace -- its running softmax
  * maximum and sum, and Uv (Delta_V o sum_i p_i u_i) over its tokens -- and a
  * combine kernel (programmatic dependent launch) that merges the splits and
@@ -163,7 +165,8 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
                                   void *workspace, size_t ws_bytes, void *stream);
 
 /* Bytes of device workspace aatc_decode_attention needs for B rows of up to
- * L tokens (0 on invalid arguments). */
+ * L tokens.  0 when the call needs none (workspace may then be NULL) and on
+ * invalid arguments. */
 size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L);
 
 /* Decode attention that allocates nothing.  The pages have no counterpart:

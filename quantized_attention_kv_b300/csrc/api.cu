@@ -244,7 +244,7 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const 
         return aatc_fail(AATC_ERR_INVALID_ARG, "packed caches must be non-NULL and 16-byte aligned");
     if (seq_lens && ((uintptr_t)seq_lens & 3u)) return aatc_fail(AATC_ERR_INVALID_ARG, "seq_lens misaligned");
     const size_t need = decode_ws_bytes(calib, B, L);
-    if (!workspace || !aligned16(workspace) || ws_bytes < need)
+    if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need))
         return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);
     return decode_run(calib, q, k_packed, v_packed, L_cap, seq_lens, L, B, out, workspace, ws_bytes,
                       (cudaStream_t)stream);

@@ -82,13 +82,14 @@ struct FastGeom {
     int units;       // B * Hkv * HG
     int S;           // splits (CTAs, partial slots) per unit
     int tiles_per;   // tiles per split
-    size_t stage_bytes, stage_region, uv_off, smem, ws_total;
+    size_t stage_bytes, stage_region, uv_off, part_off, smem, ws_total;
+    bool single;     // one split per unit: the split kernel writes the output itself
 };
 
 // Shared memory of k_decode_fast, in carve order.
 struct FastSmem {
     size_t stages, mat, blob, qtab, pbuf, mbar, scr, total;
-    size_t uv_off;
+    size_t uv_off, part_off;
 };
 
 FastSmem fast_smem_layout(int FW, int FST, int W, int NT, int ksteps, int groups)
@@ -98,7 +99,8 @@ FastSmem fast_smem_layout(int FW, int FST, int W, int NT, int ksteps, int groups
     const size_t tiles = (size_t)FW * FST * 256 * W;
     // epilogue: the warps' piece sums, then Delta_V o channel sums [D][8], partial outputs [4][8][D]
     m.uv_off = ((size_t)FW * 64 * groups * HPG * 4 + 127) & ~(size_t)127;
-    const size_t epi_region = m.uv_off + (size_t)D * 8 * 4 + (size_t)4 * 8 * D * 4;
+    m.part_off = m.uv_off + (size_t)D * 8 * 4 + (size_t)4 * 8 * D * 4;   // the split's partial (single split)
+    const size_t epi_region = m.part_off + (size_t)HPG * PROW * 4;
     m.stages = tiles > epi_region ? tiles : epi_region;
     m.mat = (size_t)D * D * 4;   // A_k^T, then Uv^T
     m.blob = sizeof(DecBlob);
@@ -138,13 +140,16 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.stage_bytes = (size_t)256 * h->W;
     f.n_tiles = L > 0 ? (L + TILE - 1) / TILE : 0;
     f.units = B * h->Hkv * f.HG;
+    f.part_off = m.part_off;
     const int per_sm = fast_ctas_per_sm(f.GMAX, f.NT, f.FW, f.smem);
     const int C = sm_count() * per_sm;
     f.S = C / f.units > 1 ? C / f.units : 1;
     if (f.S > f.n_tiles) f.S = f.n_tiles > 0 ? f.n_tiles : 1;
+    // A unit with a single split finishes in its own CTA (no combine kernel, no workspace).
+    f.single = f.n_tiles > 0 && f.S == 1;
     f.tiles_per = f.n_tiles > 0 ? (f.n_tiles + f.S - 1) / f.S : 1;
     f.S = f.n_tiles > 0 ? (f.n_tiles + f.tiles_per - 1) / f.tiles_per : 1;
-    f.ws_total = (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
+    f.ws_total = f.single ? 0 : (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
     return f;
 }
 
@@ -238,7 +243,11 @@ struct FastArgs {
     const int32_t *seq_lens;
     int L, L_cap, W, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;
     uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
-    uint32_t uv_off;        // epilogue: offset of Uv^T in the stage region (after the warp sums)
+    uint32_t uv_off;        // epilogue: offset of the channel sums in the stage region (after the warp sums)
+    uint32_t part_off;      // epilogue: offset of this split's partial in shared memory (single split)
+    int single;             // one split per unit (S = 1): finish here and write out
+    float *out;             // [B][Hq][D] (single split)
+    const float *vcst;      // [Hkv][D] mu_v - Uv (Delta_V o mid) (single split)
     const DecBlob *blob;    // [Hkv]
     const float *UvT;       // [Hkv][D][D]
     const void *q;          // [B][Hq][D] of the handle's dtype
@@ -747,7 +756,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     }
     __syncthreads();
     {
-        float *P = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
+        float *P = a.single ? reinterpret_cast<float *>(stage_base + a.part_off)
+                               : a.part + ((size_t)u * a.S + sp) * HPG * PROW;
         for (int e = tid; e < HPG * D; e += NTH) {
             const int i = e >> 7, j = e & (D - 1);
             const float y = (red[(0 * 8 + i) * D + j] + red[(1 * 8 + i) * D + j]) +
@@ -759,6 +769,21 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             P[tid * PROW + 1] = failed ? 0.f : cl[tid];
             P[tid * PROW + 2] = 0.f;
             P[tid * PROW + 3] = 0.f;
+        }
+    }
+    if (!a.single) return;
+
+    // ---- the unit's only split: o = y / l + (mu_v - Uv (Delta_V o mid))
+    __syncthreads();
+    {
+        const int Hq = a.Hkv * a.G;
+        const float *P = reinterpret_cast<const float *>(stage_base + a.part_off);
+        for (int e = tid; e < HPG * D; e += NTH) {
+            const int i = e >> 7, j = e & (D - 1), gi = hg * HPG + i;
+            const float Ls = P[i * PROW + 1];
+            if (gi < a.G)
+                a.out[((size_t)b * Hq + h * a.G + gi) * D + j] =
+                    Ls > 0.f ? P[i * PROW + 4 + j] / Ls + a.vcst[h * D + j] : 0.f;
         }
     }
 }
@@ -1188,22 +1213,21 @@ aatc_status smem_limit(const void *kern, size_t bytes)
     return AATC_OK;
 }
 
+template <typename K>
+aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a, cudaStream_t s)
+{
+    aatc_status st = smem_limit((const void *)kern, f.smem);
+    if (st != AATC_OK) return st;
+    kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
+}
+
 template <int GMAX, int NT, int FW>
 aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s)
 {
-    if (dt == AATC_BF16) {
-        auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16>;
-        aatc_status st = smem_limit((const void *)kern, f.smem);
-        if (st != AATC_OK) return st;
-        kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
-    } else {
-        auto kern = k_decode_fast<GMAX, NT, FW, float>;
-        aatc_status st = smem_limit((const void *)kern, f.smem);
-        if (st != AATC_OK) return st;
-        kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
-    }
-    AATC_CUDA(cudaGetLastError());
-    return AATC_OK;
+    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16>, FW, f, a, s);
+    return launch_variant(k_decode_fast<GMAX, NT, FW, float>, FW, f, a, s);
 }
 
 aatc_status launch_combine(const FastGeom &f, const aatc_calib *h, const float *part, float *out, cudaStream_t s)
@@ -1271,6 +1295,10 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.FST = f.FST;
         a.stage_region = (uint32_t)f.stage_region;
         a.uv_off = (uint32_t)f.uv_off;
+        a.part_off = (uint32_t)f.part_off;
+        a.single = f.single ? 1 : 0;
+        a.out = out;
+        a.vcst = h->vcst;
         a.UvT = h->UvT32;
         a.n_tiles = f.n_tiles;
         a.units = f.units;
@@ -1292,6 +1320,7 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
             else st = launch_fast<4, 2, 8>(f, a, h->dtype, s);
         }
         if (st != AATC_OK) return st;
+        if (f.single) return AATC_OK;   // single splits finished in the split kernel
         return launch_combine(f, h, part, out, s);
     }
     if (h->W > GEN_MAX_W) return aatc_fail(AATC_ERR_UNSUPPORTED, "record of %d words", h->W);

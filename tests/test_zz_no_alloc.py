@@ -65,7 +65,7 @@ def test_static_scratch_rejects_shapes_beyond_its_size():
     f = _static_fn()
     wl = synth.WORKLOADS["tiny"]
     k, v, q = synth.calib_inputs(wl, device="cuda")
-    cal = aatc.calibrate(k, v, q, wl.bits)
+    cal = aatc.calibrate(k, v, q, 5.0)        # 20-word records: the general decode path
     B = 600                                   # needs more than the 4 MiB of built-in scratch
     assert aatc.workspace_size(cal, B, 128) > (4 << 20)
     qd = torch.zeros(B, wl.n_q_heads, 128, dtype=wl.dtype, device="cuda")
