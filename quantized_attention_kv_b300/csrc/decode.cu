@@ -321,6 +321,10 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
         bulk_g2s(mat_s, a.AkT + (size_t)h * D * D, (uint32_t)(D * D * 4), mat_bar);
     }
+    // Launched with programmatic dependent launch: everything above reads only
+    // the handle; the query, the row lengths, the cache and the workspace may
+    // be written by the kernel before this one on the stream.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // query rows of the head group: element e = (head e / D, k = e % D)
     constexpr int QPER = (HPG * D + NTH - 1) / NTH;
     float qv[QPER];
@@ -810,6 +814,8 @@ __global__ void __launch_bounds__(CB_THREADS) k_decode_combine_fast(
     extern __shared__ __align__(128) float Ps[];           // [CS][HPG][PROW]
     __shared__ float Mh[8], Lh[8], Rh[8];
     __shared__ uint64_t bar;
+    // the next kernel may start its prologue; it waits for this grid before touching shared data
+    asm volatile("griddepcontrol.launch_dependents;");
     const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = u / (Hkv * HG), h = (u / HG) % Hkv, hg = u % HG;
     const float cst = vcst[h * D + (tid & (D - 1))];
@@ -1218,8 +1224,19 @@ aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a,
 {
     aatc_status st = smem_limit((const void *)kern, f.smem);
     if (st != AATC_OK) return st;
-    kern<<<f.units * f.S, FW * 32, f.smem, s>>>(a);
-    AATC_CUDA(cudaGetLastError());
+    // programmatic dependent launch: the prologue that reads only the handle
+    // overlaps the tail of the previous kernel on the stream
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(f.units * f.S);
+    cfg.blockDim = dim3(FW * 32);
+    cfg.dynamicSmemBytes = f.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, a));
     return AATC_OK;
 }
 

@@ -71,6 +71,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     __shared__ int2 wtab[16];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // a dependent decode launch may start its prologue (it waits for this grid
+    // before reading the cache)
+    asm volatile("griddepcontrol.launch_dependents;");
     if (tid < 16) {
         const int r = tid >> 2, nr = min(4, a.W - 4 * r);
         wtab[tid] = make_int2(64 * r + 2 * (tid - 4 * r), 2 * nr);
