@@ -127,6 +127,11 @@ aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const
  * above); L_cap must be a multiple of 32.  Only the bits of tokens
  * start_pos .. start_pos+L_new-1 are written (value words are shared by two
  * tokens and written 16 bits at a time).  L_new = 0 is a no-op.
+ * Kernels: L_new <= 16 (a decode step's new tokens) takes a small append
+ * kernel (one CTA per KV head, tensor and row; fp32 transform), launched as a
+ * programmatic dependent of the previous kernel on `stream` so that staging T
+ * overlaps it; longer bf16 inputs take the tensor-core encoder, fp32 inputs a
+ * plain fp32 encoder.
  * Errors: CAPACITY if start_pos + L_new > L_cap; INVALID_ARG if L_cap is not a
  * multiple of 32.  Non-finite inputs set the handle's NONFINITE status (codes
  * of such rows are unspecified). */

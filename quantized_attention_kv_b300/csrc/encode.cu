@@ -6,6 +6,10 @@
 // channel at its allocated width) and "Spend Bits Where Queries Look",
 // Abstract (fixed per-token bit count).
 //
+// Kernels: k_encode_append (up to 16 new tokens per row, a decode step),
+// k_encode_simple (fp32 inputs); bf16 prefill goes to k_encode_tc
+// (encode_tc.cu).
+//
 // Cache tiling (per batch row and KV head, 32-token tiles of 32*W words):
 // keys: token i of a tile, record word w -> half i/16 (16*W words each), row
 // r = w/4 (n_r = min(4, W-4r) words, row r at 64*r), word
@@ -124,12 +128,128 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     }
 }
 
+// Append path: a few new tokens per row, as in a decode step.  One CTA of
+// D threads per (KV head, tensor, batch row); thread j owns coefficient j and
+// computes it exactly as k_encode_simple does (fp32 FMA over k = 0..127,
+// minus T mu, scaled, rounded half to even, clamped).  The codes are ORed into
+// the token's record in shared memory and the record goes to its place in the
+// tiled cache.  T (64 KB, read from the handle) is staged in shared memory by
+// cp.async before the kernel waits for its predecessor on the stream
+// (programmatic dependent launch), so that copy overlaps the previous kernel;
+// the new tokens are read and the cache written only after the wait.
+constexpr int APPEND_MAX = 16;    // tokens per row served by this path
+constexpr int TPAD = D + 4;       // floats per staged row of T (16-byte rows, conflict-free float4 reads)
+constexpr int MAX_W = 8 * D / 32; // record words at 8 bits per channel
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(D) k_encode_append(
+    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, int L_cap, int Hkv, int W,
+    const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
+    const float *__restrict__ bv, const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
+    uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
+{
+    asm volatile("griddepcontrol.launch_dependents;");
+    extern __shared__ __align__(16) float Ts[];   // [D][TPAD]: row j of T
+    __shared__ float xs[D];
+    __shared__ uint32_t rec[MAX_W];
+    const int h = blockIdx.x, tensor = blockIdx.y, b = blockIdx.z, j = threadIdx.x;
+    const int ht = h * 2 + tensor;
+
+    // handle data only, ahead of the wait
+    const float4 *src = reinterpret_cast<const float4 *>((tensor == 0 ? Tk : Tv) + (size_t)h * D * D);
+#pragma unroll 8
+    for (int i = 0; i < D * D / 4 / D; ++i) {
+        const int e4 = j + i * D;   // float4 e4 of T: row e4 / 32, columns 4 (e4 % 32) ..
+        cp_async16(&Ts[(e4 >> 5) * TPAD + (e4 & 31) * 4], src + e4);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    const float bias = (tensor == 0 ? bk : bv)[h * D + j];
+    const float inv = tabs[ht].inv_step[j], mid = tabs[ht].mid[j], top = tabs[ht].top[j];
+    const int bits = tabs[ht].bits[j], off = plans[ht].off[j];
+    asm volatile("cp.async.wait_all;" ::: "memory");
+
+    // the new tokens and the cache may belong to the previous kernel on the stream
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const T *x = (tensor == 0 ? k : v) + ((size_t)b * Hkv + h) * L_new * D;
+    uint32_t *out = (tensor == 0 ? kp : vp) + ((size_t)b * Hkv + h) * L_cap * W;
+    bool bad = false;
+    for (int n = 0; n < L_new; ++n) {
+        const float xv = to_f32(x[(size_t)n * D + j]);
+        bad |= !isfinite(xv);
+        xs[j] = xv;
+        if (j < W) rec[j] = 0u;
+        __syncthreads();   // xs, rec, and (first token) every thread's staged rows of T
+        const float4 *tr = reinterpret_cast<const float4 *>(&Ts[j * TPAD]);
+        float acc = 0.f;
+#pragma unroll 8
+        for (int k4 = 0; k4 < D / 4; ++k4) {
+            const float4 t = tr[k4];
+            acc = fmaf(t.x, xs[4 * k4 + 0], acc);
+            acc = fmaf(t.y, xs[4 * k4 + 1], acc);
+            acc = fmaf(t.z, xs[4 * k4 + 2], acc);
+            acc = fmaf(t.w, xs[4 * k4 + 3], acc);
+        }
+        if (bits > 0) {
+            float vq = fmaf(acc - bias, inv, mid);
+            vq = fminf(fmaxf(rintf(vq), 0.f), top);
+            const uint32_t u = (uint32_t)vq;
+            const int sh = off & 31;
+            atomicOr(&rec[off >> 5], u << sh);
+            if (sh + bits > 32) atomicOr(&rec[(off >> 5) + 1], u >> (32 - sh));
+        }
+        __syncthreads();
+        const int pos = start_pos + n;
+        if (tensor == 0) {
+            if (j < W) out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, j, W)] = rec[j];
+        } else if (j < 2 * W) {
+            const size_t word = (size_t)(pos >> 5) * 32 * W + 16 * j + ((pos & 31) >> 1);
+            reinterpret_cast<uint16_t *>(out)[2 * word + (pos & 1)] = (uint16_t)(rec[j >> 1] >> (16 * (j & 1)));
+        }
+        __syncthreads();   // xs and rec are reused by the next token
+    }
+    if (__syncthreads_or(bad) && j == 0) atomicOr(status, AATC_DEV_NONFINITE);
+}
+
+template <typename T>
+aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int B, int L_new, int start_pos,
+                          int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+{
+    static const size_t smem = (size_t)D * TPAD * sizeof(float);
+    auto kern = k_encode_append<T>;
+    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(h->Hkv, 2, B);
+    cfg.blockDim = dim3(D);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, (const T *)k, (const T *)v, L_new, start_pos, L_cap, h->Hkv, h->W,
+                                 (const float *)h->Tk32, (const float *)h->Tv32, (const float *)h->bk32,
+                                 (const float *)h->bv32, (const CodecTables *)h->tab, (const HeadPlan *)h->plan,
+                                 kp, vp, h->status));
+    return AATC_OK;
+}
+
 }  // namespace
 
 aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
                        int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
 {
     if (L_new == 0 || B == 0) return AATC_OK;
+    if (L_new <= APPEND_MAX && B <= 65535) {   // a decode step's new tokens
+        if (h->dtype == AATC_BF16) return launch_append<__nv_bfloat16>(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
+        return launch_append<float>(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
+    }
     if (h->dtype == AATC_BF16 && h->tmap_ok && h->W <= 16)
         return encode_tc_run(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
     const size_t smem = (size_t)D * D * 4 + (size_t)ENC_TILE * (D + 1) * 4 +

@@ -144,7 +144,7 @@ def _bf16_two_heads():
     return _bf16_cache
 
 
-@pytest.mark.parametrize("L_new,start,L_cap,B", [(1024, 0, 1024, 2), (1000, 24, 1056, 2), (1, 7, 32, 1),
+@pytest.mark.parametrize("L_new,start,L_cap,B", [(1024, 0, 1024, 2), (1000, 24, 1056, 2), (17, 7, 32, 1),
                                                  (300, 64, 384, 3), (257, 0, 288, 1)])
 def test_encode_bf16_tensor_core_path(L_new, start, L_cap, B):
     """bf16 inputs go through the tensor-core encoder: full aligned 128-token
@@ -168,6 +168,67 @@ def test_encode_bf16_tensor_core_path(L_new, start, L_cap, B):
         for r in range(B * 2):
             oracle.cache_put(ones, kind, cache=cc[r], start=start)
         assert np.all(cc == 0xFFFFFFFF), t
+    g.check()
+
+
+def _check_written(p, x, ocal, t, kind, start, heads):
+    """Codes of the written tokens vs the oracle (rounding-tie rule), and every
+    bit of every other token untouched (the cache started as all ones)."""
+    W = ocal["W"]
+    Bsz, L_new = x.shape[0], x.shape[2]
+    _, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
+    got = _records(p, W, kind, L_new, start)
+    for h in range(heads):
+        compare_codes(got[:, h], codes[:, h], pre[:, h], ocal["bits_" + t][h])
+    cc = as_u32(p).reshape(Bsz * heads, -1).copy()
+    ones = np.full((L_new, W), 0xFFFFFFFF, dtype=np.uint32)
+    for r in range(Bsz * heads):
+        oracle.cache_put(ones, kind, cache=cc[r], start=start)
+    assert np.all(cc == 0xFFFFFFFF), t
+
+
+@pytest.mark.parametrize("case,L_new,start,L_cap,B", [("tiny", 1, 0, 32, 2), ("tiny", 16, 24, 64, 2),
+                                                      ("tiny", 3, 31, 64, 1), ("bf16", 1, 1023, 1024, 1),
+                                                      ("bf16", 5, 62, 96, 3), ("bf16", 16, 0, 32, 1),
+                                                      ("bf16", 2, 33, 64, 2)])
+def test_encode_append_path(case, L_new, start, L_cap, B):
+    """Up to 16 new tokens per row (a decode step) take the append kernel:
+    one CTA per (KV head, tensor, row), fp32 transform, records placed token
+    by token (tile boundaries and odd value half-word slots included)."""
+    c = _tiny() if case == "tiny" else _bf16_two_heads()
+    wl, ocal = c["wl"], c["ocal"]
+    H = wl.n_kv_heads
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kc, vc = synth.cache_inputs(wl, layer=2, device="cuda", seq_len=L_new, batch=B)
+    kp = torch.full((B, H, L_cap, ocal["W"]), -1, dtype=torch.int32, device="cuda")
+    vp = kp.clone()
+    aatc.encode(g, kc, vc, kp, vp, start_pos=start)
+    torch.cuda.synchronize()
+    _check_written(kp, kc, ocal, "k", oracle.KEYS, start, H)
+    _check_written(vp, vc, ocal, "v", oracle.VALUES, start, H)
+    g.check()
+
+
+def test_encode_token_by_token_matches_one_shot_oracle():
+    """A decode loop: 40 appends of one token each (every value word is
+    shared by two tokens written by different launches) give the oracle's
+    codes for all 40 tokens."""
+    c = _bf16_two_heads()
+    wl, ocal = c["wl"], c["ocal"]
+    W = ocal["W"]
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    L = 40
+    kc, vc = synth.cache_inputs(wl, layer=3, device="cuda", seq_len=L, batch=2)
+    kp = aatc.alloc_cache(g, 2, L)
+    vp = aatc.alloc_cache(g, 2, L)
+    for i in range(L):
+        aatc.encode(g, kc[:, :, i:i + 1].contiguous(), vc[:, :, i:i + 1].contiguous(), kp, vp, start_pos=i)
+    torch.cuda.synchronize()
+    for t, kind, x, p in (("k", oracle.KEYS, kc, kp), ("v", oracle.VALUES, vc, vp)):
+        _, codes, pre = oracle.encode_cache(to_np64(x), ocal, t, want_codes=True, want_pre=True)
+        got = _records(p, W, kind, L)
+        for h in range(2):
+            compare_codes(got[:, h], codes[:, h], pre[:, h], ocal["bits_" + t][h])
     g.check()
 
 
