@@ -171,14 +171,35 @@ def run_ours(args, ws, rank, local):
     # L2 (126 MB) defeat: every call reads its own copy of the packed cache,
     # rotating over enough copies that the working set is several L2 sizes
     n_rot = int(min(64, max(3, -(-3 * L2_BYTES // packed_bytes))))
-    kps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
-    vps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
+    if args.paged:
+        # paged pools: each copy's rows on shuffled blocks of args.paged tokens
+        bt = args.paged
+        bpr = -(-(L + 1) // bt)
+        gen = torch.Generator().manual_seed(1234)
+        table = torch.randperm(B * bpr + 8, generator=gen)[:B * bpr].reshape(B, bpr).to(torch.int32).to(dev)
+        kps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev) for _ in range(n_rot)]
+        vps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev) for _ in range(n_rot)]
+    else:
+        kps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
+        vps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
+
+    def enc(k_, v_, kp, vp, start):
+        if args.paged:
+            aatc.encode_paged(cal, k_, v_, kp, vp, table, start_pos=start)
+        else:
+            aatc.encode(cal, k_, v_, kp, vp, start_pos=start)
+
+    def dec(q_, kp, vp):
+        if args.paged:
+            aatc.decode_attention_paged(cal, q_, kp, vp, table, L + 1, out=out, workspace=wsb)
+        else:
+            aatc.decode_attention(cal, q_, kp, vp, L + 1, out=out, workspace=wsb)
     out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
     ws_need = aatc.workspace_size(cal, B, L + 1)
     wsb = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
     for kp, vp in zip(kps, vps):        # every copy holds a valid cache
-        aatc.encode(cal, kc, vc, kp, vp, start_pos=0)
-        aatc.encode(cal, kn, vn, kp, vp, start_pos=L)
+        enc(kc, vc, kp, vp, 0)
+        enc(kn, vn, kp, vp, L)
     torch.cuda.synchronize()
 
     q_bytes = q.numel() * q.element_size()
@@ -189,9 +210,9 @@ def run_ours(args, ws, rank, local):
 
     def step(c):
         """One step on cache copy c: prefill encode, append one token, decode."""
-        aatc.encode(cal, kc, vc, kps[c], vps[c], start_pos=0)
-        aatc.encode(cal, kn, vn, kps[c], vps[c], start_pos=L)
-        aatc.decode_attention(cal, q, kps[c], vps[c], L + 1, out=out, workspace=wsb)
+        enc(kc, vc, kps[c], vps[c], 0)
+        enc(kn, vn, kps[c], vps[c], L)
+        dec(q, kps[c], vps[c])
 
     # each step is captured once per cache copy into a CUDA graph, so the
     # timed region measures the device, not the Python launch path
@@ -207,11 +228,16 @@ def run_ours(args, ws, rank, local):
     g_dec = torch.cuda.CUDAGraph()          # decode alone, every copy once
     with torch.cuda.graph(g_dec):
         for c in range(n_rot):
-            aatc.decode_attention(cal, q, kps[c], vps[c], L + 1, out=out, workspace=wsb)
+            dec(q, kps[c], vps[c])
+    g_app = torch.cuda.CUDAGraph()          # a serving step: append one token, then decode
+    with torch.cuda.graph(g_app):
+        for c in range(n_rot):
+            enc(kn, vn, kps[c], vps[c], L)
+            dec(q, kps[c], vps[c])
     g_enc = torch.cuda.CUDAGraph()          # prefill encode alone, every copy once
     with torch.cuda.graph(g_enc):
         for c in range(n_rot):
-            aatc.encode(cal, kc, vc, kps[c], vps[c], start_pos=0)
+            enc(kc, vc, kps[c], vps[c], 0)
     torch.cuda.synchronize()
 
     for s_ in range(args.warmup):
@@ -239,6 +265,13 @@ def run_ours(args, ws, rank, local):
         for _ in range(reps):
             g_dec.replay()
         d1.record(stream)
+        g_app.replay()
+        torch.cuda.synchronize()
+        a0, a1 = ev(), ev()
+        a0.record(stream)
+        for _ in range(reps):
+            g_app.replay()
+        a1.record(stream)
         g_enc.replay()
         torch.cuda.synchronize()
         n0, n1 = ev(), ev()
@@ -249,6 +282,7 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
     dec_call_s = d0.elapsed_time(d1) / 1e3 / (reps * n_rot)
     enc_call_s = n0.elapsed_time(n1) / 1e3 / (reps * n_rot)
+    app_call_s = _max_over_ranks(a0.elapsed_time(a1) / 1e3 / (reps * n_rot), ws)
     wall = _max_over_ranks(wall, ws)
     dec_call_s = _max_over_ranks(dec_call_s, ws)
     enc_call_s = _max_over_ranks(enc_call_s, ws)
@@ -268,8 +302,8 @@ def run_ours(args, ws, rank, local):
         qd.copy_(qh, non_blocking=True)
         knd.copy_(knh, non_blocking=True)
         vnd.copy_(vnh, non_blocking=True)
-        aatc.encode(cal, knd, vnd, kp, vp, start_pos=L)
-        aatc.decode_attention(cal, qd, kp, vp, L + 1, out=out, workspace=wsb)
+        enc(knd, vnd, kp, vp, L)
+        dec(qd, kp, vp)
         outh.copy_(out, non_blocking=True)
         if evs:
             evs[1].record(stream)
@@ -309,12 +343,15 @@ def run_ours(args, ws, rank, local):
                    "l2": "defeated by rotation: each call reads its own cache copy, %d copies = %.0f MB > 126 MB L2"
                          % (n_rot, n_rot * packed_bytes / 1e6),
                    "timing": "CUDA graphs of whole steps replayed K times; CUDA events on the launching stream",
-                   "parallelism": "replicas" if ws > 1 else "single GPU"},
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "cache": ("paged, %d-token blocks, shuffled block table" % args.paged) if args.paged
+                   else "contiguous"},
         "pct_of_hbm_peak": round(100 * value / ws / peak, 2),
         "encode": {"value": round(B * L * ws / enc_call_s, 1), "unit": "tokens/s",
                    "ms": round(enc_call_s * 1e3, 4),
                    "gb_s": round((2 * B * Hkv * L * (128 * kc.element_size() + W * 4)) / enc_call_s / 1e9, 2)},
         "decode_us": round(per_launch_s * 1e6, 3),
+        "append_decode_us": round(app_call_s * 1e6, 3),
         "calibrate_ms": round(calib_ms, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(decode_bytes),
@@ -397,6 +434,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=None)
     ap.add_argument("--bits", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_TOKENS",
+                    help="run the step on paged pools with blocks of this many tokens (32 times a power of two)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     ws, rank, local = _dist()

@@ -54,7 +54,7 @@ typedef enum {
     AATC_ERR_CUDA = 3,           /* a CUDA runtime call failed */
     AATC_ERR_NO_CONVERGENCE = 4, /* Jacobi did not converge within jacobi_max_sweeps */
     AATC_ERR_NONFINITE = 5,      /* NaN/Inf in calibration or cache input */
-    AATC_ERR_CAPACITY = 6,       /* start_pos + L_new > L_cap, or L > L_cap */
+    AATC_ERR_CAPACITY = 6,       /* start_pos + L_new > L_cap, L > L_cap, or a position / block out of range */
     AATC_ERR_TIMEOUT = 7         /* a bounded wait inside a kernel gave up (reported by aatc_check) */
 } aatc_status;
 
@@ -196,6 +196,50 @@ aatc_status aatc_decode_attention_static(const aatc_calib *calib, const void *q,
                                          const uint32_t *k_packed, const uint32_t *v_packed,
                                          int L_cap, const int32_t *seq_lens, int L, int B,
                                          float *out, void *stream);
+
+/* Paged cache ([IMPL] serving integration; the layout is this library's).
+ * A pool holds n_blocks blocks.  Block p holds block_tokens tokens (32
+ * times a power of two: 32, 64, 128, ...) of every KV head: head h of block p is the
+ * block_tokens*W words starting at word (p*H_kv + h)*block_tokens*W, tiled
+ * exactly as a contiguous cache with L_cap = block_tokens (32-token tiles,
+ * layout above).  Logical block n of batch row b (its tokens
+ * n*block_tokens .. (n+1)*block_tokens - 1) is physical block
+ * block_table[b*blocks_per_row + n].  Rows may share no block they both
+ * write.  The table is read on the device, in stream order. */
+typedef struct {
+    const int32_t *block_table;   /* device [B][blocks_per_row] */
+    int blocks_per_row;           /* row stride of block_table, >= 1 */
+    int block_tokens;             /* tokens per block: 32 times a power of two */
+    int n_blocks;                 /* blocks in each pool, >= 1 */
+} aatc_pages;
+
+/* Encode into paged pools (k_pool, v_pool: device u32, n_blocks *
+ * H_kv * block_tokens * W words each).  As aatc_encode, except token n of
+ * row b goes to logical position row_start[b] + n when row_start (device
+ * int32 [B], read on the device) is given, else start_pos + n.  Kernels as
+ * aatc_encode; records of a full, 32-aligned tile leave by one bulk store per
+ * tile.
+ * Errors: INVALID_ARG for a bad `pages` (NULL table, block_tokens not 32
+ * times a power of two, ...); CAPACITY if row_start is NULL and
+ * start_pos + L_new > blocks_per_row * block_tokens.  A position or block
+ * table entry found out of range on the device skips that write and sets the
+ * handle's CAPACITY status (reported by aatc_check). */
+aatc_status aatc_encode_paged(const aatc_calib *calib, const void *k, const void *v, int B, int L_new,
+                              int start_pos, const int32_t *row_start, uint32_t *k_pool, uint32_t *v_pool,
+                              const aatc_pages *pages, void *stream);
+
+/* Decode attention over paged pools: as aatc_decode_attention, with the
+ * tiles of row b found through the block table (seq_lens / L as there;
+ * workspace of aatc_decode_workspace_size(calib, B, L) bytes).  The fast
+ * path reads each warp's block table entries three tiles ahead of their
+ * copies.
+ * Errors: as aatc_decode_attention and aatc_encode_paged; CAPACITY if
+ * L > blocks_per_row * block_tokens.  An out-of-range table entry for a tile
+ * inside a row's length sets the handle's CAPACITY status (that tile reads
+ * block 0). */
+aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, const uint32_t *k_pool,
+                                        const uint32_t *v_pool, const aatc_pages *pages, const int32_t *seq_lens,
+                                        int L, int B, float *out, void *workspace, size_t ws_bytes, void *stream);
 
 /* W = u32 words per token record of one head and tensor (B/32), or -1. */
 int aatc_record_words(const aatc_calib *calib);

@@ -27,6 +27,7 @@ D = 128
 BLOB_MAGIC, BLOB_VERSION = 0x43544141, 1
 
 EXPORTED = ["aatc_calibrate", "aatc_encode", "aatc_decode_attention", "aatc_decode_workspace_size",
+            "aatc_encode_paged", "aatc_decode_attention_paged",
             "aatc_record_words", "aatc_export_calib", "aatc_import_calib", "aatc_check", "aatc_free",
             "aatc_last_error"]
 
@@ -41,6 +42,12 @@ class CalibDesc(ctypes.Structure):
     _fields_ = [("head_dim", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("n_q_heads", ctypes.c_int),
                 ("n_calib_tokens", ctypes.c_int), ("bits_per_element", ctypes.c_double),
                 ("dtype", ctypes.c_int), ("jacobi_max_sweeps", ctypes.c_int)]
+
+
+class Pages(ctypes.Structure):
+    """aatc_pages: block table (device int32 [B][blocks_per_row]) of a paged pool."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("blocks_per_row", ctypes.c_int), ("block_tokens", ctypes.c_int),
+                ("n_blocks", ctypes.c_int)]
 
 
 _lib = None
@@ -59,6 +66,8 @@ def lib():
             "aatc_encode": (I, [P, P, P, I, I, I, I, P, P, P]),
             "aatc_decode_attention": (I, [P, P, P, P, I, P, I, I, P, P, S, P]),
             "aatc_decode_workspace_size": (S, [P, I, I]),
+            "aatc_encode_paged": (I, [P, P, P, I, I, I, P, P, P, ctypes.POINTER(Pages), P]),
+            "aatc_decode_attention_paged": (I, [P, P, P, P, ctypes.POINTER(Pages), P, I, I, P, P, S, P]),
             "aatc_record_words": (I, [P]),
             "aatc_export_calib": (I, [P, P, ctypes.POINTER(S)]),
             "aatc_import_calib": (I, [P, S, ctypes.POINTER(P)]),
@@ -257,4 +266,62 @@ def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_pa
     _check(lib().aatc_decode_attention(calib.handle, _ptr(q), _ptr(k_packed), _ptr(v_packed), k_packed.shape[2],
                                        _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+    return out
+
+
+# ----------------------------------------------------------------- paged cache
+def alloc_pool(calib: Calib, n_blocks: int, block_tokens: int, device="cuda") -> torch.Tensor:
+    """A zeroed pool of n_blocks blocks of block_tokens tokens (32 times a power of two):
+    int32 [n_blocks][H_kv][block_tokens][W]; head h of block p is tiled like a
+    contiguous cache with L_cap = block_tokens."""
+    tpb = block_tokens // TILE
+    if block_tokens <= 0 or block_tokens % TILE or tpb & (tpb - 1):
+        raise ValueError("block_tokens must be %d times a power of two" % TILE)
+    return torch.zeros(n_blocks, calib.n_kv_heads, block_tokens, calib.W, dtype=torch.int32, device=device)
+
+
+def _pages(calib: Calib, block_table: torch.Tensor, *pools: torch.Tensor) -> Pages:
+    if block_table.dim() != 2 or block_table.dtype != torch.int32:
+        raise ValueError("block_table must be int32 [B][blocks_per_row]")
+    for p in pools:
+        if p.dim() != 4 or p.shape[1] != calib.n_kv_heads or p.shape[3] != calib.W or p.element_size() != 4:
+            raise ValueError("pools must be 4-byte [n_blocks][H_kv=%d][block_tokens][W=%d], got %s"
+                             % (calib.n_kv_heads, calib.W, tuple(p.shape)))
+    if len({tuple(p.shape) for p in pools}) != 1:
+        raise ValueError("key and value pools must have the same shape")
+    bt = _ptr(block_table)
+    return Pages(bt.value, block_table.shape[1], pools[0].shape[2], pools[0].shape[0])
+
+
+def encode_paged(calib: Calib, k: torch.Tensor, v: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                 block_table: torch.Tensor, start_pos: int = 0, row_start: Optional[torch.Tensor] = None,
+                 stream=None):
+    """aatc_encode_paged: token n of row b to logical position row_start[b] + n
+    (or start_pos + n) of row b's blocks."""
+    B, H, L_new, _ = k.shape
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per batch row")
+    if row_start is not None and (row_start.dtype != torch.int32 or row_start.numel() < B):
+        raise ValueError("row_start must be int32 with one entry per batch row")
+    pg = _pages(calib, block_table, k_pool, v_pool)
+    _check(lib().aatc_encode_paged(calib.handle, _ptr(k), _ptr(v), B, L_new, int(start_pos), _ptr(row_start),
+                                   _ptr(k_pool), _ptr(v_pool), ctypes.byref(pg), _stream(stream)))
+
+
+def decode_attention_paged(calib: Calib, q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                           block_table: torch.Tensor, L: int, seq_lens: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           stream=None) -> torch.Tensor:
+    """aatc_decode_attention_paged: q [B][H_q][128] -> fp32 [B][H_q][128]."""
+    B = q.shape[0]
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must have one row per batch row")
+    pg = _pages(calib, block_table, k_pool, v_pool)
+    if out is None:
+        out = torch.empty(B, calib.n_q_heads, D, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_size(calib, B, L), 16), dtype=torch.uint8, device=q.device)
+    _check(lib().aatc_decode_attention_paged(calib.handle, _ptr(q), _ptr(k_pool), _ptr(v_pool), ctypes.byref(pg),
+                                             _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
+                                             workspace.numel() * workspace.element_size(), _stream(stream)))
     return out

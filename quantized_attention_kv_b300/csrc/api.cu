@@ -101,6 +101,8 @@ aatc_status status_from_device(uint32_t st)
         return aatc_fail(AATC_ERR_NO_CONVERGENCE, "Jacobi eigensolver did not converge");
     if (st & AATC_DEV_TIMEOUT)
         return aatc_fail(AATC_ERR_TIMEOUT, "a kernel gave up waiting for its own copies; results are invalid");
+    if (st & AATC_DEV_RANGE)
+        return aatc_fail(AATC_ERR_CAPACITY, "a cache position or block table entry was out of range (access skipped)");
     return AATC_OK;
 }
 
@@ -218,7 +220,51 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
     if (!k || !v || !k_packed || !v_packed || !aligned16(k) || !aligned16(v) || !aligned16(k_packed) ||
         !aligned16(v_packed))
         return aatc_fail(AATC_ERR_INVALID_ARG, "tensors must be non-NULL and 16-byte aligned");
-    return encode_run(calib, k, v, B, L_new, start_pos, L_cap, k_packed, v_packed, (cudaStream_t)stream);
+    return encode_run(calib, k, v, B, L_new, start_pos, nullptr, contiguous_map(L_cap), k_packed, v_packed,
+                      (cudaStream_t)stream);
+}
+
+namespace {
+aatc_status pages_map(const aatc_pages *pg, CacheMap *m)
+{
+    if (!pg) return aatc_fail(AATC_ERR_INVALID_ARG, "pages is NULL");
+    if (!pg->block_table || ((uintptr_t)pg->block_table & 3u))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "block_table must be non-NULL and 4-byte aligned");
+    const int tpb = pg->block_tokens / 32;
+    if (pg->block_tokens <= 0 || pg->block_tokens % 32 || pg->block_tokens > (1 << 24) || (tpb & (tpb - 1)))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "block_tokens = %d is not 32 times a power of two",
+                         pg->block_tokens);
+    int shift = 0;
+    while ((1 << shift) < tpb) ++shift;
+    if (pg->blocks_per_row <= 0 || pg->n_blocks <= 0)
+        return aatc_fail(AATC_ERR_INVALID_ARG, "blocks_per_row and n_blocks must be positive");
+    if ((long long)pg->blocks_per_row * pg->block_tokens > (1LL << 30))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "rows of more than 2^30 tokens");
+    *m = CacheMap{pg->block_table, pg->blocks_per_row, shift, pg->n_blocks, 0};
+    return AATC_OK;
+}
+}  // namespace
+
+aatc_status aatc_encode_paged(const aatc_calib *calib, const void *k, const void *v, int B, int L_new,
+                              int start_pos, const int32_t *row_start, uint32_t *k_pool, uint32_t *v_pool,
+                              const aatc_pages *pages, void *stream)
+{
+    g_err[0] = 0;
+    if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
+    if (B < 0 || L_new < 0 || start_pos < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
+    if (B > 32767) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
+    CacheMap m;
+    aatc_status st = pages_map(pages, &m);
+    if (st != AATC_OK) return st;
+    const long long row_tokens = (long long)pages->blocks_per_row * pages->block_tokens;
+    if (!row_start && (long long)start_pos + L_new > row_tokens)
+        return aatc_fail(AATC_ERR_CAPACITY, "start_pos + L_new = %lld exceeds blocks_per_row * block_tokens = %lld",
+                         (long long)start_pos + L_new, row_tokens);
+    if (row_start && ((uintptr_t)row_start & 3u)) return aatc_fail(AATC_ERR_INVALID_ARG, "row_start misaligned");
+    if (B == 0 || L_new == 0) return AATC_OK;
+    if (!k || !v || !k_pool || !v_pool || !aligned16(k) || !aligned16(v) || !aligned16(k_pool) || !aligned16(v_pool))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "tensors must be non-NULL and 16-byte aligned");
+    return encode_run(calib, k, v, B, L_new, start_pos, row_start, m, k_pool, v_pool, (cudaStream_t)stream);
 }
 
 size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L)
@@ -246,8 +292,34 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const 
     const size_t need = decode_ws_bytes(calib, B, L);
     if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need))
         return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);
-    return decode_run(calib, q, k_packed, v_packed, L_cap, seq_lens, L, B, out, workspace, ws_bytes,
-                      (cudaStream_t)stream);
+    return decode_run(calib, q, k_packed, v_packed, contiguous_map(L_cap), seq_lens, L, B, out, workspace,
+                      ws_bytes, (cudaStream_t)stream);
+}
+
+aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, const uint32_t *k_pool,
+                                        const uint32_t *v_pool, const aatc_pages *pages, const int32_t *seq_lens,
+                                        int L, int B, float *out, void *workspace, size_t ws_bytes, void *stream)
+{
+    g_err[0] = 0;
+    if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
+    if (B < 0 || L < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
+    if (B > 65535) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
+    CacheMap m;
+    aatc_status st = pages_map(pages, &m);
+    if (st != AATC_OK) return st;
+    const long long row_tokens = (long long)pages->blocks_per_row * pages->block_tokens;
+    if (L > row_tokens)
+        return aatc_fail(AATC_ERR_CAPACITY, "L = %d exceeds blocks_per_row * block_tokens = %lld", L, row_tokens);
+    if (B == 0) return AATC_OK;
+    if (!q || !out || !aligned16(q) || !aligned16(out))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+    if (!k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "pools must be non-NULL and 16-byte aligned");
+    if (seq_lens && ((uintptr_t)seq_lens & 3u)) return aatc_fail(AATC_ERR_INVALID_ARG, "seq_lens misaligned");
+    const size_t need = decode_ws_bytes(calib, B, L);
+    if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);
+    return decode_run(calib, q, k_pool, v_pool, m, seq_lens, L, B, out, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 int aatc_record_words(const aatc_calib *calib) { return calib ? calib->W : -1; }

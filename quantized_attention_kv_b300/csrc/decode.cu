@@ -241,7 +241,8 @@ __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) 
 struct FastArgs {
     const uint32_t *kp, *vp;
     const int32_t *seq_lens;
-    int L, L_cap, W, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;
+    CacheMap map;           // contiguous or paged cache
+    int L, W, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;
     uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
     uint32_t uv_off;        // epilogue: offset of the channel sums in the stage region (after the warp sums)
     uint32_t part_off;      // epilogue: offset of this split's partial in shared memory (single split)
@@ -268,7 +269,7 @@ struct FastArgs {
 // Each tile's P.V starts from zero and is added to the running sums in
 // fp32, so the tensor-core accumulation (which does not round to nearest)
 // never carries more than one tile.
-template <int GMAX, int NT, int FW, typename QT>
+template <int GMAX, int NT, int FW, typename QT, bool PAGED>
 __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
@@ -297,7 +298,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     const int u = blockIdx.x / a.S, sp = blockIdx.x % a.S;
     const int b = u / (a.Hkv * a.HG), h = (u / a.HG) % a.Hkv, hg = u % a.HG;
     const int ta = sp * a.tiles_per, tb = min(ta + a.tiles_per, a.n_tiles);
-    const size_t slab = ((size_t)b * a.Hkv + h) * (size_t)a.L_cap * W;
+    constexpr bool paged = PAGED;
+    const size_t slab = paged ? 0 : ((size_t)b * a.Hkv + h) * (size_t)a.map.L_cap * W;
     uint64_t *my_mbar = mbar + warp * FST;
     uint64_t *blob_bar = mbar + FW * FST;
     uint64_t *mat_bar = blob_bar + 1;   // phase 0: A_k^T, phase 1: Uv^T
@@ -325,6 +327,34 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // the handle; the query, the row lengths, the cache and the workspace may
     // be written by the kernel before this one on the stream.
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // paged cache: lane 0 reads the block table entries of the warp's first
+    // FST tiles (ent) and of its next three refills (r0, r1, r2), ahead of the
+    // tile burst; each refill then reads the entry three refills ahead, since a
+    // load issued behind the burst waits for the copies queued before it
+    // (tiles below tb are inside the table)
+    const int sh = a.map.tpb_shift;
+    int ent[3] = {0, 0, 0}, r0 = 0, r1 = 0, r2 = 0;
+    bool bad_blk = false;
+    const int32_t *trow = paged ? a.map.table + (size_t)b * a.map.bpr : nullptr;
+    if (paged && lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int tile = ta + warp + i * FW;
+            if (i < FST && tile < tb) ent[i] = trow[tile >> sh];
+        }
+        const int tr = ta + warp + FST * FW;
+        if (tr < tb) r0 = trow[tr >> sh];
+        if (tr + FW < tb) r1 = trow[(tr + FW) >> sh];
+        if (tr + 2 * FW < tb) r2 = trow[(tr + 2 * FW) >> sh];
+    }
+    // word offset of a tile of this (row, KV head) in the pool (block 0 for a bad entry)
+    auto pool_word = [&](int blk, int tile) -> size_t {
+        if (blk < 0 || blk >= a.map.n_blocks) {
+            bad_blk = true;
+            blk = 0;
+        }
+        return ((((size_t)blk * a.Hkv + h) << sh) + (size_t)(tile & ((1 << sh) - 1))) * TILE * W;
+    };
     // query rows of the head group: element e = (head e / D, k = e % D)
     constexpr int QPER = (HPG * D + NTH - 1) / NTH;
     float qv[QPER];
@@ -339,27 +369,41 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     }
     const int len = a.seq_lens ? min(max(a.seq_lens[b], 0), a.L) : a.L;
 
-    auto issue = [&](int tile, int s) {
+    auto issue = [&](size_t word, int s) {
         unsigned char *dst = my_stage + s * SB;
         mbar_arrive_expect(&my_mbar[s], 2 * tile_bytes);
-        bulk_g2s(dst, a.kp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
-        bulk_g2s(dst + tile_bytes, a.vp + slab + (size_t)tile * TILE * W, tile_bytes, &my_mbar[s]);
+        bulk_g2s(dst, a.kp + word, tile_bytes, &my_mbar[s]);
+        bulk_g2s(dst + tile_bytes, a.vp + word, tile_bytes, &my_mbar[s]);
     };
     // The warp's n-th tile goes through stage n % FST and completes phase
-    // n / FST of that stage's barrier.  The first tiles are requested up to
-    // tb, before the row length has arrived (tiles below tb are inside the
-    // cache); copies past the row's length are drained at the end.
+    // n / FST of that stage's barrier.  In a contiguous cache the first tiles
+    // are requested up to tb, before the row length has arrived (tiles below
+    // tb are inside the cache); copies past the row's length are drained at
+    // the end.  In a paged cache only tiles inside the row are requested.
     int n_issued = 0, n_done = 0;
     int st_next = 0;          // stage of the next tile to consume
     uint32_t ph_next = 0;     // its barrier phase parity
-    for (int i = 0; i < FST; ++i) {
-        const int tile = ta + warp + i * FW;
-        if (tile < tb) {
-            if (lane == 0) issue(tile, i);
-            ++n_issued;
+    if (!paged) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {   // FST <= 3
+            const int tile = ta + warp + i * FW;
+            if (i < FST && tile < tb) {
+                if (lane == 0) issue(slab + (size_t)tile * TILE * W, i);
+                ++n_issued;
+            }
         }
     }
     const int t1 = min(tb, (len + TILE - 1) / TILE);
+    if (paged) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const int tile = ta + warp + i * FW;
+            if (i < FST && tile < t1) {
+                if (lane == 0) issue(pool_word(ent[i], tile), i);
+                ++n_issued;
+            }
+        }
+    }
 
     // ---- query weights of the head group: q' = (A_k q) o Delta_K / sqrt(d),
     // scaled per head by a power of two S_i, split into fp16 hi/lo parts and
@@ -635,7 +679,15 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         if (nt < t1) {
             if (lane == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(nt, s);
+                if (paged) {
+                    issue(pool_word(r0, nt), s);
+                    r0 = r1;
+                    r1 = r2;
+                    const int nn = nt + 3 * FW;   // three refills ahead
+                    r2 = nn < t1 ? trow[nn >> sh] : 0;
+                } else {
+                    issue(slab + (size_t)nt * TILE * W, s);
+                }
             }
             ++n_issued;
         }
@@ -643,6 +695,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // copies still in flight (requested past the row's length, or left by a
     // failed wait) land before the shared memory is reused
     if (failed && lane == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
+    if (bad_blk) atomicOr(a.status, AATC_DEV_RANGE);
     for (; n_done < n_issued; ++n_done) {
         if (!mbar_wait(&my_mbar[st_next], ph_next)) failed = true;
         if (++st_next == FST) {
@@ -943,7 +996,7 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
 template <int GMAX, int NT, int FW>
 int occupancy_of(size_t smem)
 {
-    auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16>;
+    auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return 1;
     int n = 0;
@@ -1052,9 +1105,9 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *rec, int off, int b)
 // m (running max of scores), l (sum of exp), acc[j] = sum_i p_i u^V_ij.
 __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
     const float *__restrict__ qp, const uint32_t *__restrict__ kp, const uint32_t *__restrict__ vp,
-    int L_cap, const int32_t *__restrict__ seq_lens, int L, int Hkv, int G, int W, int chunk,
+    CacheMap map, const int32_t *__restrict__ seq_lens, int L, int Hkv, int G, int W, int chunk,
     int n_split, const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs,
-    float *__restrict__ part)
+    float *__restrict__ part, uint32_t *status)
 {
     __shared__ float q_s[AATC_MAX_G][D];
     __shared__ float p_s[DEC_TILE][AATC_MAX_G + 1];
@@ -1088,7 +1141,7 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
 #pragma unroll
     for (int gg = 0; gg < AATC_MAX_G; ++gg) { acc[gg] = 0.f; lsum[gg] = 0.f; }
 
-    const size_t base = ((size_t)b * Hkv + h) * (size_t)L_cap * W;
+    bool bad_blk = false;
     for (int tok0 = begin; tok0 < end; tok0 += DEC_TILE) {
         const int tok = tok0 + t;
         const bool valid = tok < end;
@@ -1097,7 +1150,12 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
 #pragma unroll
         for (int gg = 0; gg < AATC_MAX_G; ++gg) sc[gg] = -INFINITY;
         if (valid) {
-            const uint32_t *tile = kp + base + (size_t)(tok >> 5) * 32 * W;
+            long long tw = cache_tile_word(map, b, h, Hkv, W, tok >> 5);
+            if (tw < 0) {   // no block for this tile: read tile 0 of the pool, report it
+                bad_blk = true;
+                tw = 0;
+            }
+            const uint32_t *tile = kp + tw;
             for (int w = 0; w < W; ++w) rec[w] = tile[key_word_pos(tok & 31, w, W)];
             rec[W] = 0u;
 #pragma unroll
@@ -1109,7 +1167,7 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
                 for (int gg = 0; gg < AATC_MAX_G; ++gg)
                     if (gg < G) sc[gg] = fmaf(q_s[gg][j], u, sc[gg]);
             }
-            const uint32_t *vt = vp + base + (size_t)(tok >> 5) * 32 * W;
+            const uint32_t *vt = vp + tw;
             for (int w = 0; w < W; ++w) {
                 const uint32_t lo = (vt[16 * (2 * w) + ((tok & 31) >> 1)] >> (16 * (tok & 1))) & 0xFFFFu;
                 const uint32_t hi = (vt[16 * (2 * w + 1) + ((tok & 31) >> 1)] >> (16 * (tok & 1))) & 0xFFFFu;
@@ -1156,6 +1214,7 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
         P[2 + t] = acc[gg];
         if (t == 0) { P[0] = m_s[gg]; P[1] = lsum[gg]; }
     }
+    if (bad_blk) atomicOr(status, AATC_DEV_RANGE);
 }
 
 // One block per (batch row, query head): LSE-merge the splits (natural-log
@@ -1243,8 +1302,12 @@ aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a,
 template <int GMAX, int NT, int FW>
 aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s)
 {
-    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16>, FW, f, a, s);
-    return launch_variant(k_decode_fast<GMAX, NT, FW, float>, FW, f, a, s);
+    if (a.map.table) {
+        if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16, true>, FW, f, a, s);
+        return launch_variant(k_decode_fast<GMAX, NT, FW, float, true>, FW, f, a, s);
+    }
+    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16, false>, FW, f, a, s);
+    return launch_variant(k_decode_fast<GMAX, NT, FW, float, false>, FW, f, a, s);
 }
 
 aatc_status launch_combine(const FastGeom &f, const aatc_calib *h, const float *part, float *out, cudaStream_t s)
@@ -1283,7 +1346,7 @@ size_t decode_ws_bytes(const aatc_calib *h, int B, int L)
 }
 
 aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, const uint32_t *vp,
-                       int L_cap, const int32_t *seq_lens, int L, int B, float *out, void *ws,
+                       const CacheMap &map, const int32_t *seq_lens, int L, int B, float *out, void *ws,
                        size_t ws_bytes, cudaStream_t s)
 {
     if (B == 0) return AATC_OK;
@@ -1302,7 +1365,7 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.vp = vp;
         a.seq_lens = seq_lens;
         a.L = L;
-        a.L_cap = L_cap;
+        a.map = map;
         a.W = h->W;
         a.rows = f.rows;
         a.groups = f.groups;
@@ -1351,7 +1414,7 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
     else
         k_query_prep<float><<<dim3(B, h->Hq), D, 0, s>>>((const float *)q, h->Hq, h->G, h->AkT32, h->tab, qp);
     k_decode_split_general<<<dim3(p.n_split, h->Hkv, B), DEC_TILE, 0, s>>>(
-        qp, kp, vp, L_cap, seq_lens, L, h->Hkv, h->G, h->W, p.chunk, p.n_split, h->plan, h->tab, part);
+        qp, kp, vp, map, seq_lens, L, h->Hkv, h->G, h->W, p.chunk, p.n_split, h->plan, h->tab, part, h->status);
     k_decode_combine<<<dim3(B, h->Hq), D, 0, s>>>(part, p.n_split, h->Hq, h->G, h->tab, h->UvT32,
                                                   h->muv32, out);
     AATC_CUDA(cudaGetLastError());

@@ -40,10 +40,10 @@ __device__ __forceinline__ int key_word_pos(int i, int w, int W)
 
 template <typename T>
 __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
-    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, int L_cap, int Hkv,
-    int W, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
-    const float *__restrict__ bv, const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
-    uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
+    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, const int32_t *row_start,
+    CacheMap map, int Hkv, int W, const float *__restrict__ Tk, const float *__restrict__ Tv,
+    const float *__restrict__ bk, const float *__restrict__ bv, const CodecTables *__restrict__ tabs,
+    const HeadPlan *__restrict__ plans, uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
 {
     extern __shared__ float sm[];
     float *Ts = sm;                          // [D][D] transposed: Ts[kk][j] = T[j][kk]
@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     const float *bias = (tensor == 0 ? bk : bv) + h * D;
     const CodecTables &tb = tabs[h * 2 + tensor];
     offs[t] = plans[h * 2 + tensor].off[t];
-    uint32_t *out = (tensor == 0 ? kp : vp) + ((size_t)b * Hkv + h) * L_cap * W;
+    uint32_t *out = tensor == 0 ? kp : vp;
 
     for (int e = t; e < D * D; e += ENC_TILE) {
         int j = e / D, kk = e % D;
@@ -110,22 +110,28 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
         }
     }
     __syncthreads();
-    // scatter the records into the tiled cache (positions start_pos + tok0 + i)
-    const int p0 = start_pos + tok0;
+    // scatter the records into the tiled cache (positions row start + tok0 + i)
+    const int p0 = (row_start ? row_start[b] : start_pos) + tok0;
+    bool range = false;
     if (tensor == 0) {
         for (int e = t; e < ntok * W; e += ENC_TILE) {
             const int i = e / W, w = e % W, pos = p0 + i;
-            out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, w, W)] = rec[i * (W + 1) + w];
+            const long long tw = cache_tile_word(map, b, h, Hkv, W, pos >> 5);
+            if (tw < 0) { range = true; continue; }
+            out[tw + key_word_pos(pos & 31, w, W)] = rec[i * (W + 1) + w];
         }
     } else {
         uint16_t *out16 = (uint16_t *)out;
         for (int e = t; e < ntok * 2 * W; e += ENC_TILE) {
             const int i = e / (2 * W), q = e % (2 * W), pos = p0 + i;
+            const long long tw = cache_tile_word(map, b, h, Hkv, W, pos >> 5);
+            if (tw < 0) { range = true; continue; }
             const uint32_t wv = rec[i * (W + 1) + (q >> 1)];
-            const size_t word = (size_t)(pos >> 5) * 32 * W + 16 * q + ((pos & 31) >> 1);
+            const long long word = tw + 16 * q + ((pos & 31) >> 1);
             out16[2 * word + (pos & 1)] = (uint16_t)(wv >> (16 * (q & 1)));
         }
     }
+    if (range) atomicOr(status, AATC_DEV_RANGE);
 }
 
 // Append path: a few new tokens per row, as in a decode step.  One CTA of
@@ -149,8 +155,8 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src)
 
 template <typename T>
 __global__ void __launch_bounds__(D) k_encode_append(
-    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, int L_cap, int Hkv, int W,
-    const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
+    const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, const int32_t *row_start,
+    CacheMap map, int Hkv, int W, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
     const float *__restrict__ bv, const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
     uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
 {
@@ -177,8 +183,9 @@ __global__ void __launch_bounds__(D) k_encode_append(
     // the new tokens and the cache may belong to the previous kernel on the stream
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const T *x = (tensor == 0 ? k : v) + ((size_t)b * Hkv + h) * L_new * D;
-    uint32_t *out = (tensor == 0 ? kp : vp) + ((size_t)b * Hkv + h) * L_cap * W;
-    bool bad = false;
+    uint32_t *out = tensor == 0 ? kp : vp;
+    const int pos0 = row_start ? row_start[b] : start_pos;
+    bool bad = false, range = false;
     for (int n = 0; n < L_new; ++n) {
         const float xv = to_f32(x[(size_t)n * D + j]);
         bad |= !isfinite(xv);
@@ -204,21 +211,27 @@ __global__ void __launch_bounds__(D) k_encode_append(
             if (sh + bits > 32) atomicOr(&rec[(off >> 5) + 1], u >> (32 - sh));
         }
         __syncthreads();
-        const int pos = start_pos + n;
-        if (tensor == 0) {
-            if (j < W) out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, j, W)] = rec[j];
-        } else if (j < 2 * W) {
-            const size_t word = (size_t)(pos >> 5) * 32 * W + 16 * j + ((pos & 31) >> 1);
-            reinterpret_cast<uint16_t *>(out)[2 * word + (pos & 1)] = (uint16_t)(rec[j >> 1] >> (16 * (j & 1)));
+        const int pos = pos0 + n;
+        if (j < (tensor == 0 ? W : 2 * W)) {
+            const long long tw = cache_tile_word(map, b, h, Hkv, W, pos >> 5);
+            if (tw < 0) {
+                range = true;
+            } else if (tensor == 0) {
+                out[tw + key_word_pos(pos & 31, j, W)] = rec[j];
+            } else {
+                const long long word = tw + 16 * j + ((pos & 31) >> 1);
+                reinterpret_cast<uint16_t *>(out)[2 * word + (pos & 1)] = (uint16_t)(rec[j >> 1] >> (16 * (j & 1)));
+            }
         }
         __syncthreads();   // xs and rec are reused by the next token
     }
     if (__syncthreads_or(bad) && j == 0) atomicOr(status, AATC_DEV_NONFINITE);
+    if (range) atomicOr(status, AATC_DEV_RANGE);
 }
 
 template <typename T>
 aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int B, int L_new, int start_pos,
-                          int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+                          const int32_t *row_start, const CacheMap &map, uint32_t *kp, uint32_t *vp, cudaStream_t s)
 {
     static const size_t smem = (size_t)D * TPAD * sizeof(float);
     auto kern = k_encode_append<T>;
@@ -233,7 +246,7 @@ aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, (const T *)k, (const T *)v, L_new, start_pos, L_cap, h->Hkv, h->W,
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, (const T *)k, (const T *)v, L_new, start_pos, row_start, map, h->Hkv, h->W,
                                  (const float *)h->Tk32, (const float *)h->Tv32, (const float *)h->bk32,
                                  (const float *)h->bv32, (const CodecTables *)h->tab, (const HeadPlan *)h->plan,
                                  kp, vp, h->status));
@@ -242,16 +255,17 @@ aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int
 
 }  // namespace
 
-aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
-                       int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new, int start_pos,
+                       const int32_t *row_start, const CacheMap &map, uint32_t *kp, uint32_t *vp, cudaStream_t s)
 {
     if (L_new == 0 || B == 0) return AATC_OK;
     if (L_new <= APPEND_MAX && B <= 65535) {   // a decode step's new tokens
-        if (h->dtype == AATC_BF16) return launch_append<__nv_bfloat16>(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
-        return launch_append<float>(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
+        if (h->dtype == AATC_BF16)
+            return launch_append<__nv_bfloat16>(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
+        return launch_append<float>(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
     }
     if (h->dtype == AATC_BF16 && h->tmap_ok && h->W <= 16)
-        return encode_tc_run(h, k, v, B, L_new, start_pos, L_cap, kp, vp, s);
+        return encode_tc_run(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
     const size_t smem = (size_t)D * D * 4 + (size_t)ENC_TILE * (D + 1) * 4 +
                         (size_t)ENC_TILE * (h->W + 1) * 4;
     const dim3 grid((L_new + ENC_TILE - 1) / ENC_TILE, h->Hkv, 2 * B);
@@ -259,12 +273,12 @@ aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B,
         auto kern = k_encode_simple<__nv_bfloat16>;
         AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         kern<<<grid, ENC_TILE, smem, s>>>((const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, L_new,
-                                          start_pos, L_cap, h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32,
+                                          start_pos, row_start, map, h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32,
                                           h->bv32, h->tab, h->plan, kp, vp, h->status);
     } else {
         auto kern = k_encode_simple<float>;
         AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        kern<<<grid, ENC_TILE, smem, s>>>((const float *)k, (const float *)v, L_new, start_pos, L_cap,
+        kern<<<grid, ENC_TILE, smem, s>>>((const float *)k, (const float *)v, L_new, start_pos, row_start, map,
                                           h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, h->plan,
                                           kp, vp, h->status);
     }

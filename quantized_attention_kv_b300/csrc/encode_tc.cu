@@ -48,7 +48,9 @@ __device__ __forceinline__ int key_word_pos(int i, int w, int W)
 }
 
 struct EncArgs {
-    int B, H, L_new, start_pos, L_cap, W, nblk, n_items;
+    int B, H, L_new, start_pos, W, nblk, n_items;
+    const int32_t *row_start;   // [B] first position of each row, or NULL: start_pos
+    CacheMap map;               // contiguous or paged cache
     const EncCol *cols;     // [H][2][D]
     uint32_t *kp, *vp;
     uint32_t *status;
@@ -251,16 +253,28 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             if (!(fabsf(fin) <= 3.4e38f) && tok < a.L_new) atomicOr(a.status, AATC_DEV_NONFINITE);
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // staging -> bulk store
             asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
-            // ---- store the block's records
-            uint32_t *out = (t ? a.vp : a.kp) + ((size_t)b * a.H + h) * (size_t)a.L_cap * W;
-            const int p0 = a.start_pos + blk * EB;
+            // ---- store the block's records: a full block starting on a tile
+            // boundary leaves by bulk stores (one for its 4 tiles when they are
+            // contiguous, else one per tile), anything else token by token
+            uint32_t *out = t ? a.vp : a.kp;
+            const int p0 = (a.row_start ? a.row_start[b] : a.start_pos) + blk * EB;
             const int ntok = min(EB, a.L_new - blk * EB);
-            if (ntok == EB && (p0 & 31) == 0) {
-                if (gt == 0) {
-                    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                                     out + (size_t)p0 * W),
-                                 "r"(smem_u32(R)), "r"((uint32_t)(EB * W * 4))
-                                 : "memory");
+            bool range = false;
+            if (ntok == EB && (p0 & 31) == 0 && p0 >= 0) {
+                if (gt < EB / 32) {   // thread gt: tile gt of the block
+                    const long long tw = cache_tile_word(a.map, b, h, a.H, W, (p0 >> 5) + gt);
+                    if (tw < 0) {
+                        range = true;
+                    } else if (!a.map.table) {
+                        if (gt == 0)
+                            asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out + tw),
+                                         "r"(smem_u32(R)), "r"((uint32_t)(EB * W * 4))
+                                         : "memory");
+                    } else {
+                        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(out + tw),
+                                     "r"(smem_u32(R + gt * 32 * W)), "r"((uint32_t)(32 * W * 4))
+                                     : "memory");
+                    }
                     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
                     // the group writes this staging buffer again with its next item
                     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
@@ -269,8 +283,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 // partial block: per-token words (keys)
                 for (int e = gt; e < ntok * W; e += 128) {
                     const int ti = e / W, ww = e % W, pos = p0 + ti;
-                    const uint32_t word = R[(ti >> 5) * 32 * W + key_word_pos(ti & 31, ww, W)];
-                    out[(size_t)(pos >> 5) * 32 * W + key_word_pos(pos & 31, ww, W)] = word;
+                    const long long tw = cache_tile_word(a.map, b, h, a.H, W, pos >> 5);
+                    if (tw < 0) { range = true; continue; }
+                    out[tw + key_word_pos(pos & 31, ww, W)] = R[(ti >> 5) * 32 * W + key_word_pos(ti & 31, ww, W)];
                 }
             } else {
                 // partial block: per-token half-words (values)
@@ -278,13 +293,16 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 uint16_t *o16 = reinterpret_cast<uint16_t *>(out);
                 for (int e = gt; e < ntok * 2 * W; e += 128) {
                     const int ti = e / (2 * W), q = e % (2 * W), pos = p0 + ti;
+                    const long long tw = cache_tile_word(a.map, b, h, a.H, W, pos >> 5);
+                    if (tw < 0) { range = true; continue; }
                     const uint16_t hw = R16[2 * ((ti >> 5) * 32 * W + 16 * q + ((ti & 31) >> 1)) + (ti & 1)];
-                    o16[2 * ((size_t)(pos >> 5) * 32 * W + 16 * q + ((pos & 31) >> 1)) + (pos & 1)] = hw;
+                    o16[2 * (tw + 16 * q + ((pos & 31) >> 1)) + (pos & 1)] = hw;
                 }
             }
+            if (range) atomicOr(a.status, AATC_DEV_RANGE);
             asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
         }
-        if (gt == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        if (gt < EB / 32) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;");
     __syncthreads();
@@ -403,7 +421,7 @@ aatc_status enc_build(aatc_calib *h, cudaStream_t s)
 }
 
 aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new, int start_pos,
-                          int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s)
+                          const int32_t *row_start, const CacheMap &map, uint32_t *kp, uint32_t *vp, cudaStream_t s)
 {
     const unsigned long long rows = (unsigned long long)B * h->Hkv * L_new;
     CUtensorMap mk, mv, mt;
@@ -415,7 +433,8 @@ aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int
     a.H = h->Hkv;
     a.L_new = L_new;
     a.start_pos = start_pos;
-    a.L_cap = L_cap;
+    a.row_start = row_start;
+    a.map = map;
     a.W = h->W;
     a.nblk = (L_new + EB - 1) / EB;
     a.n_items = h->Hkv * 2 * B * a.nblk;

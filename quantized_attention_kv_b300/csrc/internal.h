@@ -16,7 +16,38 @@ enum : uint32_t {
     AATC_DEV_NONFINITE = 1u,
     AATC_DEV_NO_CONVERGENCE = 2u,
     AATC_DEV_TIMEOUT = 4u,        // a bounded wait inside a kernel gave up
+    AATC_DEV_RANGE = 8u,          // a cache position or block table entry out of range (access skipped)
 };
+
+// Where the 32-token tiles of the cache of one (batch row b, KV head h) live.
+// Contiguous cache: (b, h) starts at word (b*H + h)*L_cap*W.  Paged cache:
+// logical block n (tiles n*tpb .. n*tpb + tpb - 1, tpb a power of two) of
+// row b is physical block table[b*bpr + n] of the pool, and head h of block p
+// starts at word (p*H + h)*tpb*32*W.  Either way a tile is 32*W consecutive
+// words.
+struct CacheMap {
+    const int32_t *table;   // device [B][bpr], or NULL for a contiguous cache
+    int bpr;                // blocks per table row (paged)
+    int tpb_shift;          // tiles per block = 2^tpb_shift (paged)
+    int n_blocks;           // blocks in the pool (paged)
+    int L_cap;              // tokens per (row, head) (contiguous)
+};
+
+inline CacheMap contiguous_map(int L_cap) { return CacheMap{nullptr, 0, 0, 0, L_cap}; }
+
+// Word offset of tile t of (row b, head h) in a cache of H heads and W-word
+// records, or -1 when t is outside the cache or the block table names no
+// block of the pool for it.
+__device__ __forceinline__ long long cache_tile_word(const CacheMap &m, int b, int h, int H, int W, int t)
+{
+    if (t < 0) return -1;
+    if (!m.table) return (long long)t * 32 < m.L_cap ? ((long long)(b * H + h) * m.L_cap + (long long)t * 32) * W : -1;
+    const int n = t >> m.tpb_shift;
+    if (n >= m.bpr) return -1;
+    const int p = m.table[(size_t)b * m.bpr + n];
+    if (p < 0 || p >= m.n_blocks) return -1;
+    return ((((long long)p * H + h) << m.tpb_shift) + (t & ((1 << m.tpb_shift) - 1))) * 32LL * W;
+}
 
 // Per (KV head, tensor) codec tables, fp32/int, derived from bits and steps.
 // One struct per (head, tensor); tensor 0 = K, 1 = V.
@@ -146,13 +177,17 @@ bool tma_map_bf16(void *map128, const void *base, unsigned long long inner, unsi
 aatc_status dec_build(aatc_calib *h, cudaStream_t s);
 
 // ---- encode (encode.cu, encode_tc.cu) ----
+// Token n of row b goes to position (row_start ? row_start[b] : start_pos) + n
+// of the cache `map` describes (row_start: device [B], read on the device).
 aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
-                          int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s);
+                          int start_pos, const int32_t *row_start, const CacheMap &map, uint32_t *kp,
+                          uint32_t *vp, cudaStream_t s);
 aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B, int L_new,
-                       int start_pos, int L_cap, uint32_t *kp, uint32_t *vp, cudaStream_t s);
+                       int start_pos, const int32_t *row_start, const CacheMap &map, uint32_t *kp,
+                       uint32_t *vp, cudaStream_t s);
 
 // ---- decode (decode.cu) ----
 size_t decode_ws_bytes(const aatc_calib *h, int B, int L);
 aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, const uint32_t *vp,
-                       int L_cap, const int32_t *seq_lens, int L, int B, float *out, void *ws,
+                       const CacheMap &map, const int32_t *seq_lens, int L, int B, float *out, void *ws,
                        size_t ws_bytes, cudaStream_t s);

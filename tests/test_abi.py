@@ -55,6 +55,11 @@ def test_null_and_bad_arguments_rejected_on_host(L):
     assert L.aatc_encode(None, None, None, 1, 1, 0, 1, None, None, None) == aatc.ERR_INVALID_ARG
     assert L.aatc_decode_attention(None, None, None, None, 1, None, 1, 1, None, None, 0, None) == aatc.ERR_INVALID_ARG
     assert L.aatc_decode_workspace_size(None, 1, 1) == 0
+    pg = aatc.Pages(None, 1, 32, 1)
+    assert L.aatc_encode_paged(None, None, None, 1, 1, 0, None, None, None, ctypes.byref(pg), None) == \
+        aatc.ERR_INVALID_ARG
+    assert L.aatc_decode_attention_paged(None, None, None, None, ctypes.byref(pg), None, 1, 1, None, None, 0,
+                                         None) == aatc.ERR_INVALID_ARG
     assert L.aatc_record_words(None) == -1
     L.aatc_free(None)
     assert L.aatc_check(None) == aatc.ERR_INVALID_ARG
