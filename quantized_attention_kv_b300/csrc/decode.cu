@@ -126,7 +126,7 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.rows = (h->W + 3) / 4;
     f.groups = (2 * h->W + 7) / 8;
     f.GMAX = f.groups <= 2 ? 2 : (f.groups <= 3 ? 3 : 4);
-    f.FW = f.NT == 2 ? 8 : (f.GMAX <= 3 ? 16 : 12);
+    f.FW = f.NT == 2 ? 12 : 16;
     f.ksteps = 4 * f.rows;
     f.FST = 3;
     FastSmem m = fast_smem_layout(f.FW, f.FST, h->W, f.NT, f.ksteps, f.groups);
@@ -1009,11 +1009,11 @@ int fast_ctas_per_sm_uncached(int GMAX, int NT, size_t smem)
     if (NT == 1) {
         if (GMAX == 2) return occupancy_of<2, 1, 16>(smem);
         if (GMAX == 3) return occupancy_of<3, 1, 16>(smem);
-        return occupancy_of<4, 1, 12>(smem);
+        return occupancy_of<4, 1, 16>(smem);
     }
-    if (GMAX == 2) return occupancy_of<2, 2, 8>(smem);
-    if (GMAX == 3) return occupancy_of<3, 2, 8>(smem);
-    return occupancy_of<4, 2, 8>(smem);
+    if (GMAX == 2) return occupancy_of<2, 2, 12>(smem);
+    if (GMAX == 3) return occupancy_of<3, 2, 12>(smem);
+    return occupancy_of<4, 2, 12>(smem);
 }
 
 int fast_ctas_per_sm(int GMAX, int NT, int FW, size_t smem)
@@ -1393,11 +1393,11 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         if (f.NT == 1) {
             if (f.GMAX == 2) st = launch_fast<2, 1, 16>(f, a, h->dtype, s);
             else if (f.GMAX == 3) st = launch_fast<3, 1, 16>(f, a, h->dtype, s);
-            else st = launch_fast<4, 1, 12>(f, a, h->dtype, s);
+            else st = launch_fast<4, 1, 16>(f, a, h->dtype, s);
         } else {
-            if (f.GMAX == 2) st = launch_fast<2, 2, 8>(f, a, h->dtype, s);
-            else if (f.GMAX == 3) st = launch_fast<3, 2, 8>(f, a, h->dtype, s);
-            else st = launch_fast<4, 2, 8>(f, a, h->dtype, s);
+            if (f.GMAX == 2) st = launch_fast<2, 2, 12>(f, a, h->dtype, s);
+            else if (f.GMAX == 3) st = launch_fast<3, 2, 12>(f, a, h->dtype, s);
+            else st = launch_fast<4, 2, 12>(f, a, h->dtype, s);
         }
         if (st != AATC_OK) return st;
         if (f.single) return AATC_OK;   // single splits finished in the split kernel
