@@ -260,9 +260,8 @@ def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_pa
     _check_cache(calib, B, k_packed, v_packed)
     if out is None:
         out = torch.empty(B, calib.n_q_heads, D, dtype=torch.float32, device=q.device)
-    need = workspace_size(calib, B, L)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if workspace is None:   # (a given workspace is checked against the need by the library)
+        workspace = torch.empty(max(workspace_size(calib, B, L), 16), dtype=torch.uint8, device=q.device)
     _check(lib().aatc_decode_attention(calib.handle, _ptr(q), _ptr(k_packed), _ptr(v_packed), k_packed.shape[2],
                                        _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
