@@ -343,10 +343,12 @@ def _synthetic_calibration(G, bits_k, bits_v, seed=0):
     return cal
 
 
-@pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "bits2", "bits4"])
+@pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "bits2", "bits4", "bits8"])
 def test_decode_paths_match_oracle(case):
     """Fast path (GQA groups of 1..8, 2.0..4.0 bits) and the general path
-    (records above 16 words, bytes holding more than four code pieces)."""
+    (records above 16 words up to the 32-word maximum, bytes holding more than
+    four code pieces); each also through a paged pool on shuffled 32-token
+    blocks, which must give the contiguous output exactly."""
     lam = 0.95 ** np.arange(128)
     G, B_bits = 4, 352
     if case == "G1":
@@ -359,6 +361,8 @@ def test_decode_paths_match_oracle(case):
         B_bits = 256
     elif case == "bits4":
         B_bits = 512
+    elif case == "bits8":
+        B_bits = 1024
     bk, _ = oracle.allocate_bits(lam, B_bits)
     bv, _ = oracle.allocate_bits(0.93 ** np.arange(128), B_bits)
     if case == "many_pieces":
@@ -377,10 +381,22 @@ def test_decode_paths_match_oracle(case):
     q = torch.from_numpy(rng.standard_normal((Bsz, G, 128)).astype(np.float32) * 3).cuda()
     g = aatc.import_calib(cal, G, torch.float32)
     L_cap = aatc.cache_capacity(L)
-    out = aatc.decode_attention(g, q, _upload(kp, oracle.KEYS, L_cap), _upload(vp, oracle.VALUES, L_cap), L)
+    kc, vc = _upload(kp, oracle.KEYS, L_cap), _upload(vp, oracle.VALUES, L_cap)
+    out = aatc.decode_attention(g, q, kc, vc, L)
     ref = oracle.decode_attention(to_np64(q), kp, vp, cal)
     err = attn_rel_err(out.cpu().numpy(), ref)
     assert err <= ATTN_RTOL, (case, err)
+    # the same caches on shuffled 32-token blocks of a pool
+    bpr = L_cap // 32
+    perm = torch.randperm(Bsz * bpr + 5, generator=torch.Generator().manual_seed(3))
+    table = perm[:Bsz * bpr].reshape(Bsz, bpr).to(torch.int32).cuda()
+    pools = []
+    for c in (kc, vc):
+        pool = aatc.alloc_pool(g, Bsz * bpr + 5, 32)
+        pool[table.long()] = c.reshape(Bsz, 1, bpr, 32, W).permute(0, 2, 1, 3, 4)
+        pools.append(pool)
+    out_p = aatc.decode_attention_paged(g, q, pools[0], pools[1], table, L)
+    assert torch.equal(out_p, out), case
     g.check()
 
 
