@@ -131,8 +131,13 @@ __global__ void k_moment_reduce(const double *__restrict__ partial, int nchunks,
 constexpr int JAC_THREADS = 512;
 constexpr int TRI = D * (D + 1) / 2;
 constexpr int JAC_BLOCKS = 64 * 65 / 2;   // 2x2 blocks (pair k1 <= pair k2) of one round
-constexpr size_t JAC_SMEM = (size_t)(TRI + D * D) * sizeof(double) + 64 * 2 * sizeof(double) +
-                            64 * 2 * sizeof(int) + 4 * sizeof(int) + (size_t)JAC_BLOCKS * 2 * sizeof(uint16_t);
+constexpr int PRE_SWEEPS = 10;            // cap of the fp32 preconditioning sweeps
+template <typename R>
+constexpr size_t jac_smem()
+{
+    return (size_t)(TRI + D * D) * sizeof(R) + 64 * 2 * sizeof(R) + 64 * 2 * sizeof(int) + 4 * sizeof(int) +
+           (size_t)JAC_BLOCKS * 2 * sizeof(uint16_t);
+}
 
 __device__ __forceinline__ int tri(int i, int j)
 {
@@ -140,27 +145,43 @@ __device__ __forceinline__ int tri(int i, int j)
     return i * D - (i * (i - 1)) / 2 + (j - i);
 }
 
+// Mixed precision: FP64 runs at a small fraction of the FP32 rate on this GPU,
+// so the sweeps are split in two.  PRE (R = float) runs fp32 sweeps from the
+// identity until the off-diagonal reaches fp32 rounding (a pair is skipped when
+// |a_pq| <= 1e-6 sqrt(|a_pp a_qq|) or below 2^-23 of the largest diagonal
+// entry) and writes the accumulated rotations V as fp64.  The host makes V
+// orthogonal to fp64 precision (Newton-Schulz) and forms A' = V^T A V in fp64.
+// The final pass (R = double) then runs the sweeps above on A', starting its
+// accumulation from that V, so its output is the decomposition of A; it
+// needs a few sweeps (quadratic convergence from the fp32 level) instead of
+// about twelve.
+//
 // Two independent batches in one launch: blocks m < M0 take (Ain0, evals0,
-// evecs0)[m], the others (Ain1, evals1, evecs1)[m - M0].
+// evecs0, V00)[m], the others (Ain1, evals1, evecs1, V01)[m - M0].  V0 NULL:
+// start from the identity.  PRE writes only evecs (the raw rotations).
+template <typename R, bool PRE>
 __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict__ Ain0, double *__restrict__ evals0,
-                                                        double *__restrict__ evecs0, int M0,
-                                                        const double *__restrict__ Ain1, double *__restrict__ evals1,
-                                                        double *__restrict__ evecs1, int max_sweeps,
+                                                        double *__restrict__ evecs0, const double *__restrict__ V00,
+                                                        int M0, const double *__restrict__ Ain1,
+                                                        double *__restrict__ evals1, double *__restrict__ evecs1,
+                                                        const double *__restrict__ V01, int max_sweeps,
                                                         uint32_t *status)
 {
-    extern __shared__ double smem[];
-    double *A = smem;                      // packed upper triangle
-    double *V = A + TRI;                   // [D][D]
-    double *cs = V + D * D;                // [64][2]
+    extern __shared__ __align__(16) unsigned char jsm[];
+    R *A = reinterpret_cast<R *>(jsm);     // packed upper triangle
+    R *V = A + TRI;                        // [D][D]
+    R *cs = V + D * D;                     // [64][2]
     int *pq = (int *)(cs + 128);           // [64][2]
     int *flag = pq + 128;                  // [0] rotated, [1] nonfinite
     uint16_t *kpair = reinterpret_cast<uint16_t *>(flag + 4);   // [JAC_BLOCKS][2]: block -> (k1, k2)
+    __shared__ R floor_s;
     const int tid = threadIdx.x;
     const bool second = (int)blockIdx.x >= M0;
     const int m = second ? blockIdx.x - M0 : blockIdx.x;
     const double *Ain = second ? Ain1 : Ain0;
     double *evals = second ? evals1 : evals0;
     double *evecs = second ? evecs1 : evecs0;
+    const double *V0 = second ? V01 : V00;
     const double *Am = Ain + (size_t)m * D * D;
     for (int blk = tid; blk < JAC_BLOCKS; blk += JAC_THREADS) {
         int k2 = (int)((sqrt(8.0 * blk + 1.0) - 1.0) * 0.5);
@@ -174,23 +195,30 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
     __syncthreads();
     for (int e = tid; e < D * D; e += JAC_THREADS) {
         int i = e / D, j = e % D;
-        V[e] = (i == j) ? 1.0 : 0.0;
+        V[e] = V0 ? (R)V0[(size_t)m * D * D + e] : (R)((i == j) ? 1.0 : 0.0);
         if (i <= j) {
             double a = 0.5 * (Am[i * D + j] + Am[j * D + i]);
             if (!isfinite(a)) flag[1] = 1;
-            A[tri(i, j)] = a;
+            A[tri(i, j)] = (R)a;
         }
     }
     __syncthreads();
     if (flag[1]) {
         if (tid == 0) atomicOr(status, AATC_DEV_NONFINITE);
         for (int e = tid; e < D * D; e += JAC_THREADS) evecs[(size_t)m * D * D + e] = 0.0;
-        if (tid < D) evals[m * D + tid] = 0.0;
+        if (!PRE && tid < D) evals[m * D + tid] = 0.0;
         return;
     }
+    if (PRE && tid == 0) {   // fp32 noise level: 2^-23 of the largest diagonal entry
+        R mx = 0;
+        for (int i = 0; i < D; ++i) mx = fmax(mx, fabs(A[tri(i, i)]));
+        floor_s = mx * (R)1.1920929e-7;
+    }
 
+    const R tol = PRE ? (R)1e-6 : (R)JACOBI_TOL;
+    const int sweeps_cap = PRE ? PRE_SWEEPS : max_sweeps;
     bool converged = false;
-    for (int sweep = 0; sweep < max_sweeps && !converged; ++sweep) {
+    for (int sweep = 0; sweep < sweeps_cap && !converged; ++sweep) {
         if (tid == 0) flag[0] = 0;
         __syncthreads();
         for (int r = 0; r < D - 1; ++r) {
@@ -199,39 +227,39 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
                 if (tid == 0) { a = r; b = D - 1; }
                 else { a = (r + tid) % (D - 1); b = (r - tid + (D - 1)) % (D - 1); }
                 int p = min(a, b), q = max(a, b);
-                double apq = A[tri(p, q)], app = A[tri(p, p)], aqq = A[tri(q, q)];
-                double c = 1.0, s = 0.0;
-                if (fabs(apq) > JACOBI_TOL * sqrt(fabs(app * aqq))) {
-                    double tau = (aqq - app) / (2.0 * apq);
-                    double t = (tau >= 0.0 ? 1.0 : -1.0) / (fabs(tau) + sqrt(1.0 + tau * tau));
-                    c = 1.0 / sqrt(1.0 + t * t);
-                    s = t * c;
+                R apq = A[tri(p, q)], app = A[tri(p, p)], aqq = A[tri(q, q)];
+                R c = 1, sn = 0;
+                if (fabs(apq) > tol * sqrt(fabs(app * aqq)) && (!PRE || fabs(apq) > floor_s)) {
+                    R tau = (aqq - app) / (2 * apq);
+                    R t = (tau >= 0 ? (R)1 : (R)-1) / (fabs(tau) + sqrt(1 + tau * tau));
+                    c = 1 / sqrt(1 + t * t);
+                    sn = t * c;
                     flag[0] = 1;
                 }
                 pq[2 * tid] = p; pq[2 * tid + 1] = q;
-                cs[2 * tid] = c; cs[2 * tid + 1] = s;
+                cs[2 * tid] = c; cs[2 * tid + 1] = sn;
             }
             __syncthreads();
             // A <- J^T A J, one 2x2 block (pair k1, pair k2) per task, k1 <= k2
             for (int blk = tid; blk < JAC_BLOCKS; blk += JAC_THREADS) {
                 const int k1 = kpair[2 * blk], k2 = kpair[2 * blk + 1];
                 int p1 = pq[2 * k1], q1 = pq[2 * k1 + 1];
-                double c1 = cs[2 * k1], s1 = cs[2 * k1 + 1];
+                R c1 = cs[2 * k1], s1 = cs[2 * k1 + 1];
                 if (k1 == k2) {
-                    double app = A[tri(p1, p1)], aqq = A[tri(q1, q1)], apq = A[tri(p1, q1)];
-                    if (s1 != 0.0) {
-                        A[tri(p1, p1)] = c1 * c1 * app - 2.0 * c1 * s1 * apq + s1 * s1 * aqq;
-                        A[tri(q1, q1)] = s1 * s1 * app + 2.0 * c1 * s1 * apq + c1 * c1 * aqq;
-                        A[tri(p1, q1)] = 0.0;
+                    R app = A[tri(p1, p1)], aqq = A[tri(q1, q1)], apq = A[tri(p1, q1)];
+                    if (s1 != 0) {
+                        A[tri(p1, p1)] = c1 * c1 * app - 2 * c1 * s1 * apq + s1 * s1 * aqq;
+                        A[tri(q1, q1)] = s1 * s1 * app + 2 * c1 * s1 * apq + c1 * c1 * aqq;
+                        A[tri(p1, q1)] = 0;
                     }
                 } else {
                     int p2 = pq[2 * k2], q2 = pq[2 * k2 + 1];
-                    double c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
+                    R c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
                     int i_pp = tri(p1, p2), i_pq = tri(p1, q2), i_qp = tri(q1, p2), i_qq = tri(q1, q2);
-                    double xpp = A[i_pp], xpq = A[i_pq], xqp = A[i_qp], xqq = A[i_qq];
+                    R xpp = A[i_pp], xpq = A[i_pq], xqp = A[i_qp], xqq = A[i_qq];
                     // rows: R1^T X  (R = [[c, s], [-s, c]])
-                    double ypp = c1 * xpp - s1 * xqp, ypq = c1 * xpq - s1 * xqq;
-                    double yqp = s1 * xpp + c1 * xqp, yqq = s1 * xpq + c1 * xqq;
+                    R ypp = c1 * xpp - s1 * xqp, ypq = c1 * xpq - s1 * xqq;
+                    R yqp = s1 * xpp + c1 * xqp, yqq = s1 * xpq + c1 * xqq;
                     // columns: (R1^T X) R2
                     A[i_pp] = c2 * ypp - s2 * ypq;
                     A[i_pq] = s2 * ypp + c2 * ypq;
@@ -242,17 +270,21 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
             // V <- V J
             for (int e = tid; e < D * 64; e += JAC_THREADS) {
                 int i = e >> 6, k = e & 63;
-                double c = cs[2 * k], s = cs[2 * k + 1];
-                if (s == 0.0) continue;
+                R c = cs[2 * k], sn = cs[2 * k + 1];
+                if (sn == 0) continue;
                 int p = pq[2 * k], q = pq[2 * k + 1];
-                double vp = V[i * D + p], vq = V[i * D + q];
-                V[i * D + p] = c * vp - s * vq;
-                V[i * D + q] = s * vp + c * vq;
+                R vp = V[i * D + p], vq = V[i * D + q];
+                V[i * D + p] = c * vp - sn * vq;
+                V[i * D + q] = sn * vp + c * vq;
             }
             __syncthreads();
         }
         converged = (flag[0] == 0);
         __syncthreads();
+    }
+    if (PRE) {   // the raw rotations, for the fp64 pass
+        for (int e = tid; e < D * D; e += JAC_THREADS) evecs[(size_t)m * D * D + e] = (double)V[e];
+        return;
     }
     if (!converged && tid == 0) atomicOr(status, AATC_DEV_NO_CONVERGENCE);
 
@@ -275,6 +307,14 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
         double *out = evecs + (size_t)m * D * D;
         for (int i = 0; i < D; ++i) out[i * D + rank] = sg * V[i * D + tid];
     }
+}
+
+// Q <- 1.5 Q - 0.5 Y (Y = Q Q^T Q): one Newton-Schulz step towards the
+// orthogonal factor of Q, [M][D][D].
+__global__ void k_ns_step(double *__restrict__ Q, const double *__restrict__ Y, size_t n)
+{
+    const size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e < n) Q[e] = 1.5 * Q[e] - 0.5 * Y[e];
 }
 
 // ---------------------------------------------------------------------------
@@ -522,7 +562,38 @@ size_t calib_work_bytes(int Hkv, int Hq, int N)
     const size_t tc = cov_tc_scratch(Hkv, (long)G * N);   // the largest of the three (rows G N >= N)
     if (tc > partial) partial = tc;
     partial = (partial + 255) & ~(size_t)255;
-    return partial + (size_t)Hkv * 7 * mat;   // Sk Sv Sq Uq Sh Si Mk
+    return partial + (size_t)Hkv * 13 * mat;   // Sk Sv Sq Uq Sh Si Mk, Jacobi scratch 3 x 2H
+}
+
+// Eigendecomposition of m symmetric matrices A[m] (fp64), the first M0 into
+// (evals0, evecs0), the rest into (evals1, evecs1): fp32 sweeps give the
+// rotations Q; two Newton-Schulz steps make Q orthogonal in fp64
+// (Q <- Q (3 I - Q^T Q) / 2); the fp64 sweeps run on Q^T A Q, accumulating from Q.
+static aatc_status jacobi_mixed(const double *A, int m, int M0, double *evals0, double *evecs0, double *evals1,
+                         double *evecs1, double *Q, double *X, double *Y, int max_sweeps, uint32_t *status,
+                         cudaStream_t s)
+{
+    constexpr size_t M = (size_t)D * D;
+    AATC_CUDA(cudaFuncSetAttribute(k_jacobi<float, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)jac_smem<float>()));
+    AATC_CUDA(cudaFuncSetAttribute(k_jacobi<double, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)jac_smem<double>()));
+    k_jacobi<float, true><<<m, JAC_THREADS, jac_smem<float>(), s>>>(A, nullptr, Q, nullptr, m, nullptr, nullptr,
+                                                                    nullptr, nullptr, PRE_SWEEPS, status);
+    const dim3 gg(D * D / 256, m);
+    const size_t n = (size_t)m * M;
+    for (int it = 0; it < 2; ++it) {
+        k_gemm64<<<gg, 256, 0, s>>>(Q, 1, nullptr, DIAG_NONE, Q, 0, X);   // X = Q^T Q
+        k_gemm64<<<gg, 256, 0, s>>>(Q, 0, nullptr, DIAG_NONE, X, 0, Y);   // Y = Q X
+        k_ns_step<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(Q, Y, n);
+    }
+    k_gemm64<<<gg, 256, 0, s>>>(Q, 1, nullptr, DIAG_NONE, A, 0, X);       // X = Q^T A
+    k_gemm64<<<gg, 256, 0, s>>>(X, 0, nullptr, DIAG_NONE, Q, 0, Y);       // Y = Q^T A Q
+    k_jacobi<double, false><<<m, JAC_THREADS, jac_smem<double>(), s>>>(Y, evals0, evecs0, Q, M0, Y + M0 * M,
+                                                                       evals1, evecs1, Q + M0 * M, max_sweeps,
+                                                                       status);
+    AATC_CUDA(cudaGetLastError());
+    return AATC_OK;
 }
 
 aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const void *q_cal,
@@ -542,6 +613,7 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     double *Sk = (double *)((char *)base + pbytes);
     double *Sv = Sk + H * M, *Sq = Sv + H * M, *Uq = Sq + H * M, *Sh = Uq + H * M,
            *Si = Sh + H * M, *Mk = Si + H * M;
+    double *Qs = Mk + H * M, *Xs = Qs + 2 * H * M, *Ys = Xs + 2 * H * M;   // Jacobi scratch, 2H each
     aatc_status st;
     if (h->dtype == AATC_BF16)
         st = launch_stats((const __nv_bfloat16 *)k_cal, (const __nv_bfloat16 *)v_cal,
@@ -551,10 +623,11 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
                           Sk, Sv, Sq, partial, s);
     if (st != AATC_OK) return st;
 
-    AATC_CUDA(cudaFuncSetAttribute(k_jacobi, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)JAC_SMEM));
     // query metric: Sq = Uq Lq Uq^T ; Sh = Sq^{1/2}, Si = Sq^{-1/2}; with it the
-    // value KLT Sv = Uv Lv Uv^T (independent of the key path)
-    k_jacobi<<<2 * H, JAC_THREADS, JAC_SMEM, s>>>(Sq, h->lam_q, Uq, H, Sv, h->lam_v, h->U_v, max_sweeps, h->status);
+    // value KLT Sv = Uv Lv Uv^T (independent of the key path).  Sv and Sq are
+    // adjacent: one batch of 2H matrices.
+    st = jacobi_mixed(Sv, 2 * H, H, h->lam_v, h->U_v, h->lam_q, Uq, Qs, Xs, Ys, max_sweeps, h->status, s);
+    if (st != AATC_OK) return st;
     const dim3 gg(D * D / 256, H);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_SQRT, Uq, 1, Sh);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, h->lam_q, DIAG_INVSQRT, Uq, 1, Si);
@@ -562,7 +635,8 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     k_gemm64<<<gg, 256, 0, s>>>(Sh, 0, nullptr, DIAG_NONE, Sk, 0, Uq);       // Uq reused as tmp
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 0, nullptr, DIAG_NONE, Sh, 0, Mk);
     // key KLT: Mk = Uk Lk Uk^T (Uk kept in Uq)
-    k_jacobi<<<H, JAC_THREADS, JAC_SMEM, s>>>(Mk, h->lam_k, Uq, H, nullptr, nullptr, nullptr, max_sweeps, h->status);
+    st = jacobi_mixed(Mk, H, H, h->lam_k, Uq, nullptr, nullptr, Qs, Xs, Ys, max_sweeps, h->status, s);
+    if (st != AATC_OK) return st;
     // Tk = Uk^T Sh, Ak = Uk^T Si, Tk^{-1} = Si Uk, Tv = Uv^T
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Sh, 0, h->T_k);
     k_gemm64<<<gg, 256, 0, s>>>(Uq, 1, nullptr, DIAG_NONE, Si, 0, h->A_k);
