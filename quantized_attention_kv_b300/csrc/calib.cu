@@ -253,8 +253,9 @@ __global__ void __launch_bounds__(JAC_THREADS) k_jacobi(const double *__restrict
                         A[tri(p1, q1)] = 0;
                     }
                 } else {
-                    int p2 = pq[2 * k2], q2 = pq[2 * k2 + 1];
                     R c2 = cs[2 * k2], s2 = cs[2 * k2 + 1];
+                    if (s1 == 0 && s2 == 0) continue;   // identity on this block (exactly)
+                    int p2 = pq[2 * k2], q2 = pq[2 * k2 + 1];
                     int i_pp = tri(p1, p2), i_pq = tri(p1, q2), i_qp = tri(q1, p2), i_qq = tri(q1, q2);
                     R xpp = A[i_pp], xpq = A[i_pq], xqp = A[i_qp], xqq = A[i_qq];
                     // rows: R1^T X  (R = [[c, s], [-s, c]])
