@@ -88,7 +88,11 @@ typedef struct {
  * them on the tensor cores from x - mean rounded once to 28-bit fixed point
  * (one power-of-two scale per channel); the contraction itself is exact, so
  * the moments differ from fp64 ones only by that rounding (relative 2^-27 of
- * each channel's largest |x - mean|).  Eigensolver and allocation run in fp64.
+ * each channel's largest |x - mean|).  The eigensolver runs fp32 sweeps,
+ * makes their rotations orthogonal in fp64, then runs fp64 sweeps to the fp64
+ * stopping test (|a_pq| <= 1e-15 sqrt(|a_pp a_qq|)), so its results are those
+ * of an fp64 solver; jacobi_max_sweeps bounds the fp64 sweeps.  Allocation
+ * runs in fp64.
  * Synchronizes `stream` once.  Returns NO_CONVERGENCE / NONFINITE from the
  * device status; the handle is not created then. */
 aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const void *v_cal,
