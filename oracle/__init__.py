@@ -58,6 +58,8 @@ def lib():
             "orc_key_transform": (I, [P, P, I, I, D, P, P, P, P, P]),
             "orc_waterfill_theta": (D, [P, I, D, P, P]),
             "orc_allocate_bits": (I, [P, I, I, P, P]),
+            "orc_attention_weights": (None, [P, P, P, Lg, Lg, I, P, P]),
+            "orc_joint_allocation": (I, [P, P, I, D, D, I, I, P, P, P, P]),
             "orc_gauss_uniform_mse": (D, [I, D]),
             "orc_gauss_uniform_step": (D, [I]),
             "orc_steps": (None, [P, P, I, P]),
@@ -162,6 +164,55 @@ def allocate_bits(lam, B_bits: int):
     if rc != 0:
         raise ValueError("unsupported budget")
     return b, m.value
+
+
+def attention_weights(Q, K, V):
+    """Token weights of the distortion theorem for one KV head: (alpha_K, alpha_V)
+    averaged over the calibration queries Q [m][d] attending keys K [n][d] and
+    values V [n][d]: alpha_V = sum_i A_i^2, alpha_K = (1/d) sum_i A_i^2 |v_i - o|^2."""
+    Q, K, V = _f64(Q), _f64(K), _f64(V)
+    m, d = Q.shape
+    n = K.shape[0]
+    ak, av = ctypes.c_double(0.0), ctypes.c_double(0.0)
+    lib().orc_attention_weights(_p(Q), _p(K), _p(V), m, n, d, ctypes.byref(ak), ctypes.byref(av))
+    return ak.value, av.value
+
+
+def joint_allocation(lam_k, lam_v, alpha_k: float, alpha_v: float, B_total: int, granule: int = 32):
+    """One water level over K and V: returns (bits_k, bits_v, B_k, cost) for the
+    split B_k + B_v = B_total (multiples of `granule`) of least weighted distortion."""
+    lam_k, lam_v = _f64(lam_k), _f64(lam_v)
+    d = lam_k.shape[0]
+    bk, bv = np.empty(d, dtype=np.int32), np.empty(d, dtype=np.int32)
+    Bk, cost = ctypes.c_int(0), ctypes.c_double(0.0)
+    rc = lib().orc_joint_allocation(_p(lam_k), _p(lam_v), d, float(alpha_k), float(alpha_v), int(B_total),
+                                    int(granule), _p(bk), _p(bv), ctypes.byref(Bk), ctypes.byref(cost))
+    if rc != 0:
+        raise ValueError("unsupported budget")
+    return bk, bv, Bk.value, cost.value
+
+
+def joint_split(k_cal, v_cal, q_cal, cal, granule: int = 32):
+    """Joint K/V allocation per KV head from a calibration `cal` (its lam_k of the
+    whitened key covariance and lam_v): the token weights of the G query heads'
+    calibration queries attending the head's calibration keys and values, then
+    one water level over K and V with the pair budget 2 * 32 * W.  Returns a
+    list of dicts (alpha_k, alpha_v, B_k, B_v, bits_k, bits_v, cost, cost_even)."""
+    k_cal, v_cal, q_cal = _f64(k_cal), _f64(v_cal), _f64(q_cal)
+    Hkv, Hq = k_cal.shape[0], q_cal.shape[0]
+    G = Hq // Hkv
+    B = 32 * int(cal["W"])
+    out = []
+    for h in range(Hkv):
+        Qh = q_cal[h * G:(h + 1) * G].reshape(-1, q_cal.shape[-1])
+        ak, av = attention_weights(Qh, k_cal[h], v_cal[h])
+        lk, lv = cal["lam_k"][h], cal["lam_v"][h]
+        bk, bv, Bk, cost = joint_allocation(lk, lv, ak, av, 2 * B, granule)
+        even = ak * float(np.sum(lk * 4.0 ** -cal["bits_k"][h].astype(np.float64))) + \
+            av * float(np.sum(lv * 4.0 ** -cal["bits_v"][h].astype(np.float64)))
+        out.append(dict(alpha_k=ak, alpha_v=av, B_k=Bk, B_v=2 * B - Bk, bits_k=bk, bits_v=bv, cost=cost,
+                        cost_even=even))
+    return out
 
 
 def gauss_uniform_mse(b: int, step: float) -> float:

@@ -307,6 +307,112 @@ int orc_allocate_bits(const double *lam, int d, int B_bits, int *bits, double *m
 }
 
 /* ------------------------------------------------------------------------ */
+/* Attention-aware token weights and the joint K/V budget split [THM], [RWF] */
+/* ------------------------------------------------------------------------ */
+
+/* [THM] writes the value distortion as sum_i A_i^2 sum_j sigma_Vij^2 and the
+ * key distortion as (1/d) sum_j q_j^2 sum_i A_i^2 |v_i - o|^2 sigma_Kij^2.  A
+ * fixed quantizer per channel gives every token the same noise variance, so
+ * the token sums factor out of both:
+ *   alpha_V = sum_i A_i^2,   alpha_K = (1/d) sum_i A_i^2 |v_i - o|^2.
+ * Reading: both are averaged over m calibration queries Q [m][d], each of
+ * which attends all n calibration keys K [n][d] (values V [n][d]) with the
+ * 1/sqrt(d) scale and no mask.  The q_j^2 factor stays in the key metric (the
+ * query second-moment whitening), so the per-channel key weights remain the
+ * eigenvalues of the whitened key covariance.  Plain loops, exact softmax. */
+void orc_attention_weights(const double *Q, const double *K, const double *V, long m, long n, int d,
+                           double *alpha_k, double *alpha_v)
+{
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    double *o = (double *)malloc(sizeof(double) * (size_t)d);
+    const double scale = 1.0 / sqrt((double)d);
+    double ak = 0.0, av = 0.0;
+    for (long q = 0; q < m; ++q) {
+        double mx = -INFINITY;
+        for (long i = 0; i < n; ++i) {
+            double dot = 0.0;
+            for (int j = 0; j < d; ++j) dot += Q[q * d + j] * K[i * d + j];
+            s[i] = dot * scale;
+            if (s[i] > mx) mx = s[i];
+        }
+        double den = 0.0;
+        for (long i = 0; i < n; ++i) {
+            s[i] = exp(s[i] - mx);
+            den += s[i];
+        }
+        for (int j = 0; j < d; ++j) o[j] = 0.0;
+        double a2 = 0.0;
+        for (long i = 0; i < n; ++i) {
+            s[i] /= den; /* A_i */
+            a2 += s[i] * s[i];
+            for (int j = 0; j < d; ++j) o[j] += s[i] * V[i * d + j];
+        }
+        double r = 0.0;
+        for (long i = 0; i < n; ++i) {
+            double e2 = 0.0;
+            for (int j = 0; j < d; ++j) {
+                const double e = V[i * d + j] - o[j];
+                e2 += e * e;
+            }
+            r += s[i] * s[i] * e2;
+        }
+        av += a2;
+        ak += r / d;
+    }
+    free(s);
+    free(o);
+    *alpha_k = m > 0 ? ak / m : 0.0;
+    *alpha_v = m > 0 ? av / m : 0.0;
+}
+
+/* Weighted high-rate distortion of an allocation: alpha sum_j lam_j 4^-b_j. */
+static double alloc_cost(const double *lam, const int *bits, int d, double alpha)
+{
+    double c = 0.0;
+    for (int j = 0; j < d; ++j) c += ldexp(lam[j] > 0.0 ? lam[j] : 0.0, -2 * bits[j]);
+    return alpha * c;
+}
+
+/* [RWF] with the [THM] weights: one water level over the 2d channels of K and
+ * V, i.e. minimize alpha_K sum_j lam_Kj 4^-bKj + alpha_V sum_j lam_Vj 4^-bVj
+ * subject to sum bK + sum bV = B_total, 0 <= b <= 8.  Reading: each tensor's
+ * record keeps a fixed width, so the split B_K + B_V = B_total is restricted
+ * to multiples of `granule` bits (32 for the record format).  For each such
+ * split each side takes its exact top-B allocation (orc_allocate_bits), which
+ * is optimal for that side's budget; the split of least cost wins, ties going
+ * to the split nearest B_total / 2, then to the smaller B_K.  Returns -1 for an
+ * impossible budget. */
+int orc_joint_allocation(const double *lam_k, const double *lam_v, int d, double alpha_k, double alpha_v,
+                         int B_total, int granule, int *bits_k, int *bits_v, int *B_k, double *cost)
+{
+    if (granule <= 0 || B_total < 0 || B_total > 2 * ORC_MAXB * d || B_total % granule) return -1;
+    int *tk = (int *)malloc(sizeof(int) * (size_t)d), *tv = (int *)malloc(sizeof(int) * (size_t)d);
+    int best = -1;
+    double best_cost = INFINITY;
+    for (int bk = 0; bk <= B_total; bk += granule) {
+        const int bv = B_total - bk;
+        if (bk > ORC_MAXB * d || bv > ORC_MAXB * d) continue;
+        orc_allocate_bits(lam_k, d, bk, tk, NULL);
+        orc_allocate_bits(lam_v, d, bv, tv, NULL);
+        const double c = alloc_cost(lam_k, tk, d, alpha_k) + alloc_cost(lam_v, tv, d, alpha_v);
+        const int better = best < 0 || c < best_cost ||
+                           (c == best_cost && abs(2 * bk - B_total) < abs(2 * best - B_total));
+        if (better) {
+            best = bk;
+            best_cost = c;
+            memcpy(bits_k, tk, sizeof(int) * (size_t)d);
+            memcpy(bits_v, tv, sizeof(int) * (size_t)d);
+        }
+    }
+    free(tk);
+    free(tv);
+    if (best < 0) return -1;
+    *B_k = best;
+    *cost = best_cost;
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Step sizes: MSE-optimal uniform quantizer for a unit Gaussian            */
 /* ------------------------------------------------------------------------ */
 
