@@ -59,7 +59,7 @@ def lib():
             "orc_waterfill_theta": (D, [P, I, D, P, P]),
             "orc_allocate_bits": (I, [P, I, I, P, P]),
             "orc_attention_weights": (None, [P, P, P, Lg, Lg, I, P, P]),
-            "orc_joint_allocation": (I, [P, P, I, D, D, I, I, P, P, P, P]),
+            "orc_joint_allocation": (I, [P, P, I, I, P, P, I, I, P, P, P, P]),
             "orc_gauss_uniform_mse": (D, [I, D]),
             "orc_gauss_uniform_step": (D, [I]),
             "orc_steps": (None, [P, P, I, P]),
@@ -76,7 +76,7 @@ def lib():
             "orc_encode": (None, [P, Lg, I, P, P, P, P, I, P, P, P]),
             "orc_attention": (None, [P, P, P, Lg, I, P]),
             "orc_reconstruct": (None, [P, Lg, I, I, P, P, P, P, P]),
-            "orc_decode_head": (None, [P, I, P, P, Lg, I, I, P, P, P, P, P, P, P, P, P]),
+            "orc_decode_head": (None, [P, I, P, P, Lg, I, I, I, P, P, P, P, P, P, P, P, P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -178,18 +178,26 @@ def attention_weights(Q, K, V):
     return ak.value, av.value
 
 
-def joint_allocation(lam_k, lam_v, alpha_k: float, alpha_v: float, B_total: int, granule: int = 32):
-    """One water level over K and V: returns (bits_k, bits_v, B_k, cost) for the
-    split B_k + B_v = B_total (multiples of `granule`) of least weighted distortion."""
-    lam_k, lam_v = _f64(lam_k), _f64(lam_v)
-    d = lam_k.shape[0]
-    bk, bv = np.empty(d, dtype=np.int32), np.empty(d, dtype=np.int32)
+def joint_allocation_layer(lam_k, lam_v, alpha_k, alpha_v, B_total: int, granule: int = 32):
+    """One water level over K and V for the H heads of a layer (lam_k, lam_v
+    [H][d], alpha_k, alpha_v [H]) with one split B_k + B_v = B_total common to
+    the heads (multiples of `granule`).  Returns (bits_k, bits_v [H][d], B_k, cost)."""
+    lam_k, lam_v = np.atleast_2d(_f64(lam_k)), np.atleast_2d(_f64(lam_v))
+    H, d = lam_k.shape
+    ak, av = _f64(np.atleast_1d(alpha_k)), _f64(np.atleast_1d(alpha_v))
+    bk, bv = np.empty((H, d), dtype=np.int32), np.empty((H, d), dtype=np.int32)
     Bk, cost = ctypes.c_int(0), ctypes.c_double(0.0)
-    rc = lib().orc_joint_allocation(_p(lam_k), _p(lam_v), d, float(alpha_k), float(alpha_v), int(B_total),
-                                    int(granule), _p(bk), _p(bv), ctypes.byref(Bk), ctypes.byref(cost))
+    rc = lib().orc_joint_allocation(_p(lam_k), _p(lam_v), H, d, _p(ak), _p(av), int(B_total), int(granule),
+                                    _p(bk), _p(bv), ctypes.byref(Bk), ctypes.byref(cost))
     if rc != 0:
         raise ValueError("unsupported budget")
     return bk, bv, Bk.value, cost.value
+
+
+def joint_allocation(lam_k, lam_v, alpha_k: float, alpha_v: float, B_total: int, granule: int = 32):
+    """joint_allocation_layer for one head: returns (bits_k, bits_v [d], B_k, cost)."""
+    bk, bv, Bk, cost = joint_allocation_layer(lam_k, lam_v, [alpha_k], [alpha_v], B_total, granule)
+    return bk[0], bv[0], Bk, cost
 
 
 def joint_split(k_cal, v_cal, q_cal, cal, granule: int = 32):
@@ -373,13 +381,17 @@ def attention(q, K, V) -> np.ndarray:
 
 
 # ---------------------------------------------------------------- pipeline
-def calibrate(k_cal, v_cal, q_cal, bits_per_element: float, max_sweeps: int = 50):
+def calibrate(k_cal, v_cal, q_cal, bits_per_element: float, max_sweeps: int = 50, joint: bool = False):
     """Per-KV-head calibration.
 
     k_cal, v_cal: [H_kv][N][d]; q_cal: [H_q][N][d] (query head h uses KV head
     h // G).  Returns a dict of per-head arrays (leading axis H_kv):
     mu_k, mu_v, T_k, T_k_inv, A_k, lam_k, T_v (= U_v^T), U_v, lam_v, lam_q,
-    bits_k, bits_v, step_k, step_v, margin_k, margin_v, W, ok.
+    bits_k, bits_v, step_k, step_v, margin_k, margin_v, W_k, W_v, W, ok.
+    Each tensor gets B = bits_per_element * d bits per token (W = B / 32 words)
+    unless `joint`: then the pair budget 2B is split between K and V by the
+    attention-aware token weights (joint_allocation_layer, one split for the
+    layer), W_k + W_v = 2W, and W is None when the widths differ.
     """
     k_cal, v_cal, q_cal = (np.asarray(a) for a in (k_cal, v_cal, q_cal))
     Hkv, N, d = k_cal.shape
@@ -413,7 +425,23 @@ def calibrate(k_cal, v_cal, q_cal, bits_per_element: float, max_sweeps: int = 50
                          ("margin_k", mk), ("margin_v", mv)):
             out[key].append(val)
     res = {k: np.stack([np.asarray(x) for x in v]) for k, v in out.items()}
-    res["W"] = B_bits // 32
+    res["W_k"] = res["W_v"] = res["W"] = B_bits // 32
+    if joint:
+        ak, av = [], []
+        for h in range(Hkv):
+            Q = _f64(q_cal[h * G:(h + 1) * G].reshape(G * N, d))
+            a = attention_weights(Q, _f64(k_cal[h]), _f64(v_cal[h]))
+            ak.append(a[0])
+            av.append(a[1])
+        bk, bv, Bk, _ = joint_allocation_layer(res["lam_k"], res["lam_v"], ak, av, 2 * B_bits)
+        res["bits_k"], res["bits_v"] = bk, bv
+        res["step_k"] = np.stack([steps(res["lam_k"][h], bk[h]) for h in range(Hkv)])
+        res["step_v"] = np.stack([steps(res["lam_v"][h], bv[h]) for h in range(Hkv)])
+        res["margin_k"] = np.array([allocate_bits(res["lam_k"][h], Bk)[1] for h in range(Hkv)])
+        res["margin_v"] = np.array([allocate_bits(res["lam_v"][h], 2 * B_bits - Bk)[1] for h in range(Hkv)])
+        res["alpha_k"], res["alpha_v"] = np.array(ak), np.array(av)
+        res["W_k"], res["W_v"] = Bk // 32, (2 * B_bits - Bk) // 32
+        res["W"] = res["W_k"] if res["W_k"] == res["W_v"] else None
     res["G"] = G
     res["ok"] = ok
     return res
@@ -423,7 +451,7 @@ def encode_cache(X, cal, tensor: str, want_codes=False, want_pre=False):
     """Encode a cache X [B][H_kv][L][d] with calibration `cal` ('k' or 'v')."""
     X = np.asarray(X)
     Bsz, Hkv, L, d = X.shape
-    W = cal["W"]
+    W = cal.get("W_" + tensor, cal["W"])
     T = cal["T_k"] if tensor == "k" else cal["T_v"]
     rec = np.empty((Bsz, Hkv, L, W), dtype=np.uint32)
     codes = np.empty((Bsz, Hkv, L, d), dtype=np.int32) if want_codes else None
@@ -450,7 +478,7 @@ def decode_attention(q, kp, vp, cal, seq_lens=None):
     Bsz, Hq, d = q.shape
     Hkv = kp.shape[1]
     G = Hq // Hkv
-    W = cal["W"]
+    Wk, Wv = cal.get("W_k", cal["W"]), cal.get("W_v", cal["W"])
     out = np.zeros((Bsz, Hq, d))
     for b in range(Bsz):
         L = kp.shape[2] if seq_lens is None else int(seq_lens[b])
@@ -462,6 +490,6 @@ def decode_attention(q, kp, vp, cal, seq_lens=None):
             args = [_f64(cal["T_k_inv"][h]), _f64(cal["mu_k"][h]), _f32(cal["step_k"][h]),
                     _i32(cal["bits_k"][h]), _f64(cal["U_v"][h]), _f64(cal["mu_v"][h]),
                     _f32(cal["step_v"][h]), _i32(cal["bits_v"][h])]
-            lib().orc_decode_head(_p(qq), G, _p(kr), _p(vr), L, d, W, *[_p(a) for a in args], _p(o))
+            lib().orc_decode_head(_p(qq), G, _p(kr), _p(vr), L, d, Wk, Wv, *[_p(a) for a in args], _p(o))
             out[b, h * G:(h + 1) * G] = o
     return out

@@ -373,35 +373,43 @@ static double alloc_cost(const double *lam, const int *bits, int d, double alpha
     return alpha * c;
 }
 
-/* [RWF] with the [THM] weights: one water level over the 2d channels of K and
- * V, i.e. minimize alpha_K sum_j lam_Kj 4^-bKj + alpha_V sum_j lam_Vj 4^-bVj
- * subject to sum bK + sum bV = B_total, 0 <= b <= 8.  Reading: each tensor's
- * record keeps a fixed width, so the split B_K + B_V = B_total is restricted
- * to multiples of `granule` bits (32 for the record format).  For each such
- * split each side takes its exact top-B allocation (orc_allocate_bits), which
- * is optimal for that side's budget; the split of least cost wins, ties going
- * to the split nearest B_total / 2, then to the smaller B_K.  Returns -1 for an
+/* [RWF] with the [THM] weights: one water level over the channels of K and V,
+ * i.e. minimize sum_h alpha_Kh sum_j lam_Khj 4^-bKhj + alpha_Vh sum_j lam_Vhj 4^-bVhj
+ * subject to sum_j bKhj + sum_j bVhj = B_total for each of the H heads of a
+ * layer, 0 <= b <= 8.  Reading: a cache holds one record width per tensor for
+ * every head of the layer, so the split B_K + B_V = B_total is common to the
+ * heads and restricted to multiples of `granule` bits (32 for the record
+ * format).  For each such split every head takes the exact top-B allocation of
+ * each side (orc_allocate_bits), optimal for that budget; the split of least
+ * total cost wins, ties going to the split nearest B_total / 2, then to the
+ * smaller B_K.  lam_k, lam_v, bits_k, bits_v: [H][d].  Returns -1 for an
  * impossible budget. */
-int orc_joint_allocation(const double *lam_k, const double *lam_v, int d, double alpha_k, double alpha_v,
-                         int B_total, int granule, int *bits_k, int *bits_v, int *B_k, double *cost)
+int orc_joint_allocation(const double *lam_k, const double *lam_v, int H, int d, const double *alpha_k,
+                         const double *alpha_v, int B_total, int granule, int *bits_k, int *bits_v, int *B_k,
+                         double *cost)
 {
-    if (granule <= 0 || B_total < 0 || B_total > 2 * ORC_MAXB * d || B_total % granule) return -1;
-    int *tk = (int *)malloc(sizeof(int) * (size_t)d), *tv = (int *)malloc(sizeof(int) * (size_t)d);
+    if (H <= 0 || granule <= 0 || B_total < 0 || B_total > 2 * ORC_MAXB * d || B_total % granule) return -1;
+    const size_t n = (size_t)H * d;
+    int *tk = (int *)malloc(sizeof(int) * n), *tv = (int *)malloc(sizeof(int) * n);
     int best = -1;
     double best_cost = INFINITY;
     for (int bk = 0; bk <= B_total; bk += granule) {
         const int bv = B_total - bk;
         if (bk > ORC_MAXB * d || bv > ORC_MAXB * d) continue;
-        orc_allocate_bits(lam_k, d, bk, tk, NULL);
-        orc_allocate_bits(lam_v, d, bv, tv, NULL);
-        const double c = alloc_cost(lam_k, tk, d, alpha_k) + alloc_cost(lam_v, tv, d, alpha_v);
+        double c = 0.0;
+        for (int h = 0; h < H; ++h) {
+            orc_allocate_bits(lam_k + (size_t)h * d, d, bk, tk + (size_t)h * d, NULL);
+            orc_allocate_bits(lam_v + (size_t)h * d, d, bv, tv + (size_t)h * d, NULL);
+            c += alloc_cost(lam_k + (size_t)h * d, tk + (size_t)h * d, d, alpha_k[h]) +
+                 alloc_cost(lam_v + (size_t)h * d, tv + (size_t)h * d, d, alpha_v[h]);
+        }
         const int better = best < 0 || c < best_cost ||
                            (c == best_cost && abs(2 * bk - B_total) < abs(2 * best - B_total));
         if (better) {
             best = bk;
             best_cost = c;
-            memcpy(bits_k, tk, sizeof(int) * (size_t)d);
-            memcpy(bits_v, tv, sizeof(int) * (size_t)d);
+            memcpy(bits_k, tk, sizeof(int) * n);
+            memcpy(bits_v, tv, sizeof(int) * n);
         }
     }
     free(tk);
@@ -762,7 +770,7 @@ void orc_reconstruct(const uint32_t *rec, long n, int d, int W, const double *Ti
  * of one KV head: the G queries q [G][d] attend to the L reconstructed
  * tokens (keys via Tk_inv, values via Uv) -> out [G][d]. */
 void orc_decode_head(const double *q, int G, const uint32_t *krec, const uint32_t *vrec,
-                     long L, int d, int W,
+                     long L, int d, int Wk, int Wv,
                      const double *Tk_inv, const double *mu_k, const float *step_k, const int *bits_k,
                      const double *Uv, const double *mu_v, const float *step_v, const int *bits_v,
                      double *out)
@@ -770,8 +778,8 @@ void orc_decode_head(const double *q, int G, const uint32_t *krec, const uint32_
     double *Kh = (double *)malloc(sizeof(double) * (L > 0 ? L : 1) * d);
     double *Vh = (double *)malloc(sizeof(double) * (L > 0 ? L : 1) * d);
     if (L > 0) {
-        orc_reconstruct(krec, L, d, W, Tk_inv, mu_k, step_k, bits_k, Kh);
-        orc_reconstruct(vrec, L, d, W, Uv, mu_v, step_v, bits_v, Vh);
+        orc_reconstruct(krec, L, d, Wk, Tk_inv, mu_k, step_k, bits_k, Kh);
+        orc_reconstruct(vrec, L, d, Wv, Uv, mu_v, step_v, bits_v, Vh);
     }
 #pragma omp parallel for schedule(static)
     for (int g = 0; g < G; ++g) orc_attention(q + g * d, Kh, Vh, L, d, out + g * d);

@@ -143,3 +143,87 @@ def test_joint_split_on_the_tiny_workload():
         assert r["cost"] <= r["cost_even"] * (1 + 1e-12)
         bk, _ = oracle.allocate_bits(cal["lam_k"][h], r["B_k"])
         assert np.array_equal(bk, r["bits_k"])
+
+
+@pytest.mark.parametrize("granule", [1, 2])
+def test_layer_split_is_the_brute_force_optimum(granule):
+    """Two heads share one split (one record width per tensor for the layer):
+    brute force over the common B_K and every per-head bit vector."""
+    rng = np.random.default_rng(11 + granule)
+    lk, lv = rng.uniform(0.1, 10.0, (2, 2)), rng.uniform(0.1, 10.0, (2, 2))
+    ak, av = rng.uniform(0.2, 3.0, 2), rng.uniform(0.2, 3.0, 2)
+    vecs = list(itertools.product(range(9), repeat=2))
+    for B in range(0, 33, granule):
+        best = np.inf
+        for Bk in range(0, B + 1, granule):
+            tot = 0.0
+            for h in range(2):
+                ck = min((_cost(lk[h], b, ak[h]) for b in vecs if sum(b) == Bk), default=np.inf)
+                cv = min((_cost(lv[h], b, av[h]) for b in vecs if sum(b) == B - Bk), default=np.inf)
+                tot += ck + cv
+            best = min(best, tot)
+        bk, bv, Bk, cost = oracle.joint_allocation_layer(lk, lv, ak, av, B, granule)
+        assert np.all(bk.sum(axis=1) == Bk) and np.all(bk.sum(axis=1) + bv.sum(axis=1) == B)
+        assert cost == pytest.approx(best, rel=1e-12), B
+
+
+def _tiny_cals():
+    from quantized_attention_kv_b300 import synth
+    wl = synth.WORKLOADS["tiny"]
+    k, v, q = synth.calib_inputs(wl)
+    args = (k.double().numpy(), v.double().numpy(), q.double().numpy(), wl.bits)
+    return wl, oracle.calibrate(*args), oracle.calibrate(*args, joint=True)
+
+
+def test_joint_calibration_fields():
+    wl, ce, cj = _tiny_cals()
+    W = ce["W"]
+    assert cj["W_k"] + cj["W_v"] == 2 * W and cj["W_k"] != cj["W_v"] and cj["W"] is None
+    for h in range(wl.n_kv_heads):
+        assert cj["bits_k"][h].sum() == 32 * cj["W_k"] and cj["bits_v"][h].sum() == 32 * cj["W_v"]
+        assert np.array_equal(cj["bits_k"][h], oracle.allocate_bits(cj["lam_k"][h], 32 * cj["W_k"])[0])
+        assert np.array_equal(cj["step_v"][h], oracle.steps(cj["lam_v"][h], cj["bits_v"][h]))
+    for key in ("T_k", "T_v", "lam_k", "lam_v", "mu_k", "mu_v"):      # the transforms do not change
+        assert np.array_equal(cj[key], ce[key])
+
+
+def test_decode_with_unequal_record_widths():
+    """Records of W_K and W_V words: attention over the packed caches equals
+    attention over the keys and values reconstructed from the same records."""
+    from quantized_attention_kv_b300 import synth
+    wl, _, cj = _tiny_cals()
+    kc, vc = synth.cache_inputs(wl, seq_len=200, batch=1)
+    q = synth.query_inputs(wl, batch=1, step=5)
+    K, V, Q = kc.double().numpy(), vc.double().numpy(), q.double().numpy()
+    kr, _, _ = oracle.encode_cache(K, cj, "k")
+    vr, _, _ = oracle.encode_cache(V, cj, "v")
+    assert kr.shape[-1] == cj["W_k"] and vr.shape[-1] == cj["W_v"]
+    got = oracle.decode_attention(Q, kr, vr, cj)
+    Kh = oracle.reconstruct(kr[0, 0], cj["T_k_inv"][0], cj["mu_k"][0], cj["step_k"][0], cj["bits_k"][0])
+    Vh = oracle.reconstruct(vr[0, 0], cj["U_v"][0], cj["mu_v"][0], cj["step_v"][0], cj["bits_v"][0])
+    for g in range(Q.shape[1]):
+        np.testing.assert_allclose(got[0, g], oracle.attention(Q[0, g], Kh, Vh), rtol=1e-12, atol=1e-12)
+
+
+def test_joint_allocation_lowers_the_attention_error():
+    """The theorem's weighting in use: on the tiny workload, the attention error
+    of the joint split (relative to the output's variation around the value
+    mean) is below that of the even split."""
+    from quantized_attention_kv_b300 import synth
+    wl, ce, cj = _tiny_cals()
+    kc, vc = synth.cache_inputs(wl, seq_len=512, batch=2)
+    q = synth.query_inputs(wl, batch=2, step=3)
+    K, V, Q = kc.double().numpy(), vc.double().numpy(), q.double().numpy()
+    errs = []
+    for cal in (ce, cj):
+        kr, _, _ = oracle.encode_cache(K, cal, "k")
+        vr, _, _ = oracle.encode_cache(V, cal, "v")
+        o_hat = oracle.decode_attention(Q, kr, vr, cal)
+        num = den = 0.0
+        for b in range(2):
+            for g in range(Q.shape[1]):
+                o = oracle.attention(Q[b, g], K[b, 0], V[b, 0])
+                num += np.sum((o - o_hat[b, g]) ** 2)
+                den += np.sum((o - V[b, 0].mean(axis=0)) ** 2)
+        errs.append(num / den)
+    assert errs[1] < 0.8 * errs[0], errs
