@@ -52,16 +52,28 @@ def _peaks():
         return 6400.0, "fallback"
 
 
+# sources the decode kernels are built from: the kernels, the structures and
+# constants they share with the host, and the record layout and read plan
+DECODE_SOURCES = ("decode.cu", "internal.h", "plan.cu")
+
+
+def decode_source_hash(root=None):
+    """First 16 hex digits of the sha256 of the decode sources, concatenated."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(root or ROOT, "quantized_attention_kv_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def _traffic(algorithmic_bytes):
     """DRAM bytes per decode call from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    import hashlib
+    taken on the current decode sources (else None)."""
     try:
         with open(os.path.join(ROOT, "profiles", "decode_traffic.json")) as f:
             rec = json.load(f)
-        src = os.path.join(ROOT, "quantized_attention_kv_b300", "csrc", "decode.cu")
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if rec.get("decode_cu_sha256_16") != h:
+        if rec.get("decode_sources_sha256_16") != decode_source_hash():
             return None
         return rec["dram_bytes_per_call"]
     except Exception:

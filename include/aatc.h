@@ -189,9 +189,13 @@ size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L);
  * is not allowed.  It calls no cudaMalloc/cudaFree.
  *   - Shapes needing more scratch than 4 MiB (aatc_decode_workspace_size)
  *     are rejected with AATC_ERR_CAPACITY before any launch.
+ *   - Arguments are checked as aatc_decode_attention checks them (same
+ *     statuses) before the scratch size is compared with the array.
  *   - The first call on a device looks up the array's device address (once
  *     per device, with that device current); make that first call before any
- *     stream capture.
+ *     stream capture.  The address is kept for the life of the process: after
+ *     a cudaDeviceReset the library must be unloaded and loaded again before
+ *     this entry point is used on that device.
  *   - Every call on a device shares the one array and overwrites what the
  *     previous call left there (nothing in it needs to start at zero).  Calls
  *     that overlap on the GPU -- on different streams, or from several host

@@ -246,6 +246,15 @@ def quantize(c, step, bits) -> np.ndarray:
     return u
 
 
+def prequant(c, step, bits) -> np.ndarray:
+    """fp32 pre-rounding values v_j = c_j/Delta_j + (2^b_j - 1)/2 of quantize
+    (0 for pruned channels): where the rounding decision is taken."""
+    c, step, bits = _f64(c), _f32(step), _i32(bits)
+    v = np.empty(c.shape[0], dtype=np.float32)
+    lib().orc_prequant(_p(c), _p(step), _p(bits), c.shape[0], _p(v))
+    return v
+
+
 def dequantize(u, step, bits) -> np.ndarray:
     u, step, bits = _i32(u), _f32(step), _i32(bits)
     c = np.empty(u.shape[0])

@@ -391,6 +391,11 @@ int orc_joint_allocation(const double *lam_k, const double *lam_v, int H, int d,
     if (H <= 0 || granule <= 0 || B_total < 0 || B_total > 2 * ORC_MAXB * d || B_total % granule) return -1;
     const size_t n = (size_t)H * d;
     int *tk = (int *)malloc(sizeof(int) * n), *tv = (int *)malloc(sizeof(int) * n);
+    if (!tk || !tv) {
+        free(tk);
+        free(tv);
+        return -1;
+    }
     int best = -1;
     double best_cost = INFINITY;
     for (int bk = 0; bk <= B_total; bk += granule) {

@@ -273,11 +273,12 @@ size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L)
     return decode_ws_bytes(calib, B, L);
 }
 
-aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const uint32_t *k_packed,
-                                  const uint32_t *v_packed, int L_cap, const int32_t *seq_lens, int L,
-                                  int B, float *out, void *workspace, size_t ws_bytes, void *stream)
+}  // extern "C"
+
+aatc_status decode_check_args(const aatc_calib *calib, const void *q, const uint32_t *k_packed,
+                              const uint32_t *v_packed, int L_cap, const int32_t *seq_lens, int L, int B,
+                              const float *out)
 {
-    g_err[0] = 0;
     if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
     if (B < 0 || L < 0 || L_cap < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
     if (B > 65535 || L_cap > (1 << 28)) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
@@ -289,6 +290,18 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const 
     if (L_cap > 0 && (!k_packed || !v_packed || !aligned16(k_packed) || !aligned16(v_packed)))
         return aatc_fail(AATC_ERR_INVALID_ARG, "packed caches must be non-NULL and 16-byte aligned");
     if (seq_lens && ((uintptr_t)seq_lens & 3u)) return aatc_fail(AATC_ERR_INVALID_ARG, "seq_lens misaligned");
+    return AATC_OK;
+}
+
+extern "C" {
+
+aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const uint32_t *k_packed,
+                                  const uint32_t *v_packed, int L_cap, const int32_t *seq_lens, int L,
+                                  int B, float *out, void *workspace, size_t ws_bytes, void *stream)
+{
+    g_err[0] = 0;
+    aatc_status st = decode_check_args(calib, q, k_packed, v_packed, L_cap, seq_lens, L, B, out);
+    if (st != AATC_OK || B == 0) return st;
     const size_t need = decode_ws_bytes(calib, B, L);
     if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need))
         return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);

@@ -48,8 +48,10 @@ extern "C" aatc_status aatc_decode_attention_static(const aatc_calib *calib, con
                                                     int L_cap, const int32_t *seq_lens, int L, int B,
                                                     float *out, void *stream)
 {
-    if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
-    if (B < 0 || L < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
+    // the same argument checks as aatc_decode_attention, before the scratch
+    // size is worked out from B and L
+    aatc_status st = decode_check_args(calib, q, k_packed, v_packed, L_cap, seq_lens, L, B, out);
+    if (st != AATC_OK || B == 0) return st;
     const size_t need = decode_ws_bytes(calib, B, L);
     if (need > AATC_STATIC_SCRATCH_BYTES)
         return aatc_fail(AATC_ERR_CAPACITY,
@@ -57,7 +59,7 @@ extern "C" aatc_status aatc_decode_attention_static(const aatc_calib *calib, con
                          "(use aatc_decode_attention with a caller workspace)",
                          need, (unsigned)AATC_STATIC_SCRATCH_BYTES);
     void *scratch = nullptr;
-    aatc_status st = scratch_for_current_device(&scratch);
+    st = scratch_for_current_device(&scratch);
     if (st != AATC_OK) return st;
     // The decode kernels overwrite every scratch byte they later read, so the
     // previous call's contents need no clearing.

@@ -187,6 +187,11 @@ aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B,
                        uint32_t *vp, cudaStream_t s);
 
 // ---- decode (decode.cu) ----
+// Host checks of aatc_decode_attention's arguments other than the workspace
+// (api.cu); AATC_OK also for B == 0 (nothing to do).
+aatc_status decode_check_args(const aatc_calib *calib, const void *q, const uint32_t *k_packed,
+                              const uint32_t *v_packed, int L_cap, const int32_t *seq_lens, int L, int B,
+                              const float *out);
 size_t decode_ws_bytes(const aatc_calib *h, int B, int L);
 aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, const uint32_t *vp,
                        const CacheMap &map, const int32_t *seq_lens, int L, int B, float *out, void *ws,

@@ -51,3 +51,51 @@ def attn_rel_err(out_gpu: np.ndarray, out_ref: np.ndarray) -> float:
 
 def to_np64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().double().numpy()
+
+
+def records(cache_t, W, kind, L, start=0):
+    """Records [B][H][L][W] of tokens start.. read from a GPU cache through the oracle's tiling."""
+    c = as_u32(cache_t)
+    Bsz, H = c.shape[:2]
+    c = c.reshape(Bsz, H, -1)
+    out = np.empty((Bsz, H, L, W), dtype=np.uint32)
+    for b in range(Bsz):
+        for h in range(H):
+            out[b, h] = oracle.cache_get(np.ascontiguousarray(c[b, h]), W, kind, L, start)
+    return out
+
+
+def upload(rec, kind, L_cap):
+    """Oracle records [B][H][L][W] placed in a tiled GPU cache of L_cap tokens."""
+    Bsz, H, _, W = rec.shape
+    c = oracle.to_cache(rec, kind, L_cap).view(np.int32).reshape(Bsz, H, L_cap, W)
+    return torch.from_numpy(c).cuda()
+
+
+def synthetic_calibration(G, bits_k, bits_v, seed=0, H=1):
+    """A calibration with chosen bit allocations (orthogonal transforms from
+    QR, steps from the oracle), to reach every decode path; H KV heads that
+    share it."""
+    rng = np.random.default_rng(seed)
+    d = 128
+    cal = {}
+    Qk, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    Qv, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    lam_k = 0.95 ** np.arange(d)
+    lam_v = 0.93 ** np.arange(d)
+    rep = lambda a: np.repeat(np.asarray(a)[None], H, axis=0)  # noqa: E731
+    cal["mu_k"] = rep(rng.standard_normal(d))
+    cal["mu_v"] = rep(rng.standard_normal(d))
+    cal["T_k"] = rep(Qk.T)
+    cal["T_k_inv"] = rep(Qk)
+    cal["A_k"] = rep(Qk.T)
+    cal["T_v"] = rep(Qv.T)
+    cal["U_v"] = rep(Qv)
+    cal["lam_k"], cal["lam_v"], cal["lam_q"] = rep(lam_k), rep(lam_v), rep(np.ones(d))
+    cal["bits_k"] = rep(np.asarray(bits_k, dtype=np.int32))
+    cal["bits_v"] = rep(np.asarray(bits_v, dtype=np.int32))
+    cal["step_k"] = rep(oracle.steps(lam_k, bits_k))
+    cal["step_v"] = rep(oracle.steps(lam_v, bits_v))
+    cal["W"] = int(np.sum(bits_k)) // 32
+    cal["G"] = G
+    return cal

@@ -14,17 +14,23 @@ import bench  # noqa: E402
 
 def test_traffic_only_for_the_measured_decode_source(tmp_path, monkeypatch):
     rec = json.load(open(os.path.join(ROOT, "profiles", "decode_traffic.json")))
-    assert bench._traffic(1) == rec["dram_bytes_per_call"]        # taken on the current decode.cu
     fake = tmp_path / "repo"
     (fake / "profiles").mkdir(parents=True)
-    (fake / "quantized_attention_kv_b300" / "csrc").mkdir(parents=True)
-    shutil.copy(os.path.join(ROOT, "profiles", "decode_traffic.json"), fake / "profiles")
-    src = open(os.path.join(ROOT, "quantized_attention_kv_b300", "csrc", "decode.cu")).read()
-    (fake / "quantized_attention_kv_b300" / "csrc" / "decode.cu").write_text(src)
+    csrc = fake / "quantized_attention_kv_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    srcs = {n: open(os.path.join(ROOT, "quantized_attention_kv_b300", "csrc", n)).read()
+            for n in bench.DECODE_SOURCES}
+    for n, t in srcs.items():
+        (csrc / n).write_text(t)
+    rec["decode_sources_sha256_16"] = bench.decode_source_hash(str(fake))
+    (fake / "profiles" / "decode_traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(fake))
     assert bench._traffic(1) == rec["dram_bytes_per_call"]
-    (fake / "quantized_attention_kv_b300" / "csrc" / "decode.cu").write_text(src + "\n// changed\n")
-    assert bench._traffic(1) is None                              # the kernel changed since
+    for n in bench.DECODE_SOURCES:                                # any of them changed since
+        (csrc / n).write_text(srcs[n] + "\n// changed\n")
+        assert bench._traffic(1) is None, n
+        (csrc / n).write_text(srcs[n])
+        assert bench._traffic(1) == rec["dram_bytes_per_call"]
 
 
 def test_clock_summary(tmp_path):

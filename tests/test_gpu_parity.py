@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import oracle
-from parity_util import ATTN_RTOL, as_u32, attn_rel_err, compare_codes, to_np64
+from parity_util import (ATTN_RTOL, as_u32, attn_rel_err, compare_codes, records, synthetic_calibration,
+                         to_np64, upload)
 from quantized_attention_kv_b300 import aatc, synth
 
 pytestmark = pytest.mark.gpu
@@ -95,16 +96,7 @@ def test_calibration_errors_reported():
 
 
 # ----------------------------------------------------------------- encode
-def _records(cache_t, W, kind, L, start=0):
-    """Records [B][H][L][W] of tokens start.. read from a GPU cache through the oracle's tiling."""
-    c = as_u32(cache_t)
-    Bsz, H = c.shape[:2]
-    c = c.reshape(Bsz, H, -1)
-    out = np.empty((Bsz, H, L, W), dtype=np.uint32)
-    for b in range(Bsz):
-        for h in range(H):
-            out[b, h] = oracle.cache_get(np.ascontiguousarray(c[b, h]), W, kind, L, start)
-    return out
+_records = records
 
 
 @pytest.mark.parametrize("L_new,start,L_cap", [(1024, 0, 1024), (1000, 24, 1056), (1, 7, 32), (129, 0, 160),
@@ -286,10 +278,7 @@ def _oracle_records(wl, ocal, B, L, layer=0):
     return kp, vp
 
 
-def _upload(rec, kind, L_cap):
-    Bsz, H, _, W = rec.shape
-    c = oracle.to_cache(rec, kind, L_cap).view(np.int32).reshape(Bsz, H, L_cap, W)
-    return torch.from_numpy(c).cuda()
+_upload = upload
 
 
 @pytest.mark.parametrize("lens", [[1024], [1, 1024, 0], [127, 129, 1000], [31, 32, 33, 64, 2]])
@@ -316,31 +305,7 @@ def test_decode_matches_oracle_from_identical_codes(lens):
     g.check()
 
 
-def _synthetic_calibration(G, bits_k, bits_v, seed=0):
-    """A calibration with chosen bit allocations (orthogonal transforms from
-    QR, steps from the oracle), to reach every decode path."""
-    rng = np.random.default_rng(seed)
-    d = 128
-    cal = {}
-    Qk, _ = np.linalg.qr(rng.standard_normal((d, d)))
-    Qv, _ = np.linalg.qr(rng.standard_normal((d, d)))
-    lam_k = 0.95 ** np.arange(d)
-    lam_v = 0.93 ** np.arange(d)
-    cal["mu_k"] = rng.standard_normal((1, d))
-    cal["mu_v"] = rng.standard_normal((1, d))
-    cal["T_k"] = Qk.T[None]
-    cal["T_k_inv"] = Qk[None]
-    cal["A_k"] = Qk.T[None]
-    cal["T_v"] = Qv.T[None]
-    cal["U_v"] = Qv[None]
-    cal["lam_k"], cal["lam_v"], cal["lam_q"] = lam_k[None], lam_v[None], np.ones((1, d))
-    cal["bits_k"] = np.asarray(bits_k, dtype=np.int32)[None]
-    cal["bits_v"] = np.asarray(bits_v, dtype=np.int32)[None]
-    cal["step_k"] = oracle.steps(lam_k, bits_k)[None]
-    cal["step_v"] = oracle.steps(lam_v, bits_v)[None]
-    cal["W"] = int(np.sum(bits_k)) // 32
-    cal["G"] = G
-    return cal
+_synthetic_calibration = synthetic_calibration
 
 
 @pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "bits2", "bits4", "bits8"])
@@ -480,18 +445,19 @@ def _end_to_end(wl, sample, layer=0, seq_len=None, bits=None, decode_step=False)
     return worst, ties
 
 
+# every KV head of at least one row is compared in each workload
 def test_end_to_end_llama_32k_with_decode_step():
-    _end_to_end(WL["llama_32k"], sample=[(0, 0), (0, 5)], decode_step=True)
+    _end_to_end(WL["llama_32k"], sample=[(0, h) for h in range(8)], decode_step=True)
 
 
 def test_end_to_end_llama_b16_8k():
-    _end_to_end(WL["llama_b16_8k"], sample=[(0, 0), (15, 7)])
+    _end_to_end(WL["llama_b16_8k"], sample=[(0, h) for h in range(8)] + [(15, 7)])
 
 
 def test_end_to_end_qwen_128k():
-    _end_to_end(WL["qwen_128k"], sample=[(3, 2)])
+    _end_to_end(WL["qwen_128k"], sample=[(3, h) for h in range(4)])
 
 
 @pytest.mark.parametrize("bits", [2.0, 2.75, 4.0])
 def test_end_to_end_stack_layer_budgets(bits):
-    _end_to_end(WL["llama_stack"], sample=[(0, 3)], layer=31, seq_len=4096, bits=bits)
+    _end_to_end(WL["llama_stack"], sample=[(0, h) for h in range(8)], layer=31, seq_len=4096, bits=bits)

@@ -174,3 +174,64 @@ def test_cache_tiling_is_a_permutation_and_round_trips():
         back = oracle.cache_get(c, W, oracle.VALUES, L)
         assert np.array_equal(back[33:36], new)
         assert np.array_equal(back[:33], rec[:33]) and np.array_equal(back[36:], rec[36:])
+
+
+def test_prequant_hand_values():
+    """The pre-rounding value v = c/Delta + (2^b - 1)/2, rounded once to fp32,
+    worked out by hand ("End-to-End Implementation": rotate, then quantize per
+    channel; mid-rise levels), and the code each one gives."""
+    cases = [
+        # c,          step,  b, v (exact),                 code
+        (0.0,         1.596, 1, 0.5,                       0),    # exact fp32 tie -> even (0)
+        (0.8,         1.6,   1, 1.0,                       1),    # 0.8/1.6 in fp64 -> 1.0 after fp32 rounding
+        (0.25,        0.5,   3, 4.0,                       4),
+        (-1.0,        0.5,   3, 1.5,                       2),    # tie -> even (2)
+        (1.0,         0.25,  8, 131.5,                     132),  # tie -> even (132)
+        (-40.0,       0.25,  8, -32.5,                     0),    # below the range: clamped
+        (40.0,        0.25,  8, 287.5,                     255),  # above the range: clamped
+        (1.0 / 3.0,   1.0,   2, np.float32(11.0 / 6.0),    2),    # 11/6 rounded to the nearest fp32
+        (1.0 + 1e-9,  1.0,   2, 2.5,                       2),    # 2.500000001 rounds to fp32 2.5: tie -> 2
+        (5.0,         1.0,   0, 0.0,                       0),    # pruned channel
+    ]
+    for c, s, b, v, u in cases:
+        got = oracle.prequant([c], [s], [b])[0]
+        assert got.dtype == np.float32
+        assert got == np.float32(v), (c, s, b, got, v)
+        assert oracle.quantize([c], [s], [b])[0] == u, (c, s, b)
+    # the fp32 rounding is the one the decision uses: just above a half-integer
+    # in fp64 but equal to it in fp32 rounds to even, just above it in fp32 rounds up
+    up = float(np.nextafter(np.float32(2.5), np.float32(3.0)))
+    assert oracle.prequant([up - 1.5], [1.0], [2])[0] == np.float32(up)
+    assert oracle.quantize([up - 1.5], [1.0], [2])[0] == 3
+
+
+def test_quantize_is_clamped_rint_of_prequant():
+    """quantize(c) == clamp(rint(prequant(c)), 0, 2^b - 1) (half to even) for
+    every width, negative coefficients and values far outside the range."""
+    rng = np.random.default_rng(8)
+    d = 4000
+    bits = rng.integers(0, 9, size=d)
+    step = (0.05 + rng.random(d)).astype(np.float32)
+    top = (1 << bits) - 1
+    c = rng.standard_normal(d) * step * np.maximum(top, 1) * 0.8    # mostly inside the range
+    c[::7] *= 5.0                                                     # some far outside, both signs
+    c[::11] = (rng.integers(-3, 300, size=c[::11].size) + 0.5 - top[::11] / 2.0) * step[::11]  # exact ties
+    pre = oracle.prequant(c, step, bits)
+    u = oracle.quantize(c, step, bits)
+    expect = np.clip(np.rint(pre.astype(np.float64)), 0, top).astype(np.int64)
+    expect[bits == 0] = 0
+    assert np.array_equal(u, expect)
+    assert np.all(pre[bits == 0] == 0)
+    assert np.sum((bits > 0) & (pre - np.floor(pre) == 0.5)) > 100     # ties were exercised
+    # encode reports the same pre-rounding values for the coefficients T (x - mu)
+    dd = 16
+    T = rng.standard_normal((dd, dd))
+    X = rng.standard_normal((50, dd))
+    mu = rng.standard_normal(dd)
+    b16 = np.array([8, 6, 5, 4, 3, 3, 2, 1, 0, 0, 0, 0, 0, 0, 0, 0])   # 32 bits: one record word
+    st16 = (0.1 + rng.random(dd)).astype(np.float32)
+    _, codes, pre_e = oracle.encode(X, T, mu, st16, b16, want_codes=True, want_pre=True)
+    for i in range(50):
+        cc = T @ (X[i] - mu)
+        assert np.array_equal(pre_e[i], oracle.prequant(cc, st16, b16))
+        assert np.array_equal(codes[i], oracle.quantize(cc, st16, b16))

@@ -61,6 +61,54 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
         assert attn_rel_err(got.cpu().numpy(), ref.cpu().numpy()) <= ATTN_RTOL
 
 
+def test_static_scratch_general_path_matches_workspace_decode_twice():
+    """Records of 20 words take the general decode path (query prep, split and
+    combine kernels, with q' and the partials laid out differently in the
+    scratch): two calls in a row of different lengths still match the
+    workspace decode."""
+    f = _static_fn()
+    wl = synth.WORKLOADS["tiny"]
+    k, v, q = synth.calib_inputs(wl, device="cuda")
+    cal = aatc.calibrate(k, v, q, 5.0)
+    assert cal.W == 20
+    B, L = 3, 1024
+    assert 0 < aatc.workspace_size(cal, B, L) <= (4 << 20)
+    kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=L, batch=B)
+    kp = aatc.alloc_cache(cal, B, L)
+    vp = aatc.alloc_cache(cal, B, L)
+    aatc.encode(cal, kc, vc, kp, vp)
+    for step, Lc in ((0, 1024), (1, 300)):
+        qd = synth.query_inputs(wl, device="cuda", batch=B, step=step)
+        ref = aatc.decode_attention(cal, qd, kp, vp, Lc)
+        got = torch.full_like(ref, float("nan"))
+        st = _call_static(f, cal, qd, kp, vp, Lc, None, got)
+        assert st == aatc.OK, aatc.last_error()
+        torch.cuda.synchronize()
+        assert torch.isfinite(got).all()
+        assert attn_rel_err(got.cpu().numpy(), ref.cpu().numpy()) <= ATTN_RTOL, Lc
+
+
+def test_static_scratch_checks_arguments_before_its_size():
+    """Bad arguments get the same status as aatc_decode_attention gives them,
+    not a scratch-size error worked out from them."""
+    f = _static_fn()
+    wl = synth.WORKLOADS["tiny"]
+    k, v, q = synth.calib_inputs(wl, device="cuda")
+    cal = aatc.calibrate(k, v, q, wl.bits)
+    qd = synth.query_inputs(wl, device="cuda")
+    kp = aatc.alloc_cache(cal, 1, 64)
+    out = torch.zeros(1, wl.n_q_heads, 128, device="cuda")
+    st = _call_static(f, cal, qd, kp, kp, 65, None, out)        # L above L_cap
+    assert st == aatc.ERR_CAPACITY and "L_cap" in aatc.last_error()
+    P = ctypes.c_void_p
+    st = f(cal.handle, P(qd.data_ptr()), P(kp.data_ptr()), P(kp.data_ptr()), 64, None, 64, 70000,
+           P(out.data_ptr()), P(torch.cuda.current_stream().cuda_stream))
+    assert st == aatc.ERR_INVALID_ARG and "too large" in aatc.last_error()
+    st = f(cal.handle, P(qd.data_ptr()), None, None, 64, None, 64, 1, P(out.data_ptr()), None)
+    assert st == aatc.ERR_INVALID_ARG and "packed caches" in aatc.last_error()
+    assert torch.all(out == 0)                # nothing was launched
+
+
 def test_static_scratch_rejects_shapes_beyond_its_size():
     f = _static_fn()
     wl = synth.WORKLOADS["tiny"]
