@@ -176,11 +176,11 @@ def run_ours(args, ws, rank, local):
 
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    cal = aatc.calibrate(k_cal, v_cal, q_cal, bits)
+    cal = aatc.calibrate(k_cal, v_cal, q_cal, bits, joint=args.joint)
     torch.cuda.synchronize()
     calib_ms = (time.perf_counter() - t0) * 1e3
-    W = cal.W
-    packed_bytes = 2 * B * Hkv * (L + 1) * W * 4
+    Wk, Wv = cal.W_k, cal.W_v
+    packed_bytes = B * Hkv * (L + 1) * (Wk + Wv) * 4
     # L2 (126 MB) defeat: every call reads its own copy of the packed cache,
     # rotating over enough copies that the working set is several L2 sizes
     n_rot = int(min(64, max(3, -(-3 * L2_BYTES // packed_bytes))))
@@ -190,11 +190,11 @@ def run_ours(args, ws, rank, local):
         bpr = -(-(L + 1) // bt)
         gen = torch.Generator().manual_seed(1234)
         table = torch.randperm(B * bpr + 8, generator=gen)[:B * bpr].reshape(B, bpr).to(torch.int32).to(dev)
-        kps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev) for _ in range(n_rot)]
-        vps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev) for _ in range(n_rot)]
+        kps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev, tensor="k") for _ in range(n_rot)]
+        vps = [aatc.alloc_pool(cal, B * bpr + 8, bt, device=dev, tensor="v") for _ in range(n_rot)]
     else:
-        kps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
-        vps = [aatc.alloc_cache(cal, B, L + 1, device=dev) for _ in range(n_rot)]
+        kps = [aatc.alloc_cache(cal, B, L + 1, device=dev, tensor="k") for _ in range(n_rot)]
+        vps = [aatc.alloc_cache(cal, B, L + 1, device=dev, tensor="v") for _ in range(n_rot)]
 
     def enc(k_, v_, kp, vp, start):
         if args.paged:
@@ -209,7 +209,7 @@ def run_ours(args, ws, rank, local):
             aatc.decode_attention(cal, q_, kp, vp, L + 1, out=out, workspace=wsb)
     out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
     ws_need = aatc.workspace_size(cal, B, L + 1)
-    wsb = torch.empty(max(ws_need, 16), dtype=torch.uint8, device=dev)
+    wsb = aatc.new_workspace(cal, B, L + 1, device=dev)
     for kp, vp in zip(kps, vps):        # every copy holds a valid cache
         enc(kc, vc, kp, vp, 0)
         enc(kn, vn, kp, vp, L)
@@ -269,36 +269,36 @@ def run_ours(args, ws, rank, local):
         _barrier(ws)
         wall = time.perf_counter() - w0
         step_ms_dev = e0.elapsed_time(e1) / args.steps
-        # decode and encode alone (same rotation), for the per-kernel rates
-        reps = max(3, args.steps // n_rot)
-        g_dec.replay()
-        torch.cuda.synchronize()
-        d0, d1 = ev(), ev()
-        d0.record(stream)
-        for _ in range(reps):
-            g_dec.replay()
-        d1.record(stream)
-        g_app.replay()
-        torch.cuda.synchronize()
-        a0, a1 = ev(), ev()
-        a0.record(stream)
-        for _ in range(reps):
-            g_app.replay()
-        a1.record(stream)
-        g_enc.replay()
-        torch.cuda.synchronize()
-        n0, n1 = ev(), ev()
-        n0.record(stream)
-        for _ in range(reps):
-            g_enc.replay()
-        n1.record(stream)
-        torch.cuda.synchronize()
-    dec_call_s = d0.elapsed_time(d1) / 1e3 / (reps * n_rot)
-    enc_call_s = n0.elapsed_time(n1) / 1e3 / (reps * n_rot)
-    app_call_s = _max_over_ranks(a0.elapsed_time(a1) / 1e3 / (reps * n_rot), ws)
+        # decode and encode alone (same rotation), for the per-kernel rates:
+        # each replay of a graph (one call per cache copy) is timed on its own,
+        # at least 200 calls in all; per-call times are replay time / copies
+        reps = max(10, -(-200 // n_rot))
+
+        def timed(g):
+            g.replay()
+            torch.cuda.synchronize()
+            evs = [(ev(), ev()) for _ in range(reps)]
+            for a_, b_ in evs:
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            return sorted(a_.elapsed_time(b_) / 1e3 / n_rot for a_, b_ in evs)
+
+        dec_t = timed(g_dec)
+        app_t = timed(g_app)
+        enc_t = timed(g_enc)
+
+    def pct(v, q):
+        return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+
+    dec_call_s = _max_over_ranks(pct(dec_t, 0.5), ws)
+    enc_call_s = _max_over_ranks(pct(enc_t, 0.5), ws)
+    app_call_s = _max_over_ranks(pct(app_t, 0.5), ws)
     wall = _max_over_ranks(wall, ws)
-    dec_call_s = _max_over_ranks(dec_call_s, ws)
-    enc_call_s = _max_over_ranks(enc_call_s, ws)
+    spread = {name: {"p10_us": round(pct(v, 0.1) * 1e6, 3), "median_us": round(pct(v, 0.5) * 1e6, 3),
+                     "p90_us": round(pct(v, 0.9) * 1e6, 3), "calls": len(v) * n_rot, "replays": len(v)}
+              for name, v in (("decode", dec_t), ("append_decode", app_t), ("encode", enc_t))}
     kp, vp = kps[0], vps[0]
 
     # end to end through the public API with host buffers: H2D of the step's
@@ -319,26 +319,45 @@ def run_ours(args, ws, rank, local):
     qd, knd, vnd = views_d
     outh = torch.empty(out.shape, dtype=torch.float32).pin_memory()
 
-    def e2e_step(evs=None, c=0):
+    def e2e_step(evs=None, c=0, host=None):
         kp, vp = kps[c % n_rot], vps[c % n_rot]
         if evs:
             evs[0].record(stream)
+        t0 = time.perf_counter()
         dbuf.copy_(hbuf, non_blocking=True)
+        t1 = time.perf_counter()
         enc(knd, vnd, kp, vp, L)
+        t2 = time.perf_counter()
         dec(qd, kp, vp)
+        t3 = time.perf_counter()
         outh.copy_(out, non_blocking=True)
+        t4 = time.perf_counter()
         if evs:
             evs[1].record(stream)
+        if host is not None:
+            host["h2d"] += t1 - t0
+            host["append"] += t2 - t1
+            host["decode"] += t3 - t2
+            host["d2h"] += t4 - t3
 
-    for c in range(3):
+    # warm-up, then at least 100 timed steps: the host path reaches a steady
+    # state only after a few dozen calls
+    for c in range(20):
         e2e_step(c=c)
     torch.cuda.synchronize()
-    e2e_evs = [[ev() for _ in range(2)] for _ in range(args.steps)]
-    for s in range(args.steps):
-        e2e_step(e2e_evs[s], c=s)
+    n_e2e = max(100, args.steps)
+    e2e_evs = [[ev() for _ in range(2)] for _ in range(n_e2e)]
+    host = {"h2d": 0.0, "append": 0.0, "decode": 0.0, "d2h": 0.0}
+    w0 = time.perf_counter()
+    for s in range(n_e2e):
+        e2e_step(e2e_evs[s], c=s, host=host)
     torch.cuda.synchronize()
-    e2e_ms = [e[0].elapsed_time(e[1]) for e in e2e_evs]
-    e2e_s = _max_over_ranks(sum(e2e_ms) / 1e3, ws)
+    e2e_wall_us = (time.perf_counter() - w0) / n_e2e * 1e6
+    # host time of each call of the step, averaged over the timed loop; the
+    # device keeps up when their sum is below the device time of a step
+    host = {k_: round(v_ / n_e2e * 1e6, 2) for k_, v_ in host.items()}
+    e2e_ms = sorted(e[0].elapsed_time(e[1]) for e in e2e_evs)
+    e2e_step_s = _max_over_ranks(e2e_ms[len(e2e_ms) // 2] / 1e3, ws)   # median step
     h2d = sum(nbytes_in)
     d2h = out_bytes
 
@@ -361,26 +380,37 @@ def run_ours(args, ws, rank, local):
         "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
         "data": "synthetic (seeded Gaussian KV shaped like the workload; no weights or datasets)",
         "config": {"workload": wl.name, "batch": B, "seq_len": L + 1, "n_q_heads": Hq, "n_kv_heads": Hkv,
-                   "head_dim": 128, "bits_per_element": bits, "record_words": W,
+                   "head_dim": 128, "bits_per_element": bits, "record_words": [Wk, Wv],
+                   "allocation": "joint K/V split" if args.joint else "B bits per tensor",
                    "l2": "defeated by rotation: each call reads its own cache copy, %d copies = %.0f MB > 126 MB L2"
                          % (n_rot, n_rot * packed_bytes / 1e6),
-                   "timing": "CUDA graphs of whole steps replayed K times; CUDA events on the launching stream",
+                   "timing": "CUDA graphs of whole steps replayed K times; decode/encode rates: the median of "
+                             "separately timed graph replays (one call per cache copy, >= 200 calls); CUDA events "
+                             "on the launching stream",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "cache": ("paged, %d-token blocks, shuffled block table" % args.paged) if args.paged
                    else "contiguous"},
         "pct_of_hbm_peak": round(100 * value / ws / peak, 2),
         "encode": {"value": round(B * L * ws / enc_call_s, 1), "unit": "tokens/s",
                    "ms": round(enc_call_s * 1e3, 4),
-                   "gb_s": round((2 * B * Hkv * L * (128 * kc.element_size() + W * 4)) / enc_call_s / 1e9, 2)},
+                   "gb_s": round((B * Hkv * L * (2 * 128 * kc.element_size() + (Wk + Wv) * 4)) / enc_call_s / 1e9,
+                                 2)},
         "decode_us": round(per_launch_s * 1e6, 3),
         "append_decode_us": round(app_call_s * 1e6, 3),
+        "call_times": spread,
         "calibrate_ms": round(calib_ms, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(decode_bytes),
                      "kernel": "decode_attention call (k_decode_fast%s)" % ("" if ws_need == 0 else " + k_decode_combine_fast"),
                      "peak_kind": peak_kind},
-        "e2e": {"value": round(decode_bytes * args.steps * ws / e2e_s / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": round(decode_bytes * ws / e2e_step_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e2e_step_s * 1e6, 2), "wall_us_per_step": round(e2e_wall_us, 2),
+                "steps": n_e2e, "host_us_per_call": host,
+                "what": "median over steps of the device time from before the H2D copy of the step's query "
+                        "and new key/value token (one pinned buffer) to after the D2H copy of the output, "
+                        "through the Python API (append encode, decode attention); calls are enqueued back "
+                        "to back"},
         "gpu_launches": args.steps * (2 * ENCODE_KERNELS_PER_CALL + _decode_kernels_per_call(ws_need)),
         "n_cache_copies": n_rot,
         "clocks": clk.summary(),
@@ -456,6 +486,8 @@ def main():
     ap.add_argument("--seq-len", type=int, default=None)
     ap.add_argument("--bits", type=float, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--joint", action="store_true",
+                    help="calibrate with the joint K/V budget split (attention-aware token weights)")
     ap.add_argument("--paged", type=int, default=0, metavar="BLOCK_TOKENS",
                     help="run the step on paged pools with blocks of this many tokens (32 times a power of two)")
     args = ap.parse_args()

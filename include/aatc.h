@@ -72,6 +72,11 @@ typedef struct {
                                  of 32 and at most 8*128 (e.g. 2.0, 2.75, 4.0) */
     aatc_dtype dtype;         /* element type of every K/V/Q input of this handle */
     int jacobi_max_sweeps;    /* <= 0 selects 50 */
+    int joint_kv;             /* 0: keys and values get B bits each.  Nonzero: the
+                                 pair budget 2B is split between keys and values
+                                 (B_K + B_V = 2B, both multiples of 32, each at
+                                 most 8*128), one split for every KV head, by the
+                                 attention-aware token weights (see aatc_calibrate) */
 } aatc_calib_desc;
 
 /* Calibration ([ABS], [KLT], [RWF], [THM], [NOVA]).
@@ -154,20 +159,24 @@ aatc_status aatc_encode(const aatc_calib *calib, const void *k, const void *v, i
  * q' = (Tk^{-T} q) o Delta_K / sqrt(128) against the codes, values are
  * accumulated in the transform domain and the inverse transform Uv is
  * applied once per head.  workspace: device scratch of at least
- * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned, contents
- * need not be initialized (the call sets up what it needs, on `stream`);
- * calls that share a workspace must be ordered on one stream.  When the rows
- * and KV head groups already fill the GPU, each is one CTA of a single kernel
- * that writes `out` directly (no workspace).  Otherwise two kernels are
- * launched on `stream`: a split kernel that writes one partial result per
- * (row, KV head group, split) to the workspace -- its running softmax
- * maximum and sum, and Uv (Delta_V o sum_i p_i u_i) over its tokens -- and a
- * combine kernel (programmatic dependent launch) that merges the splits and
- * adds mu_v - Uv (Delta_V o mid).  Records above 16 words or layouts whose
- * bytes hold more than four code pieces take a slower general path of three
- * kernels.
+ * aatc_decode_workspace_size(calib, B, L) bytes, caller-owned; it must hold
+ * zeros before its first use (e.g. cudaMemset once when it is allocated),
+ * and every call leaves it ready for the next one, whatever the shape; calls
+ * that share a workspace must be ordered on one stream.  One kernel is
+ * launched on `stream` (as a programmatic dependent of the previous one).
+ * When the rows and KV head groups already fill the GPU, each is one CTA
+ * that writes `out` directly (no workspace).  Otherwise each (row, KV head
+ * group) is split over several CTAs: each leaves a partial result in the
+ * workspace -- its running softmax maximum and sum and
+ * Delta_V o sum_i p_i u_i over its tokens, in the transform domain -- and
+ * counts itself in; the CTA counted in last merges the partials, applies Uv
+ * once per query head, adds mu_v - Uv (Delta_V o mid) and writes `out`.
+ * Records above 16 words or layouts whose bytes hold more than four code
+ * pieces take a slower general path of three kernels.
  * Errors: CAPACITY if L > L_cap; INVALID_ARG if the workspace is too small or
- * L_cap is not a multiple of 32. */
+ * L_cap is not a multiple of 32.  A workspace whose counters were not zero
+ * at entry sets the handle's status (INVALID_ARG from aatc_check); the
+ * output of that call is unspecified. */
 aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q,
                                   const uint32_t *k_packed, const uint32_t *v_packed, int L_cap,
                                   const int32_t *seq_lens, int L, int B, float *out,
@@ -196,8 +205,9 @@ size_t aatc_decode_workspace_size(const aatc_calib *calib, int B, int L);
  *     stream capture.  The address is kept for the life of the process: after
  *     a cudaDeviceReset the library must be unloaded and loaded again before
  *     this entry point is used on that device.
- *   - Every call on a device shares the one array and overwrites what the
- *     previous call left there (nothing in it needs to start at zero).  Calls
+ *   - Every call on a device shares the one array.  The first call on a
+ *     device also clears the array (cudaMemsetAsync on its stream), which
+ *     the split counters need; every call leaves them at zero again.  Calls
  *     that overlap on the GPU -- on different streams, or from several host
  *     threads -- race on it: order them on one stream. */
 aatc_status aatc_decode_attention_static(const aatc_calib *calib, const void *q,
@@ -249,8 +259,28 @@ aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, 
                                         const uint32_t *v_pool, const aatc_pages *pages, const int32_t *seq_lens,
                                         int L, int B, float *out, void *workspace, size_t ws_bytes, void *stream);
 
-/* W = u32 words per token record of one head and tensor (B/32), or -1. */
+/* Testing hook (no counterpart in the method): makes a bounded wait inside
+ * the decode kernels give up, to exercise the TIMEOUT report without
+ * faulting or hanging the GPU.  While skip_tile_copy != 0, every later call
+ * of the fast decode path (contiguous or paged) leaves the first tile copy of
+ * the first warp of its first CTA unissued; that warp's wait for it gives up
+ * after wait_tries tries of at most about 20 us each, the call completes with
+ * an unspecified output, and the handle's status reports AATC_ERR_TIMEOUT
+ * (aatc_check).  Every copy that was issued is still waited for in full
+ * (65,536 tries, about 1.3 s), so nothing is left in flight.
+ * aatc_test_wait_fault(0, 0) restores normal operation.  Process-wide; meant
+ * for tests only.  Always AATC_OK. */
+aatc_status aatc_test_wait_fault(int skip_tile_copy, int wait_tries);
+
+/* W = u32 words per token record of one head (B/32) when keys and values
+ * have the same record width, else -1 (see aatc_record_words_kv). */
 int aatc_record_words(const aatc_calib *calib);
+
+/* Record words of one tensor: tensor 0 = keys (B_K/32), 1 = values (B_V/32);
+ * -1 for a NULL handle or another tensor index.  Key caches hold W_K words
+ * per token, value caches W_V; every layout rule above applies with the
+ * tensor's own W. */
+int aatc_record_words_kv(const aatc_calib *calib, int tensor);
 
 /* Serialize a handle into a caller-owned HOST buffer: a versioned
  * little-endian blob (see aatc_import_calib).  If host_buf is NULL only the
@@ -259,12 +289,13 @@ int aatc_record_words(const aatc_calib *calib);
 aatc_status aatc_export_calib(const aatc_calib *calib, void *host_buf, size_t *bytes);
 
 /* Build a handle from a HOST blob.  Layout: int32 header {magic 0x43544141
- * ("AATC"), version 1, head_dim, n_kv_heads, n_q_heads, B bits, dtype, 0},
+ * ("AATC"), version 2, head_dim, n_kv_heads, n_q_heads, B_K bits, dtype,
+ * B_V bits} (version 1 blobs, whose last word is 0, have B_V = B_K),
  * then for each array below all KV heads in order (H = n_kv_heads, d = 128):
  * f64 mu_k[H][d], mu_v[H][d], T_k[H][d][d], T_k_inv[H][d][d], A_k[H][d][d],
  * T_v[H][d][d], U_v[H][d][d], lam_k[H][d], lam_v[H][d], lam_q[H][d];
  * int32 bits_k[H][d], bits_v[H][d]; f32 step_k[H][d], step_v[H][d].
- * Bits must sum to B per head and tensor, each in 0..8.  Derived device
+ * Bits must sum to B_K (keys) and B_V (values) per head, each in 0..8.  Derived device
  * tables (biases, record layout, decode tables) are rebuilt on the device. */
 aatc_status aatc_import_calib(const void *host_buf, size_t bytes, aatc_calib **out);
 

@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <new>
 
 #include "internal.h"
@@ -14,7 +15,7 @@ namespace {
 thread_local char g_err[512] = "";
 
 constexpr int32_t BLOB_MAGIC = 0x43544141;   // "AATC"
-constexpr int32_t BLOB_VERSION = 1;
+constexpr int32_t BLOB_VERSION = 2;   // version 1 blobs (one budget) still import
 constexpr int D = AATC_D;
 
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
@@ -39,11 +40,11 @@ Layout layout_for(int H)
     L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
     L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
     L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
-              L.plans + L.dblob + L.f32_vec + L.t3 + L.cols + 1024;
+              L.plans + L.dblob + L.f32_vec + L.t3 + L.cols + 1024 + 2 * L.f64_vec;
     return L;
 }
 
-aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib **out)
+aatc_status new_handle(int Hkv, int Hq, int Bk, int Bv, aatc_dtype dtype, aatc_calib **out)
 {
     aatc_calib *h = new (std::nothrow) aatc_calib();
     if (!h) return aatc_fail(AATC_ERR_INVALID_ARG, "out of host memory");
@@ -51,8 +52,12 @@ aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib 
     h->Hkv = Hkv;
     h->Hq = Hq;
     h->G = Hq / Hkv;
-    h->Bbits = Bbits;
-    h->W = Bbits / 32;
+    h->Bk = Bk;
+    h->Bv = Bv;
+    h->Wk = Bk / 32;
+    h->Wv = Bv / 32;
+    h->Bpair = Bk + Bv;
+    h->joint = false;
     h->dtype = dtype;
     Layout L = layout_for(Hkv);
     cudaError_t e = cudaMalloc(&h->arena, L.total);
@@ -87,6 +92,8 @@ aatc_status new_handle(int Hkv, int Hq, int Bbits, aatc_dtype dtype, aatc_calib 
     p = (char *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);   // T3: TMA source, keep it well aligned
     h->T3 = take(L.t3);
     h->enc_cols = (EncCol *)take(L.cols);
+    h->alpha = (double *)take(L.f64_vec);    // [H][2] (fits: H * 128 doubles)
+    h->split = (int32_t *)take(256);
     h->status = (uint32_t *)take(256);
     e = cudaMemset(h->status, 0, sizeof(uint32_t));
     if (e != cudaSuccess) { cudaFree(h->arena); delete h; return aatc_cuda_fail(e, "cudaMemset"); }
@@ -101,6 +108,9 @@ aatc_status status_from_device(uint32_t st)
         return aatc_fail(AATC_ERR_NO_CONVERGENCE, "Jacobi eigensolver did not converge");
     if (st & AATC_DEV_TIMEOUT)
         return aatc_fail(AATC_ERR_TIMEOUT, "a kernel gave up waiting for its own copies; results are invalid");
+    if (st & AATC_DEV_WORKSPACE)
+        return aatc_fail(AATC_ERR_INVALID_ARG,
+                         "a decode workspace was not zeroed before its first use (its split counters were not 0)");
     if (st & AATC_DEV_RANGE)
         return aatc_fail(AATC_ERR_CAPACITY, "a cache position or block table entry was out of range (access skipped)");
     return AATC_OK;
@@ -153,6 +163,25 @@ aatc_status aatc_cuda_fail(cudaError_t e, const char *what)
     return aatc_fail(AATC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+aatc_status kernel_smem_limit(const void *kern, size_t bytes)
+{
+    // one entry per (device, kernel): the attribute is raised once, and again
+    // only for a larger size, so launches on the hot path make no runtime call
+    static struct { int dev; const void *k; size_t set; } seen[64];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    AATC_CUDA(cudaGetDevice(&dev));
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    while (i < used && !(seen[i].k == kern && seen[i].dev == dev)) ++i;
+    if (i < used && seen[i].set >= bytes) return AATC_OK;
+    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
+    if (i == used && used < 64) seen[used++] = {dev, kern, 0};
+    if (i < used) seen[i].set = bytes;
+    return AATC_OK;
+}
+
 extern "C" {
 
 const char *aatc_last_error(void) { return g_err; }
@@ -181,8 +210,9 @@ aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const
     cudaStream_t s = (cudaStream_t)stream;
 
     aatc_calib *h = nullptr;
-    st = new_handle(desc->n_kv_heads, desc->n_q_heads, Bbits, desc->dtype, &h);
+    st = new_handle(desc->n_kv_heads, desc->n_q_heads, Bbits, Bbits, desc->dtype, &h);
     if (st != AATC_OK) return st;
+    h->joint = desc->joint_kv != 0;
     void *work = nullptr;
     size_t wb = calib_work_bytes(desc->n_kv_heads, desc->n_q_heads, desc->n_calib_tokens);
     cudaError_t e = cudaMalloc(&work, wb);
@@ -195,6 +225,15 @@ aatc_status aatc_calibrate(const aatc_calib_desc *desc, const void *k_cal, const
         if (e != cudaSuccess) st = aatc_cuda_fail(e, "calibration");
     } else {
         cudaStreamSynchronize(s);
+    }
+    if (st == AATC_OK && h->joint) {   // the split chosen on the device sets the record widths
+        int32_t sp[2] = {0, 0};
+        e = cudaMemcpy(sp, h->split, sizeof(sp), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) st = aatc_cuda_fail(e, "cudaMemcpy(split)");
+        h->Bk = sp[0];
+        h->Bv = sp[1];
+        h->Wk = sp[0] / 32;
+        h->Wv = sp[1] / 32;
     }
     cudaFree(work);
     if (st == AATC_OK) st = status_from_device(dev);
@@ -335,7 +374,13 @@ aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, 
     return decode_run(calib, q, k_pool, v_pool, m, seq_lens, L, B, out, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
-int aatc_record_words(const aatc_calib *calib) { return calib ? calib->W : -1; }
+int aatc_record_words(const aatc_calib *calib) { return calib && calib->Wk == calib->Wv ? calib->Wk : -1; }
+
+int aatc_record_words_kv(const aatc_calib *calib, int tensor)
+{
+    if (!calib || (tensor != 0 && tensor != 1)) return -1;
+    return tensor ? calib->Wv : calib->Wk;
+}
 
 aatc_status aatc_export_calib(const aatc_calib *calib, void *host_buf, size_t *bytes)
 {
@@ -346,7 +391,7 @@ aatc_status aatc_export_calib(const aatc_calib *calib, void *host_buf, size_t *b
     if (!host_buf) { *bytes = need; return AATC_OK; }
     if (*bytes < need) return aatc_fail(AATC_ERR_INVALID_ARG, "buffer of %zu bytes required", need);
     AATC_CUDA(cudaDeviceSynchronize());
-    int32_t hdr[8] = {BLOB_MAGIC, BLOB_VERSION, D, calib->Hkv, calib->Hq, calib->Bbits, (int32_t)calib->dtype, 0};
+    int32_t hdr[8] = {BLOB_MAGIC, BLOB_VERSION, D, calib->Hkv, calib->Hq, calib->Bk, (int32_t)calib->dtype, calib->Bv};
     char *p = (char *)host_buf;
     memcpy(p, hdr, sizeof(hdr));
     p += sizeof(hdr);
@@ -372,13 +417,13 @@ aatc_status aatc_import_calib(const void *host_buf, size_t bytes, aatc_calib **o
     if (bytes < 8 * sizeof(int32_t)) return aatc_fail(AATC_ERR_INVALID_ARG, "blob too short");
     int32_t hdr[8];
     memcpy(hdr, host_buf, sizeof(hdr));
-    if (hdr[0] != BLOB_MAGIC || hdr[1] != BLOB_VERSION)
-        return aatc_fail(AATC_ERR_INVALID_ARG, "not an AATC calibration blob (version 1)");
+    if (hdr[0] != BLOB_MAGIC || (hdr[1] != 1 && hdr[1] != BLOB_VERSION))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "not an AATC calibration blob (version 1 or 2)");
     if (hdr[2] != D) return aatc_fail(AATC_ERR_UNSUPPORTED, "head_dim must be 128");
-    const int H = hdr[3], Hq = hdr[4], Bbits = hdr[5];
+    const int H = hdr[3], Hq = hdr[4], Bk = hdr[5], Bv = hdr[1] == 1 ? hdr[5] : hdr[7];
     if (H < 1 || Hq < H || Hq % H || Hq / H > AATC_MAX_G)
         return aatc_fail(AATC_ERR_INVALID_ARG, "bad head counts in blob");
-    if (Bbits <= 0 || Bbits % 32 || Bbits > AATC_MAXB * D)
+    if (Bk <= 0 || Bk % 32 || Bk > AATC_MAXB * D || Bv <= 0 || Bv % 32 || Bv > AATC_MAXB * D)
         return aatc_fail(AATC_ERR_UNSUPPORTED, "bad bit budget in blob");
     if (hdr[6] != AATC_F32 && hdr[6] != AATC_BF16) return aatc_fail(AATC_ERR_INVALID_ARG, "bad dtype");
     if (bytes < blob_bytes(H)) return aatc_fail(AATC_ERR_INVALID_ARG, "blob truncated");
@@ -395,10 +440,10 @@ aatc_status aatc_import_calib(const void *host_buf, size_t bytes, aatc_calib **o
             sk += a;
             sv += b;
         }
-        if (sk != Bbits || sv != Bbits) return aatc_fail(AATC_ERR_INVALID_ARG, "bits do not sum to the budget");
+        if (sk != Bk || sv != Bv) return aatc_fail(AATC_ERR_INVALID_ARG, "bits do not sum to the budget");
     }
     aatc_calib *h = nullptr;
-    aatc_status st = new_handle(H, Hq, Bbits, (aatc_dtype)hdr[6], &h);
+    aatc_status st = new_handle(H, Hq, Bk, Bv, (aatc_dtype)hdr[6], &h);
     if (st != AATC_OK) return st;
     void *dsts[] = {h->mu_k, h->mu_v, h->T_k, h->T_k_inv, h->A_k, h->T_v, h->U_v, h->lam_k, h->lam_v,
                     h->lam_q, h->bits_k, h->bits_v, h->step_k, h->step_v};

@@ -428,8 +428,44 @@ const StepTable &step_table()
     return t;
 }
 
+// Exact top-B selection for one (head, tensor) by one block of 1024 threads;
+// thread t owns gain g = lam_j 4^{-(t%8)} of channel j = t/8 and ends with
+// nb[j] = b_j.  Every thread returns its gain.
+__device__ double topB_alloc(const double *lam, int B, double *gain, int *nb, unsigned long long *mx)
+{
+    const int t = threadIdx.x;
+    const int j = t >> 3, tb = t & 7;
+    const double g = ldexp(fmax(lam[j], 0.0), -2 * tb);
+    gain[t] = g;
+    if (t < D) nb[t] = 0;
+    if (t == 0) *mx = 0ull;
+    __syncthreads();
+    atomicMax(mx, (unsigned long long)__double_as_longlong(g));
+    __syncthreads();
+    long long lo = 0, hi = (long long)*mx + 1;   // count(g >= 0) = all >= B > 0 = count(g >= hi)
+    while (hi - lo > 1) {
+        long long mid = lo + (hi - lo) / 2;
+        int c = __syncthreads_count(g >= __longlong_as_double(mid));
+        if (c >= B) lo = mid; else hi = mid;
+    }
+    const double gstar = __longlong_as_double(lo);
+    const int above = __syncthreads_count(g > gstar);
+    bool take = g > gstar;
+    if (g == gstar) {
+        int before = 0;
+        for (int k = 0; k < t; ++k) before += (gain[k] == gstar);
+        take = (above + before) < B;
+    }
+    if (take) atomicAdd(&nb[j], 1);
+    __syncthreads();
+    return g;
+}
+
+// Budget B (0 < B <= 8 D) of tensor `tensor` (0 = keys): from the joint split
+// chosen on the device when given, else the handle's own.
 __global__ void __launch_bounds__(1024) k_waterfill(const double *__restrict__ lam_k,
-                                                    const double *__restrict__ lam_v, int Bbits,
+                                                    const double *__restrict__ lam_v, int Bk, int Bv,
+                                                    const int32_t *__restrict__ split,
                                                     int32_t *__restrict__ bits_k, int32_t *__restrict__ bits_v,
                                                     float *__restrict__ step_k, float *__restrict__ step_v,
                                                     StepTable steps)
@@ -440,37 +476,268 @@ __global__ void __launch_bounds__(1024) k_waterfill(const double *__restrict__ l
     __shared__ unsigned long long mx;
     const int h = blockIdx.x, tensor = blockIdx.y, t = threadIdx.x;
     const double *lam = (tensor == 0 ? lam_k : lam_v) + h * D;
-    const int j = t >> 3, tb = t & 7;
-    const double g = ldexp(fmax(lam[j], 0.0), -2 * tb);
-    gain[t] = g;
+    const int B = split ? split[tensor] : (tensor == 0 ? Bk : Bv);
     if (t <= AATC_MAXB) s_tab[t] = steps.s[t];
-    if (t < D) nb[t] = 0;
-    if (t == 0) mx = 0ull;
-    __syncthreads();
-    atomicMax(&mx, (unsigned long long)__double_as_longlong(g));
-    __syncthreads();
-    long long lo = 0, hi = (long long)mx + 1;   // count(g >= 0) = all >= B > 0 = count(g >= hi)
-    while (hi - lo > 1) {
-        long long mid = lo + (hi - lo) / 2;
-        int c = __syncthreads_count(g >= __longlong_as_double(mid));
-        if (c >= Bbits) lo = mid; else hi = mid;
-    }
-    const double gstar = __longlong_as_double(lo);
-    const int above = __syncthreads_count(g > gstar);
-    bool take = g > gstar;
-    if (g == gstar) {
-        int before = 0;
-        for (int k = 0; k < t; ++k) before += (gain[k] == gstar);
-        take = (above + before) < Bbits;
-    }
-    if (take) atomicAdd(&nb[j], 1);
-    __syncthreads();
+    topB_alloc(lam, B, gain, nb, &mx);
     if (t < D) {
         int b = nb[t];
         (tensor == 0 ? bits_k : bits_v)[h * D + t] = b;
         float st = b > 0 ? (float)(s_tab[b] * sqrt(fmax(lam[t], 0.0))) : 0.0f;
         (tensor == 0 ? step_k : step_v)[h * D + t] = st;
     }
+}
+
+// Attention-aware token weights of each KV head ("Theorem: Additive Error
+// Decomposition": value noise is weighted by A_i^2, key noise by
+// A_i^2 |v_i - o|^2 and the query metric, which the key transform already
+// holds):
+//   alpha_V = mean_q sum_i A_qi^2,   alpha_K = mean_q (1/d) sum_i A_qi^2 |v_i - o_q|^2
+// over the G N calibration queries of the head's group, each attending all N
+// calibration keys of the head with the 1/sqrt(d) scale, no mask.  With
+// e_i = 2^(s_i - m) (online maximum m), l = sum e, L2 = sum e^2,
+// a = sum e v, a2 = sum e^2 v, n2 = sum e^2 |v|^2 (values centred by their
+// calibration mean, which leaves v_i - o unchanged):
+//   sum_i A_i^2 = L2 / l^2,
+//   sum_i A_i^2 |v_i - o|^2 = (n2 - 2 (a . a2) / l + |a|^2 L2 / l^2) / l^2.
+// One CTA per (64 queries, KV head); fp32 inside a query, fp64 across queries.
+// Thread (tq, tk) scores queries 4tq.. against keys 4tk.. of a 64-key tile and
+// then accumulates a and a2 of queries 4tq.. over channels 8tk.. .
+constexpr int AQ = 64, AKT = 64, ATH = 256;
+constexpr int QP = AQ + 4, KP = AKT + 4;   // padded rows of the transposed tiles (fewer bank conflicts)
+constexpr size_t ALPHA_SMEM = (size_t)(D * QP + D * KP + AKT * D + AKT * AQ + AKT) * sizeof(float);
+
+template <typename T>
+__device__ __forceinline__ float ld_f32(const T *p) { return (float)to_f64(*p); }
+
+template <typename T>
+__global__ void __launch_bounds__(ATH) k_alpha(const T *__restrict__ k_cal, const T *__restrict__ v_cal,
+                                               const T *__restrict__ q_cal, const double *__restrict__ mu_v, int N,
+                                               int G, double *__restrict__ part)
+{
+    extern __shared__ __align__(16) float asm_[];
+    float *Qt = asm_;                 // [D][QP]   queries, transposed
+    float *Kt = Qt + D * QP;          // [D][KP]   keys, transposed
+    float *Vs = Kt + D * KP;          // [AKT][D]  values minus their mean
+    float *Pt = Vs + AKT * D;         // [AKT][AQ] e of (key, query)
+    float *vn = Pt + AKT * AQ;        // [AKT]     |v|^2
+    __shared__ double red[2][ATH / 32];
+    const int h = blockIdx.y, qb = blockIdx.x, tid = threadIdx.x;
+    const int tq = tid >> 4, tk = tid & 15;
+    const long nq = (long)G * N;
+    const float sc = 1.4426950408889634f / sqrtf((float)D);   // log2(e) / sqrt(d)
+    // queries of this block: query n of the group is row n % N of query head h G + n / N
+    for (int e = tid; e < AQ * D; e += ATH) {
+        const int qi = e / D, kd = e % D;
+        const long n = (long)qb * AQ + qi;
+        float x = 0.f;
+        if (n < nq) x = ld_f32(q_cal + ((size_t)(h * G + n / N) * N + n % N) * D + kd);
+        Qt[kd * QP + qi] = x;
+    }
+    float m[4], l[4], L2[4], n2[4], a[4][8], a2[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        m[r] = -INFINITY;
+        l[r] = L2[r] = n2[r] = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) a[r][c8] = a2[r][c8] = 0.f;
+    }
+    const T *Kh = k_cal + (size_t)h * N * D;
+    const T *Vh = v_cal + (size_t)h * N * D;
+    for (int k0 = 0; k0 < N; k0 += AKT) {
+        __syncthreads();   // the previous tile is used up
+        for (int e = tid; e < AKT * D; e += ATH) {
+            const int ki = e / D, kd = e % D;
+            const bool in = k0 + ki < N;
+            Kt[kd * KP + ki] = in ? ld_f32(Kh + (size_t)(k0 + ki) * D + kd) : 0.f;
+            Vs[ki * D + kd] = in ? (float)(to_f64(Vh[(size_t)(k0 + ki) * D + kd]) - mu_v[h * D + kd]) : 0.f;
+        }
+        __syncthreads();
+        if (tid < AKT) {
+            float s2 = 0.f;
+            for (int kd = 0; kd < D; ++kd) s2 = fmaf(Vs[tid * D + kd], Vs[tid * D + kd], s2);
+            vn[tid] = s2;
+        }
+        // scores of queries 4tq.. x keys 4tk.., log2 domain
+        float sv[4][4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) sv[r][c4] = 0.f;
+#pragma unroll 4
+        for (int kd = 0; kd < D; ++kd) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(&Qt[kd * QP + 4 * tq]);
+            const float4 k4 = *reinterpret_cast<const float4 *>(&Kt[kd * KP + 4 * tk]);
+            const float qq[4] = {q4.x, q4.y, q4.z, q4.w}, kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) sv[r][c4] = fmaf(qq[r], kk[c4], sv[r][c4]);
+        }
+        __syncthreads();   // vn is ready
+        float f[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                sv[r][c4] = k0 + 4 * tk + c4 < N ? sv[r][c4] * sc : -INFINITY;
+                tmax = fmaxf(tmax, sv[r][c4]);
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+            const float mn = fmaxf(m[r], tmax);
+            f[r] = m[r] == -INFINITY ? 0.f : exp2f(m[r] - mn);
+            m[r] = mn;
+            float ls = 0.f, l2s = 0.f, n2s = 0.f;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const float e = exp2f(sv[r][c4] - mn);
+                sv[r][c4] = e;
+                ls += e;
+                l2s = fmaf(e, e, l2s);
+                n2s = fmaf(e * e, vn[4 * tk + c4], n2s);
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                ls += __shfl_xor_sync(0xffffffffu, ls, o);
+                l2s += __shfl_xor_sync(0xffffffffu, l2s, o);
+                n2s += __shfl_xor_sync(0xffffffffu, n2s, o);
+            }
+            l[r] = fmaf(l[r], f[r], ls);
+            L2[r] = fmaf(L2[r], f[r] * f[r], l2s);
+            n2[r] = fmaf(n2[r], f[r] * f[r], n2s);
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<float4 *>(&Pt[(4 * tk + c4) * AQ + 4 * tq]) =
+                make_float4(sv[0][c4], sv[1][c4], sv[2][c4], sv[3][c4]);
+        __syncthreads();
+        // a, a2 of queries 4tq.. over channels 8tk..
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                a[r][c8] *= f[r];
+                a2[r][c8] *= f[r] * f[r];
+            }
+        const int kn = min(AKT, N - k0);
+        for (int ki = 0; ki < kn; ++ki) {
+            const float4 p4 = *reinterpret_cast<const float4 *>(&Pt[ki * AQ + 4 * tq]);
+            const float4 va = *reinterpret_cast<const float4 *>(&Vs[ki * D + 8 * tk]);
+            const float4 vb = *reinterpret_cast<const float4 *>(&Vs[ki * D + 8 * tk + 4]);
+            const float pp[4] = {p4.x, p4.y, p4.z, p4.w};
+            const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float e2 = pp[r] * pp[r];
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    a[r][c8] = fmaf(pp[r], vv[c8], a[r][c8]);
+                    a2[r][c8] = fmaf(e2, vv[c8], a2[r][c8]);
+                }
+            }
+        }
+    }
+    // per query: a . a2 and |a|^2 over the channels (16 threads per query group)
+    double av = 0.0, ak = 0.0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        float d1 = 0.f, d2 = 0.f;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+            d1 = fmaf(a[r][c8], a2[r][c8], d1);
+            d2 = fmaf(a[r][c8], a[r][c8], d2);
+        }
+#pragma unroll
+        for (int o = 1; o < 16; o <<= 1) {
+            d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+            d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+        }
+        const long n = (long)qb * AQ + 4 * tq + r;
+        if (tk == 0 && n < nq && l[r] > 0.f) {
+            const double ld = l[r], il2 = 1.0 / (ld * ld);
+            av += (double)L2[r] * il2;
+            ak += ((double)n2[r] - 2.0 * (double)d1 / ld + (double)d2 * (double)L2[r] * il2) * il2 / D;
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        av += __shfl_xor_sync(0xffffffffu, av, o);
+        ak += __shfl_xor_sync(0xffffffffu, ak, o);
+    }
+    if ((tid & 31) == 0) {
+        red[0][tid >> 5] = ak;
+        red[1][tid >> 5] = av;
+    }
+    __syncthreads();
+    if (tid < 2) {
+        double sum = 0.0;
+        for (int w = 0; w < ATH / 32; ++w) sum += red[tid][w];
+        part[((size_t)h * gridDim.x + qb) * 2 + tid] = sum;
+    }
+}
+
+// alpha[h][t] = sum over the query blocks / (G N).
+__global__ void k_alpha_reduce(const double *__restrict__ part, int nqb, long nq, double *__restrict__ alpha)
+{
+    const int h = blockIdx.x, t = threadIdx.x;
+    if (t >= 2) return;
+    double s = 0.0;
+    for (int b = 0; b < nqb; ++b) s += part[((size_t)h * nqb + b) * 2 + t];
+    alpha[h * 2 + t] = s / (double)nq;
+}
+
+// Joint K/V budget split ("Theorem: Additive Error Decomposition" weights,
+// "Optimal Bit Allocation via Reverse Water-Filling" over both tensors): for
+// every word-aligned split B_K + B_V = Bpair (each 32..8 D) the exact top-B
+// allocation of each head and tensor, and its distortion sum_j lam_j 4^{-b_j}.
+// One block per (split, head, tensor).
+__global__ void __launch_bounds__(1024) k_split_cost(const double *__restrict__ lam_k,
+                                                     const double *__restrict__ lam_v, int Bk0, int Bpair,
+                                                     double *__restrict__ cost)
+{
+    __shared__ double gain[D * AATC_MAXB];
+    __shared__ int nb[D];
+    __shared__ unsigned long long mx;
+    __shared__ double red[32];
+    const int c = blockIdx.x, h = blockIdx.y, tensor = blockIdx.z, t = threadIdx.x;
+    const int H = gridDim.y;
+    const int Bk = Bk0 + 32 * c, B = tensor == 0 ? Bk : Bpair - Bk;
+    const double *lam = (tensor == 0 ? lam_k : lam_v) + h * D;
+    topB_alloc(lam, B, gain, nb, &mx);
+    double v = t < D ? ldexp(fmax(lam[t], 0.0), -2 * nb[t]) : 0.0;
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((t & 31) == 0) red[t >> 5] = v;
+    __syncthreads();
+    if (t < 32) {
+        v = red[t];
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (t == 0) cost[((size_t)c * H + h) * 2 + tensor] = v;
+    }
+}
+
+// The split of least sum_h alpha_Kh cost_K + alpha_Vh cost_V over the heads
+// (ties to the split nearest Bpair / 2, then the smaller B_K) -> split[0] =
+// B_K, split[1] = B_V.  One thread.
+__global__ void k_split_pick(const double *__restrict__ cost, const double *__restrict__ alpha, int n_cand, int H,
+                             int Bk0, int Bpair, int32_t *__restrict__ split)
+{
+    int best = -1;
+    double best_c = 0.0;
+    for (int c = 0; c < n_cand; ++c) {
+        double tot = 0.0;
+        for (int h = 0; h < H; ++h)
+            tot += alpha[h * 2 + 0] * cost[((size_t)c * H + h) * 2 + 0] +
+                   alpha[h * 2 + 1] * cost[((size_t)c * H + h) * 2 + 1];
+        const int Bk = Bk0 + 32 * c;
+        const bool better = best < 0 || tot < best_c ||
+                            (tot == best_c && abs(2 * Bk - Bpair) < abs(2 * (Bk0 + 32 * best) - Bpair));
+        if (better) {
+            best = c;
+            best_c = tot;
+        }
+    }
+    split[0] = Bk0 + 32 * best;
+    split[1] = Bpair - split[0];
 }
 
 // ---------------------------------------------------------------------------
@@ -644,7 +911,38 @@ aatc_status calib_run(aatc_calib *h, const void *k_cal, const void *v_cal, const
     k_gemm64<<<gg, 256, 0, s>>>(Si, 0, nullptr, DIAG_NONE, Uq, 0, h->T_k_inv);
     k_transpose64<<<gg, 256, 0, s>>>(h->U_v, h->T_v);
     AATC_CUDA(cudaGetLastError());
-    k_waterfill<<<dim3(H, 2), 1024, 0, s>>>(h->lam_k, h->lam_v, h->Bbits, h->bits_k, h->bits_v,
+    const int32_t *split = nullptr;
+    if (h->joint) {
+        // joint allocation: the token weights of the calibration attention, then
+        // the word-aligned split of the pair budget (each tensor 32 .. 8 D bits)
+        // of least weighted distortion over the heads; the moment partials'
+        // scratch is free by now
+        const int nqb = (G * N + AQ - 1) / AQ;
+        double *apart = partial;
+        double *cost = apart + (size_t)H * nqb * 2;
+        const int Bk0 = h->Bpair - AATC_MAXB * D > 32 ? h->Bpair - AATC_MAXB * D : 32;
+        const int Bk1 = h->Bpair - 32 < AATC_MAXB * D ? h->Bpair - 32 : AATC_MAXB * D;
+        if (Bk1 < Bk0) return aatc_fail(AATC_ERR_UNSUPPORTED, "pair budget of %d bits cannot be split", h->Bpair);
+        const int n_cand = (Bk1 - Bk0) / 32 + 1;
+        if (h->dtype == AATC_BF16) {
+            st = kernel_smem_limit((const void *)k_alpha<__nv_bfloat16>, ALPHA_SMEM);
+            if (st != AATC_OK) return st;
+            k_alpha<__nv_bfloat16><<<dim3(nqb, H), ATH, ALPHA_SMEM, s>>>(
+                (const __nv_bfloat16 *)k_cal, (const __nv_bfloat16 *)v_cal, (const __nv_bfloat16 *)q_cal, h->mu_v, N,
+                G, apart);
+        } else {
+            st = kernel_smem_limit((const void *)k_alpha<float>, ALPHA_SMEM);
+            if (st != AATC_OK) return st;
+            k_alpha<float><<<dim3(nqb, H), ATH, ALPHA_SMEM, s>>>((const float *)k_cal, (const float *)v_cal,
+                                                               (const float *)q_cal, h->mu_v, N, G, apart);
+        }
+        k_alpha_reduce<<<H, 32, 0, s>>>(apart, nqb, (long)G * N, h->alpha);
+        k_split_cost<<<dim3(n_cand, H, 2), 1024, 0, s>>>(h->lam_k, h->lam_v, Bk0, h->Bpair, cost);
+        k_split_pick<<<1, 1, 0, s>>>(cost, h->alpha, n_cand, H, Bk0, h->Bpair, h->split);
+        AATC_CUDA(cudaGetLastError());
+        split = h->split;
+    }
+    k_waterfill<<<dim3(H, 2), 1024, 0, s>>>(h->lam_k, h->lam_v, h->Bk, h->Bv, split, h->bits_k, h->bits_v,
                                             h->step_k, h->step_v, step_table());
     AATC_CUDA(cudaGetLastError());
     return calib_derive(h, s);

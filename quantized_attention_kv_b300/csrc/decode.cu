@@ -12,24 +12,25 @@
 // each packed record is streamed once.
 //
 // Fast path (record words <= 16, at most 4 code pieces per record byte):
-//   k_decode_fast   one persistent CTA per SM over a balanced share of all
-//                   (batch row, KV head, head group, 32-token tile) work.  Per
-//                   segment it computes q' for the head group and expands it
-//                   to one fp16 hi/lo weight per record piece in mma.sync
-//                   B-fragment order; each warp streams its own tiles into
-//                   shared memory with cp.async.bulk, unpacks pieces with one
-//                   AND per two fp16 operands, runs scores and P.V on mma.sync
-//                   (fp16 hi/lo operands, fp32 accumulation) with an exp2
-//                   online softmax; warps merge by log-sum-exp into one
-//                   partial per segment.
-//   k_decode_combine_fast  per (batch row, KV head, head group), launched
-//                   with programmatic dependent launch: merges the partials
-//                   and applies Uv once per head.
+//   k_decode_fast   one CTA per SM, each over a contiguous range of 32-token
+//                   tiles of one (batch row, KV head, head group).  It
+//                   computes q' for the head group and expands it to one fp16
+//                   hi/lo weight per record piece in mma.sync B-fragment
+//                   order; each warp streams its own tiles into shared memory
+//                   with cp.async.bulk (evict-first in L2), unpacks pieces
+//                   with one AND per two fp16 operands, runs scores and P.V on
+//                   mma.sync (fp16 hi/lo operands, fp32 accumulation) with an
+//                   exp2 online softmax; the warps merge by log-sum-exp.  A
+//                   unit split over several CTAs leaves one partial per split
+//                   (in the transform domain) and the split counted in last
+//                   merges them; either way Uv is applied once per head, by
+//                   one CTA, and the output written.
 // General path (any shape): one thread per token, codes read by offset.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -63,6 +64,13 @@ constexpr int FAST_MAX_W = 16;
 constexpr int PROW = 4 + D;      // floats per partial: m, l, 2 pad, acc[D] (acc 16-byte aligned)
 constexpr int PSH = 6;           // P operands carry p * 2^PSH
 constexpr float RESCALE_T = 8.f; // the running maximum is raised once a score exceeds it by this (log2)
+// Workspace of a call with several splits per unit: split counters (one per
+// unit; units number fewer than the CTAs, so at most MAX_COUNTED) at offset 0,
+// where every call finds them, then the partial slots.
+constexpr int MAX_COUNTED = 256;
+constexpr int MERGE_MIN_SLOTS = 16;   // the merge stages at least this many partial slots at a time
+constexpr int SCR_CBAR = 256;    // epilogue: c [D][8] starts this many floats into the scratch (after the warp maxima and sums)
+constexpr size_t WS_COUNTERS = MAX_COUNTED * sizeof(unsigned);
 
 // Work split: every (batch row, KV head, head group) is a "unit" of
 // n_tiles = ceil(L/32) tiles, cut into S = max(1, resident CTAs / units)
@@ -82,25 +90,27 @@ struct FastGeom {
     int units;       // B * Hkv * HG
     int S;           // splits (CTAs, partial slots) per unit
     int tiles_per;   // tiles per split
-    size_t stage_bytes, stage_region, uv_off, part_off, smem, ws_total;
+    size_t stage_bytes, stage_region, smem, ws_total;
     bool single;     // one split per unit: the split kernel writes the output itself
 };
 
 // Shared memory of k_decode_fast, in carve order.
 struct FastSmem {
     size_t stages, mat, blob, qtab, pbuf, mbar, scr, total;
-    size_t uv_off, part_off;
 };
 
-FastSmem fast_smem_layout(int FW, int FST, int W, int NT, int ksteps, int groups)
+// Wkv = W_K + W_V: words of one token's key and value records together.
+FastSmem fast_smem_layout(int FW, int FST, int Wkv, int NT, int ksteps, int groups)
 {
     FastSmem m;
     const int HPG = 4 * NT;
-    const size_t tiles = (size_t)FW * FST * 256 * W;
-    // epilogue: the warps' piece sums, then Delta_V o channel sums [D][8], partial outputs [4][8][D]
-    m.uv_off = ((size_t)FW * 64 * groups * HPG * 4 + 127) & ~(size_t)127;
-    m.part_off = m.uv_off + (size_t)D * 8 * 4 + (size_t)4 * 8 * D * 4;   // the split's partial (single split)
-    const size_t epi_region = m.part_off + (size_t)HPG * PROW * 4;
+    const size_t tiles = (size_t)FW * FST * 128 * Wkv;
+    // epilogue in the stage region: the warps' piece sums (packed when a warp's
+    // own stages are too small), later the unit's partial slots (merge) and
+    // the k-quarter partial outputs [4][8][D]
+    size_t epi_region = (size_t)FW * 64 * groups * HPG * 4;
+    if (epi_region < (size_t)4 * 8 * D * 4) epi_region = (size_t)4 * 8 * D * 4;
+    if (epi_region < (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4) epi_region = (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4;
     m.stages = tiles > epi_region ? tiles : epi_region;
     m.mat = (size_t)D * D * 4;   // A_k^T, then Uv^T
     m.blob = sizeof(DecBlob);
@@ -108,7 +118,7 @@ FastSmem fast_smem_layout(int FW, int FST, int W, int NT, int ksteps, int groups
     m.pbuf = (size_t)FW * 8 * NT * PSTRIDE * 2;
     m.mbar = (((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15;
     const size_t pro = ((size_t)D * 8 + (size_t)HPG * D) * 4;   // query rows, q'
-    const size_t epi = (size_t)2 * FW * HPG * 4;                 // warp maxima and sums
+    const size_t epi = ((size_t)SCR_CBAR + D * 8) * 4;           // warp maxima and sums, then c [D][8]
     m.scr = pro > epi ? pro : epi;
     m.total = m.stages + m.mat + m.blob + m.qtab + m.pbuf + m.mbar + m.scr;
     return m;
@@ -123,24 +133,22 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.NT = h->G <= 4 ? 1 : 2;
     f.HPG = 4 * f.NT;
     f.HG = (h->G + f.HPG - 1) / f.HPG;
-    f.rows = (h->W + 3) / 4;
-    f.groups = (2 * h->W + 7) / 8;
+    f.rows = (h->Wk + 3) / 4;
+    f.groups = (2 * h->Wv + 7) / 8;
     f.GMAX = f.groups <= 2 ? 2 : (f.groups <= 3 ? 3 : 4);
     f.FW = f.NT == 2 ? 12 : 16;
     f.ksteps = 4 * f.rows;
     f.FST = 3;
-    FastSmem m = fast_smem_layout(f.FW, f.FST, h->W, f.NT, f.ksteps, f.groups);
+    FastSmem m = fast_smem_layout(f.FW, f.FST, h->Wk + h->Wv, f.NT, f.ksteps, f.groups);
     if (m.total > (size_t)sm_limit_bytes()) {
         f.FST = 2;
-        m = fast_smem_layout(f.FW, f.FST, h->W, f.NT, f.ksteps, f.groups);
+        m = fast_smem_layout(f.FW, f.FST, h->Wk + h->Wv, f.NT, f.ksteps, f.groups);
     }
     f.smem = m.total;
     f.stage_region = m.stages;
-    f.uv_off = m.uv_off;
-    f.stage_bytes = (size_t)256 * h->W;
+    f.stage_bytes = (size_t)128 * (h->Wk + h->Wv);
     f.n_tiles = L > 0 ? (L + TILE - 1) / TILE : 0;
     f.units = B * h->Hkv * f.HG;
-    f.part_off = m.part_off;
     const int per_sm = fast_ctas_per_sm(f.GMAX, f.NT, f.FW, f.smem);
     const int C = sm_count() * per_sm;
     f.S = C / f.units > 1 ? C / f.units : 1;
@@ -149,11 +157,11 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.single = f.n_tiles > 0 && f.S == 1;
     f.tiles_per = f.n_tiles > 0 ? (f.n_tiles + f.S - 1) / f.S : 1;
     f.S = f.n_tiles > 0 ? (f.n_tiles + f.tiles_per - 1) / f.tiles_per : 1;
-    f.ws_total = f.single ? 0 : (((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255;
+    f.ws_total = f.single ? 0 : WS_COUNTERS + ((((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255);
     return f;
 }
 
-bool fast_ok(const aatc_calib *h) { return h->W <= FAST_MAX_W && h->fast_layout; }
+bool fast_ok(const aatc_calib *h) { return h->Wk <= FAST_MAX_W && h->Wv <= FAST_MAX_W && h->fast_layout; }
 
 // ---- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -173,12 +181,13 @@ __device__ __forceinline__ void mbar_arrive_expect(uint64_t *mb, uint32_t bytes)
 }
 
 // Bounded wait of a whole warp on a phase of an mbarrier: false (on every
-// lane) if it did not complete within the iteration limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *mb, uint32_t parity)
+// lane) if it did not complete within `tries` tries.
+constexpr int WAIT_TRIES = 1 << 16;   // about 1.3 s
+__device__ __forceinline__ bool mbar_wait(uint64_t *mb, uint32_t parity, int tries = WAIT_TRIES)
 {
     const uint32_t a = smem_u32(mb);
     // each try may suspend the thread for up to ~20 us until the phase completes
-    for (int it = 0; it < (1 << 16); ++it) {
+    for (int it = 0; it < tries; ++it) {
         uint32_t done;
         asm volatile(
             "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
@@ -197,6 +206,25 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(mb))
+        : "memory");
+}
+
+// L2 policy for data read once per call (the packed cache): evicted first, so
+// that what every call reuses -- the kernels' code, the handle's tables, the
+// query and the partials -- stays in L2 while the cache streams through it.
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *mb, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(mb)), "l"(pol)
         : "memory");
 }
 
@@ -242,10 +270,8 @@ struct FastArgs {
     const uint32_t *kp, *vp;
     const int32_t *seq_lens;
     CacheMap map;           // contiguous or paged cache
-    int L, W, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;
+    int L, Wk, Wv, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;   // Wk / Wv: record words
     uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
-    uint32_t uv_off;        // epilogue: offset of the channel sums in the stage region (after the warp sums)
-    uint32_t part_off;      // epilogue: offset of this split's partial in shared memory (single split)
     int single;             // one split per unit (S = 1): finish here and write out
     float *out;             // [B][Hq][D] (single split)
     const float *vcst;      // [Hkv][D] mu_v - Uv (Delta_V o mid) (single split)
@@ -254,7 +280,11 @@ struct FastArgs {
     const void *q;          // [B][Hq][D] of the handle's dtype
     const float *AkT;       // [Hkv][D][D]
     float *part;            // [units][S][HPG][PROW]
+    unsigned *counter;      // [units] splits counted in so far (0 between calls)
+    int merge_slots;        // partial slots the stage region holds at a time (the merge)
     uint32_t *status;
+    int wait_tries;         // test hook: limit of the wait for the copy left unissued
+    int skip_first_copy;    // test hook: CTA 0, warp 0 leaves its first tile copy unissued
 };
 
 // One CTA = one split of one unit.  Every warp streams its own tiles
@@ -274,13 +304,13 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
     constexpr int HPG = 4 * NT;
-    asm volatile("griddepcontrol.launch_dependents;");   // the combine kernel may start its prologue
+    asm volatile("griddepcontrol.launch_dependents;");   // the next kernel on the stream may start its prologue
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int g = lane >> 2, c = lane & 3;
-    const int W = a.W, rows = a.rows, groups = a.groups, FST = a.FST;
+    const int Wk = a.Wk, Wv = a.Wv, rows = a.rows, groups = a.groups, FST = a.FST;
     const int ksteps = rows * 4;
-    const uint32_t SB = 256u * W, tile_bytes = 128u * W;
+    const uint32_t SB = 128u * (Wk + Wv), kbytes = 128u * Wk, vbytes = 128u * Wv;   // stage = K tile, V tile
 
     // shared memory carve-up (as in fast_smem_layout)
     unsigned char *stage_base = smem;
@@ -299,7 +329,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     const int b = u / (a.Hkv * a.HG), h = (u / a.HG) % a.Hkv, hg = u % a.HG;
     const int ta = sp * a.tiles_per, tb = min(ta + a.tiles_per, a.n_tiles);
     constexpr bool paged = PAGED;
-    const size_t slab = paged ? 0 : ((size_t)b * a.Hkv + h) * (size_t)a.map.L_cap * W;
+    // first tile of this (row, KV head) in a contiguous cache, in tiles of 32 tokens
+    const size_t slab_t = paged ? 0 : ((size_t)b * a.Hkv + h) * (size_t)(a.map.L_cap / TILE);
     uint64_t *my_mbar = mbar + warp * FST;
     uint64_t *blob_bar = mbar + FW * FST;
     uint64_t *mat_bar = blob_bar + 1;   // phase 0: A_k^T, phase 1: Uv^T
@@ -347,33 +378,41 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         if (tr + FW < tb) r1 = trow[(tr + FW) >> sh];
         if (tr + 2 * FW < tb) r2 = trow[(tr + 2 * FW) >> sh];
     }
-    // word offset of a tile of this (row, KV head) in the pool (block 0 for a bad entry)
-    auto pool_word = [&](int blk, int tile) -> size_t {
+    // tile index (in 32-token tiles) of a tile of this (row, KV head) in the pool
+    // (block 0 for a bad entry); a tile's words start at 32 W times it
+    auto pool_tile = [&](int blk, int tile) -> size_t {
         if (blk < 0 || blk >= a.map.n_blocks) {
             bad_blk = true;
             blk = 0;
         }
-        return ((((size_t)blk * a.Hkv + h) << sh) + (size_t)(tile & ((1 << sh) - 1))) * TILE * W;
+        return (((size_t)blk * a.Hkv + h) << sh) + (size_t)(tile & ((1 << sh) - 1));
     };
-    // query rows of the head group: element e = (head e / D, k = e % D)
+    // query rows of the head group: element e = (head e / D, k = e % D), loaded
+    // as raw bits ahead of the tile burst and converted after it, so that no
+    // thread waits for them before issuing its copies
     constexpr int QPER = (HPG * D + NTH - 1) / NTH;
-    float qv[QPER];
+    uint32_t qraw[QPER];
     {
-        const QT *qg = reinterpret_cast<const QT *>(a.q);
         const int Hq = a.Hkv * a.G;
 #pragma unroll
         for (int r = 0; r < QPER; ++r) {
             const int e = tid + r * NTH, gi = hg * HPG + (e >> 7);
-            qv[r] = (e < HPG * D && gi < a.G) ? to_f32(qg[((size_t)b * Hq + h * a.G + gi) * D + (e & (D - 1))]) : 0.f;
+            const size_t idx = ((size_t)b * Hq + h * a.G + gi) * D + (e & (D - 1));
+            qraw[r] = 0u;
+            if (e < HPG * D && gi < a.G) {
+                if (sizeof(QT) == 2) qraw[r] = reinterpret_cast<const unsigned short *>(a.q)[idx];
+                else qraw[r] = reinterpret_cast<const uint32_t *>(a.q)[idx];
+            }
         }
     }
     const int len = a.seq_lens ? min(max(a.seq_lens[b], 0), a.L) : a.L;
 
-    auto issue = [&](size_t word, int s) {
+    const uint64_t stream_pol = evict_first_policy();
+    auto issue = [&](size_t tidx, int s) {   // tile tidx of the cache (K and V) into stage s
         unsigned char *dst = my_stage + s * SB;
-        mbar_arrive_expect(&my_mbar[s], 2 * tile_bytes);
-        bulk_g2s(dst, a.kp + word, tile_bytes, &my_mbar[s]);
-        bulk_g2s(dst + tile_bytes, a.vp + word, tile_bytes, &my_mbar[s]);
+        mbar_arrive_expect(&my_mbar[s], kbytes + vbytes);
+        bulk_g2s_hint(dst, a.kp + tidx * TILE * Wk, kbytes, &my_mbar[s], stream_pol);
+        bulk_g2s_hint(dst + kbytes, a.vp + tidx * TILE * Wv, vbytes, &my_mbar[s], stream_pol);
     };
     // The warp's n-th tile goes through stage n % FST and completes phase
     // n / FST of that stage's barrier.  In a contiguous cache the first tiles
@@ -381,28 +420,39 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // tb are inside the cache); copies past the row's length are drained at
     // the end.  In a paged cache only tiles inside the row are requested.
     int n_issued = 0, n_done = 0;
+    // test hook (aatc_test_wait_fault): this warp's first copy is never issued,
+    // so its wait for it runs out (after a.wait_tries tries) and reports TIMEOUT
+    const bool hook = a.skip_first_copy && blockIdx.x == 0 && warp == 0;
     int st_next = 0;          // stage of the next tile to consume
     uint32_t ph_next = 0;     // its barrier phase parity
-    if (!paged) {
+    const int t1 = min(tb, (len + TILE - 1) / TILE);
+    // first copies of stages [i0, i1): the copy engine takes requests one at
+    // a time, so the issuing lane waits while the CTA's requests queue up;
+    // stage 0 goes out before the query weights are built, the rest after
+    auto burst = [&](int i0, int i1) {
 #pragma unroll
         for (int i = 0; i < 3; ++i) {   // FST <= 3
             const int tile = ta + warp + i * FW;
-            if (i < FST && tile < tb) {
-                if (lane == 0) issue(slab + (size_t)tile * TILE * W, i);
+            if (i < i0 || i >= i1) continue;
+            if (!paged && tile < tb) {
+                if (lane == 0 && !(hook && i == 0)) issue(slab_t + (size_t)tile, i);
+                ++n_issued;
+            }
+            if (paged && tile < t1) {
+                if (lane == 0 && !(hook && i == 0)) issue(pool_tile(ent[i], tile), i);
                 ++n_issued;
             }
         }
-    }
-    const int t1 = min(tb, (len + TILE - 1) / TILE);
-    if (paged) {
+    };
+    burst(0, 1);
+
+    float qv[QPER];
 #pragma unroll
-        for (int i = 0; i < 3; ++i) {
-            const int tile = ta + warp + i * FW;
-            if (i < FST && tile < t1) {
-                if (lane == 0) issue(pool_word(ent[i], tile), i);
-                ++n_issued;
-            }
-        }
+    for (int r = 0; r < QPER; ++r) {
+        uint32_t x;   // bf16 or fp32 bits -> fp32 bits; asm volatile keeps it (the load's first use) after the burst
+        if (sizeof(QT) == 2) asm volatile("shl.b32 %0, %1, 16;" : "=r"(x) : "r"(qraw[r]));
+        else asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(qraw[r]));
+        qv[r] = __uint_as_float(x);
     }
 
     // ---- query weights of the head group: q' = (A_k q) o Delta_K / sqrt(d),
@@ -448,7 +498,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             for (int i = 0; i < HPG; ++i) red[(ks * HPG + i) * D + j] = o[i];
         }
         __syncthreads();
-        // A_k^T is used up: Uv^T for the epilogue comes into the same buffer
+        // A_k^T is used up: Uv^T comes into the same buffer for the split that
+        // finishes the unit (the only one, or whichever is counted in last)
         if (tid == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
@@ -503,6 +554,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 #pragma unroll
         for (int t = 0; t < NT; ++t) sc[t] = LOG2E * pow2i(24 - s_exp(4 * t + c));
     }
+    burst(1, FST);
     __syncthreads();
 
     float m_run[NT], l_run[NT];
@@ -525,7 +577,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         const int tile = ta + warp + it * FW;
         if (tile >= t1) break;
         const int s = st_next;
-        if (!mbar_wait(&my_mbar[s], ph_next)) {
+        if (!mbar_wait(&my_mbar[s], ph_next, (hook && n_done == 0) ? a.wait_tries : WAIT_TRIES)) {
             failed = true;
             break;
         }
@@ -535,7 +587,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             ph_next ^= 1u;
         }
         const uint32_t *Kt = reinterpret_cast<const uint32_t *>(my_stage + s * SB);
-        const uint32_t *Vt = Kt + TILE * W;
+        const uint32_t *Vt = Kt + TILE * Wk;
 
         // ---- scores: C[hf][r & 1] rows g / g+8 = tokens 16 hf + 2g / +1, columns 2c / 2c+1 =
         // head c hi / lo; two chains per half-tile (even and odd key rows)
@@ -551,14 +603,14 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             if (r >= rows) break;
-            const int nr = min(4, W - 4 * r);
+            const int nr = min(4, Wk - 4 * r);
             const uint4 mA = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][0]);
             const uint4 mB = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][4]);
             const uint32_t mk[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
             uint32_t x0[2], x1[2], y0[2], y1[2];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                const uint2 kw = *reinterpret_cast<const uint2 *>(Kt + hf * 16 * W + 64 * r + g * 2 * nr + 2 * c);
+                const uint2 kw = *reinterpret_cast<const uint2 *>(Kt + hf * 16 * Wk + 64 * r + g * 2 * nr + 2 * c);
                 x0[hf] = kw.x;
                 x1[hf] = kw.y;
                 y0[hf] = kw.x >> 8;
@@ -680,13 +732,13 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             if (lane == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 if (paged) {
-                    issue(pool_word(r0, nt), s);
+                    issue(pool_tile(r0, nt), s);
                     r0 = r1;
                     r1 = r2;
                     const int nn = nt + 3 * FW;   // three refills ahead
                     r2 = nn < t1 ? trow[nn >> sh] : 0;
                 } else {
-                    issue(slab + (size_t)nt * TILE * W, s);
+                    issue(slab_t + (size_t)nt, s);
                 }
             }
             ++n_issued;
@@ -697,7 +749,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     if (failed && lane == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
     if (bad_blk) atomicOr(a.status, AATC_DEV_RANGE);
     for (; n_done < n_issued; ++n_done) {
-        if (!mbar_wait(&my_mbar[st_next], ph_next)) failed = true;
+        // (the copy the test hook left unissued has nothing to drain)
+        if (!(hook && n_done == 0) && !mbar_wait(&my_mbar[st_next], ph_next)) failed = true;
         if (++st_next == FST) {
             st_next = 0;
             ph_next ^= 1u;
@@ -708,16 +761,18 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         for (int t = 0; t < NT; ++t) { m_run[t] = -INFINITY; l_run[t] = 0.f; }
     }
 
-    // ---- merge the warps in piece space, gather the pieces into channels and
-    // leave the transform domain for this split: y_i = Uv (Delta_V o sum_t p_it u_t)
-    // (the midpoint and mu_v terms are the same for every split: the combine adds them)
+    // ---- merge the warps in piece space and gather the pieces into channels:
+    // c_i = Delta_V o sum_t p_it u_t, still in the transform domain.  A unit with
+    // several splits leaves (m, l, c) per query head in its partial slot and the
+    // combine kernel applies Uv once per head; a unit with a single split
+    // applies Uv here.
     const int rows_tot = 64 * groups;
     float *wm = scr;                                          // [FW][HPG]
     float *wl = wm + FW * HPG;                                // [FW][HPG]
-    float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG]
+    float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG], warp stride wstride
     const float *UT = mat_s;                                  // [D][D] Uv^T (prefetched)
-    float *cbarT = reinterpret_cast<float *>(stage_base + a.uv_off);   // [D][8] Delta_V o channel sums
-    float *red = cbarT + D * 8;                               // [4][8][D] k-quarter partial outputs
+    float *cbarT = scr + SCR_CBAR;                            // [D][8] Delta_V o channel sums
+    float *red = reinterpret_cast<float *>(stage_base);       // [4][8][D] k-quarter partial outputs (after the gather)
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         float l = l_run[t];
@@ -729,43 +784,46 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             wl[warp * HPG + 4 * t + c] = l;
         }
     }
-    __syncthreads();   // every warp is out of its loop: the stages are free
+    // the warps' piece sums (unscaled, each against its own running maximum):
+    // in the warp's own stages when they hold them (the warp is done with them),
+    // else packed over all stages once every warp is out of its loop
+    const bool own = (size_t)rows_tot * HPG * 4 <= (size_t)FST * SB;
+    const int wstride = own ? (int)(FST * SB / 4) : rows_tot * HPG;   // floats between warps
+    if (!own) __syncthreads();
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int i = 4 * t + c;
-        float M = -INFINITY;
-#pragma unroll 4
-        for (int w = 0; w < FW; ++w) M = fmaxf(M, wm[w * HPG + i]);
-        const float f = m_run[t] == -INFINITY ? 0.f : ex2(m_run[t] - M);
 #pragma unroll
         for (int gr = 0; gr < GMAX; ++gr) {
             if (gr >= groups) break;
 #pragma unroll
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int row = (gr * 4 + m4) * 16 + g;
-                wacc[((size_t)warp * rows_tot + row) * HPG + i] = acc[gr][m4][t][0] * f;
-                wacc[((size_t)warp * rows_tot + row + 8) * HPG + i] = acc[gr][m4][t][1] * f;
+                wacc[(size_t)warp * wstride + row * HPG + i] = acc[gr][m4][t][0];
+                wacc[(size_t)warp * wstride + (row + 8) * HPG + i] = acc[gr][m4][t][1];
             }
         }
     }
-    if (warp < HPG) {   // warp i: maximum and sum of head i over the warps (FW <= 32)
-        const int i = warp;
-        const float mw = lane < FW ? wm[lane * HPG + i] : -INFINITY;
-        float M = mw;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float Ls = mw == -INFINITY ? 0.f : wl[lane * HPG + i] * ex2(mw - M);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-        if (lane == 0) {
-            cm[i] = M;
-            cl[i] = Ls;
-        }
-    }
-    __syncthreads();
-    // channel sums sum_t p_t u_tj (both sides carry 2^PSH), times Delta_V,j
+    // a wait that gave up in any warp invalidates the whole split
+    failed = __syncthreads_or(failed);
+    // thread (head i, channel j): merge the warps by log-sum-exp and gather the
+    // channel's pieces: c_ij = Delta_V,j sum_w 2^(m_w - M) sum_t p_t u_tj
+    // (both sides carry 2^PSH), straight to the partial slot (several splits)
+    // or to shared memory (the unit's only split); l likewise
+    float *Pg = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
     for (int e = tid; e < HPG * D; e += NTH) {
         const int i = e >> 7, j = e & (D - 1);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < FW; ++w) M = fmaxf(M, wm[w * HPG + i]);
+        float f[FW];
+        float Ls = 0.f;
+#pragma unroll
+        for (int w = 0; w < FW; ++w) {
+            const float mw = wm[w * HPG + i];
+            f[w] = mw == -INFINITY ? 0.f : ex2(mw - M);
+            Ls = fmaf(wl[w * HPG + i], f[w], Ls);
+        }
         float v = 0.f;
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
@@ -773,17 +831,103 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             if (vg >= 0) {
                 const float *src = wacc + (size_t)(vg & 255) * HPG + i;
                 float s0 = 0.f, s1 = 0.f;
-                int w = 0;
-                for (; w + 2 <= FW; w += 2) {
-                    s0 += src[(size_t)w * rows_tot * HPG];
-                    s1 += src[(size_t)(w + 1) * rows_tot * HPG];
+#pragma unroll
+                for (int w = 0; w < FW; w += 2) {
+                    s0 = fmaf(f[w], src[(size_t)w * wstride], s0);
+                    if (w + 1 < FW) s1 = fmaf(f[w + 1], src[(size_t)(w + 1) * wstride], s1);
                 }
-                if (w < FW) s0 += src[(size_t)w * rows_tot * HPG];
                 // fp16 operands: piece * 2^(p - 24); piece * 2^ex is the code part
                 v = fmaf(s0 + s1, pow2i((vg >> 8) - 64 + 24), v);
             }
         }
-        cbarT[j * 8 + i] = v * blob_s->vstep[j];
+        v *= blob_s->vstep[j];
+        if (a.single) {
+            cbarT[j * 8 + i] = v;
+            if (j == 0) cl[i] = Ls;
+        } else {
+            Pg[i * PROW + 4 + j] = failed ? 0.f : v;
+            if (j < 4) Pg[i * PROW + j] = j == 0 ? (failed ? -INFINITY : M) : j == 1 ? (failed ? 0.f : Ls) : 0.f;
+        }
+    }
+    if (!a.single) {
+        // count this split in (the partial is visible device-wide first); the
+        // split counted in last merges the unit and puts the counter back to 0
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned old = atomicAdd(a.counter + u, 1u);
+            if (old >= (unsigned)a.S) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
+            mxi[0] = old == (unsigned)(a.S - 1);
+        }
+        __syncthreads();
+        if (!mxi[0]) {
+            mbar_wait(mat_bar, 1);   // (long landed) no copy may be in flight when the CTA exits
+            return;
+        }
+        __threadfence();
+        if (tid == 0) a.counter[u] = 0u;
+        // merge, once per head: c = sum_s 2^(m_s - M) c_s and l likewise.  The
+        // unit's partial slots are contiguous: chunks of up to merge_slots of
+        // them come into the stages, every thread loading its share at once
+        // from L2 (ld.global.cg: no stale L1 line), one round trip per chunk;
+        // thread (head i, channel j) merges from shared memory, rescaling its
+        // running sums between chunks.
+        constexpr int EPT = (HPG * D + NTH - 1) / NTH;
+        float Mr[EPT], ar[EPT], lr[EPT];
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+            Mr[q] = -INFINITY;
+            ar[q] = 0.f;
+            lr[q] = 0.f;
+        }
+        const float *Pu = a.part + (size_t)u * a.S * HPG * PROW;
+        float *Ps = reinterpret_cast<float *>(stage_base);
+        for (int c0 = 0; c0 < a.S; c0 += a.merge_slots) {
+            const int n = min(a.merge_slots, a.S - c0);
+            const int nq = n * HPG * PROW / 4;   // float4 of the chunk
+            const float4 *src4 = reinterpret_cast<const float4 *>(Pu + (size_t)c0 * HPG * PROW);
+            for (int k = tid; k < nq; k += NTH) reinterpret_cast<float4 *>(Ps)[k] = __ldcg(src4 + k);
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < EPT; ++q) {
+                const int e = tid + q * NTH;
+                if (e >= HPG * D) break;
+                const int i = e >> 7, j = e & (D - 1);
+                const float *pi = Ps + i * PROW;
+                const int sstep = HPG * PROW;
+                float M = Mr[q];
+                for (int s2 = 0; s2 < n; ++s2) M = fmaxf(M, pi[s2 * sstep]);
+                const float r = Mr[q] == -INFINITY ? 0.f : ex2(Mr[q] - M);
+                float a0 = ar[q] * r, a1 = 0.f, l0 = lr[q] * r, l1 = 0.f;
+                int s2 = 0;
+                for (; s2 + 2 <= n; s2 += 2) {
+                    const float m0 = pi[s2 * sstep], m1 = pi[(s2 + 1) * sstep];
+                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
+                    a1 = fmaf(w1, pi[(s2 + 1) * sstep + 4 + j], a1);
+                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
+                    l1 = fmaf(w1, pi[(s2 + 1) * sstep + 1], l1);
+                }
+                if (s2 < n) {
+                    const float m0 = pi[s2 * sstep];
+                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
+                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
+                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
+                }
+                Mr[q] = M;
+                ar[q] = a0 + a1;
+                lr[q] = l0 + l1;
+            }
+            __syncthreads();   // the chunk's stage is refilled by the next one
+        }
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+            const int e = tid + q * NTH;
+            if (e >= HPG * D) break;
+            const int i = e >> 7, j = e & (D - 1);
+            cbarT[j * 8 + i] = ar[q];
+            if (j == 0) cl[i] = lr[q];
+        }
     }
     __syncthreads();
     if (!mbar_wait(mat_bar, 1)) failed = true;
@@ -812,142 +956,23 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         }
     }
     __syncthreads();
-    {
-        float *P = a.single ? reinterpret_cast<float *>(stage_base + a.part_off)
-                               : a.part + ((size_t)u * a.S + sp) * HPG * PROW;
-        for (int e = tid; e < HPG * D; e += NTH) {
-            const int i = e >> 7, j = e & (D - 1);
-            const float y = (red[(0 * 8 + i) * D + j] + red[(1 * 8 + i) * D + j]) +
-                            (red[(2 * 8 + i) * D + j] + red[(3 * 8 + i) * D + j]);
-            P[i * PROW + 4 + j] = failed ? 0.f : y;
-        }
-        if (tid < HPG) {
-            P[tid * PROW + 0] = failed ? -INFINITY : cm[tid];
-            P[tid * PROW + 1] = failed ? 0.f : cl[tid];
-            P[tid * PROW + 2] = 0.f;
-            P[tid * PROW + 3] = 0.f;
-        }
-    }
-    if (!a.single) return;
-
-    // ---- the unit's only split: o = y / l + (mu_v - Uv (Delta_V o mid))
-    __syncthreads();
+    // ---- o = Uv c / l + (mu_v - Uv (Delta_V o mid)), once per head
     {
         const int Hq = a.Hkv * a.G;
-        const float *P = reinterpret_cast<const float *>(stage_base + a.part_off);
         for (int e = tid; e < HPG * D; e += NTH) {
             const int i = e >> 7, j = e & (D - 1), gi = hg * HPG + i;
-            const float Ls = P[i * PROW + 1];
+            const float y = (red[(0 * 8 + i) * D + j] + red[(1 * 8 + i) * D + j]) +
+                            (red[(2 * 8 + i) * D + j] + red[(3 * 8 + i) * D + j]);
+            const float Ls = cl[i];
             if (gi < a.G)
                 a.out[((size_t)b * Hq + h * a.G + gi) * D + j] =
-                    Ls > 0.f ? P[i * PROW + 4 + j] / Ls + a.vcst[h * D + j] : 0.f;
+                    (Ls > 0.f && !failed) ? y / Ls + a.vcst[h * D + j] : 0.f;
         }
-    }
-}
-
-// Merge the splits of one unit:
-//   o = sum_s w_s y_s / sum_s w_s l_s + (mu_v - Uv (Delta_V o mid)),  w_s = 2^(m_s - M)
-// where y_s = Uv (Delta_V o sum_t p_t u_t) over split s.  Launched after
-// k_decode_fast with programmatic dependent launch.  The unit's partial slots
-// are contiguous: they come in by bulk copies of up to CS slots, and each
-// slot's weight is kept in its spare word 2.  The code is a few short loops
-// (it runs once per launch, from a cold instruction cache).
-constexpr int CB_THREADS = 512;
-constexpr size_t CB_STAGE_BYTES = 96 * 1024;
-int cb_chunk(int HPG) { return (int)(CB_STAGE_BYTES / ((size_t)HPG * PROW * 4)); }
-size_t cb_smem(int S, int HPG)
-{
-    const int cs = cb_chunk(HPG);
-    return (size_t)(S < cs ? S : cs) * HPG * PROW * 4;
-}
-__global__ void __launch_bounds__(CB_THREADS) k_decode_combine_fast(
-    const float *__restrict__ part, int S, int CS, int Hkv, int G, int HG, int HPG,
-    const float *__restrict__ vcst, float *__restrict__ out, uint32_t *status)
-{
-    extern __shared__ __align__(128) float Ps[];           // [CS][HPG][PROW]
-    __shared__ float Mh[8], Lh[8], Rh[8];
-    __shared__ uint64_t bar;
-    // the next kernel may start its prologue; it waits for this grid before touching shared data
-    asm volatile("griddepcontrol.launch_dependents;");
-    const int u = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int b = u / (Hkv * HG), h = (u / HG) % Hkv, hg = u % HG;
-    const float cst = vcst[h * D + (tid & (D - 1))];
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (tid < 8) {
-        Mh[tid] = -INFINITY;
-        Lh[tid] = 0.f;
-    }
-    __syncthreads();
-    asm volatile("griddepcontrol.wait;" ::: "memory");   // partials of k_decode_fast
-
-    const float *Pu = part + (size_t)u * S * HPG * PROW;
-    float A[2] = {0.f, 0.f};   // pairs e = tid + q CB_THREADS: head e / D, channel e % D
-    bool ok = true;
-    for (int c0 = 0, k = 0; c0 < S; c0 += CS, ++k) {
-        const int n = min(CS, S - c0);
-        if (tid == 0) {
-            const uint32_t bytes = (uint32_t)((size_t)n * HPG * PROW * 4);
-            mbar_arrive_expect(&bar, bytes);
-            bulk_g2s(Ps, Pu + (size_t)c0 * HPG * PROW, bytes, &bar);
-        }
-        ok = mbar_wait(&bar, (uint32_t)(k & 1)) && ok;
-        if (warp < HPG) {   // warp i: running maximum and sum of head i, slot weights
-            const int i = warp;
-            float mc = -INFINITY;
-            for (int s = lane; s < n; s += 32) mc = fmaxf(mc, Ps[(s * HPG + i) * PROW]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
-            const float Mo = Mh[i], M = fmaxf(Mo, mc);
-            float Lc = 0.f;
-            for (int s = lane; s < n; s += 32) {
-                float *P = Ps + (s * HPG + i) * PROW;
-                const float w = P[0] == -INFINITY ? 0.f : ex2(P[0] - M);
-                P[2] = w;
-                Lc = fmaf(P[1], w, Lc);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Lc += __shfl_xor_sync(0xffffffffu, Lc, o);
-            __syncwarp();
-            if (lane == 0) {
-                const float r = Mo == -INFINITY ? 0.f : ex2(Mo - M);
-                Rh[i] = r;
-                Lh[i] = Lh[i] * r + Lc;
-                Mh[i] = M;
-            }
-        }
-        __syncthreads();
-        for (int q = 0; q < 2; ++q) {
-            const int e = tid + q * CB_THREADS;
-            if (e >= HPG * D) break;
-            const int i = e >> 7, j = e & (D - 1);
-            float a0 = A[q] * Rh[i], a1 = 0.f;
-            const float *P = Ps + i * PROW;
-            int s = 0;
-            for (; s + 2 <= n; s += 2) {
-                a0 = fmaf(P[(s * HPG) * PROW + 2], P[(s * HPG) * PROW + 4 + j], a0);
-                a1 = fmaf(P[((s + 1) * HPG) * PROW + 2], P[((s + 1) * HPG) * PROW + 4 + j], a1);
-            }
-            if (s < n) a0 = fmaf(P[(s * HPG) * PROW + 2], P[(s * HPG) * PROW + 4 + j], a0);
-            A[q] = a0 + a1;
-        }
-        __syncthreads();   // the stage is refilled by the next chunk
-    }
-    if (!ok && tid == 0) atomicOr(status, AATC_DEV_TIMEOUT);
-    const int Hq = Hkv * G;
-    for (int q = 0; q < 2; ++q) {
-        const int e = tid + q * CB_THREADS;
-        if (e >= HPG * D) break;
-        const int i = e >> 7, j = e & (D - 1), gi = hg * HPG + i;
-        const float Ls = Lh[i];   // j = tid % D: cst is channel j's
-        if (gi < G) out[((size_t)b * Hq + h * G + gi) * D + j] = (Ls > 0.f && ok) ? A[q] / Ls + cst : 0.f;
     }
 }
 
 // Per-head fast-decoder tables from the plans and codec tables.
-__global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs, int W,
+__global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs, int Wk, int Wv,
                             const double *__restrict__ Uv, const double *__restrict__ muv, DecBlob *__restrict__ out,
                             float *__restrict__ vcst)
 {
@@ -964,18 +989,18 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
         vcst[(size_t)h * D + j] = (float)acc;
     }
     DecBlob &o = out[h];
-    const int rows_tot = 64 * ((2 * W + 7) / 8);
+    const int rows_tot = 64 * ((2 * Wv + 7) / 8);
     for (int e = tid; e < 16 * 8; e += blockDim.x) {
         const int w = e >> 3, k = e & 7;
-        o.kmask[w][k] = w < W ? pk.mask[w][k] : 0u;
+        o.kmask[w][k] = w < Wk ? pk.mask[w][k] : 0u;
         for (int half = 0; half < 2; ++half) {
-            const int ch = w < W ? pk.ch[w][k][half] : -1;
+            const int ch = w < Wk ? pk.ch[w][k][half] : -1;
             o.kslot[w][k][half] = (int16_t)(ch < 0 ? -1 : (ch | ((pk.ex[w][k][half] + 64) << 8)));
         }
     }
     for (int e = tid; e < 32 * 8; e += blockDim.x) {
         const int hw = e >> 3, k = e & 7;
-        o.vmask[hw][k] = hw < 2 * W ? pv.mask[hw][k] : 0u;
+        o.vmask[hw][k] = hw < 2 * Wv ? pv.mask[hw][k] : 0u;
     }
     for (int j = tid; j < D; j += blockDim.x) {
         o.ksc[j] = tk.bits[j] ? tk.step[j] * 0.08838834764831845f : 0.f;
@@ -986,7 +1011,7 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
         for (int row = 0; row < rows_tot && n < 2; ++row) {
             const int gr = row >> 6, m4 = (row >> 4) & 3, rr = row & 15;
             const int hw = 8 * gr + (rr & 7), k = 2 * m4 + (rr >> 3);
-            if (hw < 2 * W && pv.ch[hw][k][0] == j) got[n++] = (int16_t)(row | ((pv.ex[hw][k][0] + 64) << 8));
+            if (hw < 2 * Wv && pv.ch[hw][k][0] == j) got[n++] = (int16_t)(row | ((pv.ex[hw][k][0] + 64) << 8));
         }
         o.vgat[j][0] = got[0];
         o.vgat[j][1] = got[1];
@@ -1105,7 +1130,7 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t *rec, int off, int b)
 // m (running max of scores), l (sum of exp), acc[j] = sum_i p_i u^V_ij.
 __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
     const float *__restrict__ qp, const uint32_t *__restrict__ kp, const uint32_t *__restrict__ vp,
-    CacheMap map, const int32_t *__restrict__ seq_lens, int L, int Hkv, int G, int W, int chunk,
+    CacheMap map, const int32_t *__restrict__ seq_lens, int L, int Hkv, int G, int Wk, int Wv, int chunk,
     int n_split, const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs,
     float *__restrict__ part, uint32_t *status)
 {
@@ -1150,14 +1175,15 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
 #pragma unroll
         for (int gg = 0; gg < AATC_MAX_G; ++gg) sc[gg] = -INFINITY;
         if (valid) {
-            long long tw = cache_tile_word(map, b, h, Hkv, W, tok >> 5);
-            if (tw < 0) {   // no block for this tile: read tile 0 of the pool, report it
+            long long tw = cache_tile_word(map, b, h, Hkv, Wk, tok >> 5);
+            long long twv = cache_tile_word(map, b, h, Hkv, Wv, tok >> 5);
+            if (tw < 0 || twv < 0) {   // no block for this tile: read tile 0 of the pool, report it
                 bad_blk = true;
-                tw = 0;
+                tw = twv = 0;
             }
             const uint32_t *tile = kp + tw;
-            for (int w = 0; w < W; ++w) rec[w] = tile[key_word_pos(tok & 31, w, W)];
-            rec[W] = 0u;
+            for (int w = 0; w < Wk; ++w) rec[w] = tile[key_word_pos(tok & 31, w, Wk)];
+            rec[Wk] = 0u;
 #pragma unroll
             for (int gg = 0; gg < AATC_MAX_G; ++gg) sc[gg] = 0.f;
             for (int j = 0; j < D; ++j) {
@@ -1167,13 +1193,13 @@ __global__ void __launch_bounds__(DEC_TILE) k_decode_split_general(
                 for (int gg = 0; gg < AATC_MAX_G; ++gg)
                     if (gg < G) sc[gg] = fmaf(q_s[gg][j], u, sc[gg]);
             }
-            const uint32_t *vt = vp + tw;
-            for (int w = 0; w < W; ++w) {
+            const uint32_t *vt = vp + twv;
+            for (int w = 0; w < Wv; ++w) {
                 const uint32_t lo = (vt[16 * (2 * w) + ((tok & 31) >> 1)] >> (16 * (tok & 1))) & 0xFFFFu;
                 const uint32_t hi = (vt[16 * (2 * w + 1) + ((tok & 31) >> 1)] >> (16 * (tok & 1))) & 0xFFFFu;
                 rec[w] = lo | (hi << 16);
             }
-            rec[W] = 0u;
+            rec[Wv] = 0u;
             for (int j = 0; j < D; ++j) v_s[t][j] = bv[j] ? (uint8_t)code_at(rec, offv[j], bv[j]) : 0;
         } else {
             for (int j = 0; j < D; ++j) v_s[t][j] = 0;
@@ -1260,28 +1286,10 @@ size_t general_ws_bytes(const aatc_calib *h, int B, int L)
     return ((qp + 255) / 256) * 256 + part;
 }
 
-// Raise a kernel's dynamic shared memory limit once per kernel (and per
-// larger size seen).  Keyed by the kernel's address: every instance of a
-// template has the same function type.
-aatc_status smem_limit(const void *kern, size_t bytes)
-{
-    static struct { const void *k; size_t set; } seen[32];
-    static int used = 0;
-    static std::mutex mu;
-    std::lock_guard<std::mutex> lock(mu);
-    int i = 0;
-    while (i < used && seen[i].k != kern) ++i;
-    if (i < used && seen[i].set >= bytes) return AATC_OK;
-    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes));
-    if (i == used && used < 32) seen[used++] = {kern, 0};
-    if (i < used) seen[i].set = bytes;
-    return AATC_OK;
-}
-
 template <typename K>
 aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a, cudaStream_t s)
 {
-    aatc_status st = smem_limit((const void *)kern, f.smem);
+    aatc_status st = kernel_smem_limit((const void *)kern, f.smem);
     if (st != AATC_OK) return st;
     // programmatic dependent launch: the prologue that reads only the handle
     // overlaps the tail of the previous kernel on the stream
@@ -1310,31 +1318,22 @@ aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cud
     return launch_variant(k_decode_fast<GMAX, NT, FW, float, false>, FW, f, a, s);
 }
 
-aatc_status launch_combine(const FastGeom &f, const aatc_calib *h, const float *part, float *out, cudaStream_t s)
-{
-    const size_t smem = cb_smem(f.S, f.HPG);
-    aatc_status st0 = smem_limit((const void *)k_decode_combine_fast, smem);
-    if (st0 != AATC_OK) return st0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(f.units);
-    cfg.blockDim = dim3(CB_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    AATC_CUDA(cudaLaunchKernelEx(&cfg, k_decode_combine_fast, part, f.S, cb_chunk(f.HPG), h->Hkv, h->G, f.HG,
-                                 f.HPG, (const float *)h->vcst, out, h->status));
-    return AATC_OK;
-}
+// Test hook state (aatc_test_wait_fault): read at every fast-path launch.
+std::atomic<int> g_hook_skip{0};
+std::atomic<int> g_hook_tries{WAIT_TRIES};
 
 }  // namespace
 
+extern "C" aatc_status aatc_test_wait_fault(int skip_tile_copy, int wait_tries)
+{
+    g_hook_skip.store(skip_tile_copy ? 1 : 0);
+    g_hook_tries.store(wait_tries > 0 ? wait_tries : WAIT_TRIES);
+    return AATC_OK;
+}
+
 aatc_status dec_build(aatc_calib *h, cudaStream_t s)
 {
-    k_dec_build<<<h->Hkv, D, 0, s>>>(h->plan, h->tab, h->W, h->U_v, h->mu_v, h->dblob, h->vcst);
+    k_dec_build<<<h->Hkv, D, 0, s>>>(h->plan, h->tab, h->Wk, h->Wv, h->U_v, h->mu_v, h->dblob, h->vcst);
     AATC_CUDA(cudaGetLastError());
     return AATC_OK;
 }
@@ -1359,14 +1358,17 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
             AATC_CUDA(cudaMemsetAsync(out, 0, (size_t)B * h->Hq * D * sizeof(float), s));
             return AATC_OK;
         }
-        float *part = (float *)ws;
+        if (!f.single && f.units > MAX_COUNTED)
+            return aatc_fail(AATC_ERR_UNSUPPORTED, "%d units with several splits each", f.units);
+        float *part = f.single ? nullptr : (float *)((char *)ws + WS_COUNTERS);
         FastArgs a;
         a.kp = kp;
         a.vp = vp;
         a.seq_lens = seq_lens;
         a.L = L;
         a.map = map;
-        a.W = h->W;
+        a.Wk = h->Wk;
+        a.Wv = h->Wv;
         a.rows = f.rows;
         a.groups = f.groups;
         a.Hkv = h->Hkv;
@@ -1374,8 +1376,6 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.HG = f.HG;
         a.FST = f.FST;
         a.stage_region = (uint32_t)f.stage_region;
-        a.uv_off = (uint32_t)f.uv_off;
-        a.part_off = (uint32_t)f.part_off;
         a.single = f.single ? 1 : 0;
         a.out = out;
         a.vcst = h->vcst;
@@ -1388,7 +1388,11 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.q = q;
         a.AkT = h->AkT32;
         a.part = part;
+        a.counter = f.single ? nullptr : (unsigned *)ws;
+        a.merge_slots = (int)(f.stage_region / ((size_t)f.HPG * PROW * 4));
         a.status = h->status;
+        a.wait_tries = g_hook_tries.load(std::memory_order_relaxed);
+        a.skip_first_copy = g_hook_skip.load(std::memory_order_relaxed);
         aatc_status st;
         if (f.NT == 1) {
             if (f.GMAX == 2) st = launch_fast<2, 1, 16>(f, a, h->dtype, s);
@@ -1399,11 +1403,10 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
             else if (f.GMAX == 3) st = launch_fast<3, 2, 12>(f, a, h->dtype, s);
             else st = launch_fast<4, 2, 12>(f, a, h->dtype, s);
         }
-        if (st != AATC_OK) return st;
-        if (f.single) return AATC_OK;   // single splits finished in the split kernel
-        return launch_combine(f, h, part, out, s);
+        return st;
     }
-    if (h->W > GEN_MAX_W) return aatc_fail(AATC_ERR_UNSUPPORTED, "record of %d words", h->W);
+    if (h->Wk > GEN_MAX_W || h->Wv > GEN_MAX_W)
+        return aatc_fail(AATC_ERR_UNSUPPORTED, "records of %d / %d words", h->Wk, h->Wv);
     SplitPlan p = plan_splits(B, h->Hkv, L);
     float *qp = (float *)ws;
     size_t qp_bytes = (((size_t)B * h->Hq * D * sizeof(float) + 255) / 256) * 256;
@@ -1414,7 +1417,8 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
     else
         k_query_prep<float><<<dim3(B, h->Hq), D, 0, s>>>((const float *)q, h->Hq, h->G, h->AkT32, h->tab, qp);
     k_decode_split_general<<<dim3(p.n_split, h->Hkv, B), DEC_TILE, 0, s>>>(
-        qp, kp, vp, map, seq_lens, L, h->Hkv, h->G, h->W, p.chunk, p.n_split, h->plan, h->tab, part, h->status);
+        qp, kp, vp, map, seq_lens, L, h->Hkv, h->G, h->Wk, h->Wv, p.chunk, p.n_split, h->plan, h->tab, part,
+        h->status);
     k_decode_combine<<<dim3(B, h->Hq), D, 0, s>>>(part, p.n_split, h->Hq, h->G, h->tab, h->UvT32,
                                                   h->muv32, out);
     AATC_CUDA(cudaGetLastError());

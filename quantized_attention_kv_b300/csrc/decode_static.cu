@@ -24,8 +24,10 @@ std::mutex g_scratch_mu;
 
 // In host code g_decode_scratch names a host-side stand-in, not device
 // memory, so its device address is looked up once per device (with that
-// device current) and cached.
-aatc_status scratch_for_current_device(void **out)
+// device current) and cached.  At that set-up the array is also cleared on
+// the caller's stream: the decode's split counters must start at zero (each
+// call leaves them at zero again).
+aatc_status scratch_for_current_device(void **out, cudaStream_t s)
 {
     int dev = -1;
     AATC_CUDA(cudaGetDevice(&dev));
@@ -35,6 +37,8 @@ aatc_status scratch_for_current_device(void **out)
         void *p = nullptr;
         cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
         if (e != cudaSuccess) return aatc_cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+        e = cudaMemsetAsync(p, 0, AATC_STATIC_SCRATCH_BYTES, s);
+        if (e != cudaSuccess) return aatc_cuda_fail(e, "cudaMemsetAsync(decode scratch)");
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
@@ -59,10 +63,10 @@ extern "C" aatc_status aatc_decode_attention_static(const aatc_calib *calib, con
                          "(use aatc_decode_attention with a caller workspace)",
                          need, (unsigned)AATC_STATIC_SCRATCH_BYTES);
     void *scratch = nullptr;
-    st = scratch_for_current_device(&scratch);
+    st = scratch_for_current_device(&scratch, (cudaStream_t)stream);
     if (st != AATC_OK) return st;
-    // The decode kernels overwrite every scratch byte they later read, so the
-    // previous call's contents need no clearing.
+    // The decode kernels overwrite every other scratch byte before they read
+    // it, so nothing else needs clearing between calls.
     return aatc_decode_attention(calib, q, k_packed, v_packed, L_cap, seq_lens, L, B, out, scratch,
                                  AATC_STATIC_SCRATCH_BYTES, stream);
 }

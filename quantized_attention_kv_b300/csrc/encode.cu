@@ -41,7 +41,7 @@ __device__ __forceinline__ int key_word_pos(int i, int w, int W)
 template <typename T>
 __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, const int32_t *row_start,
-    CacheMap map, int Hkv, int W, const float *__restrict__ Tk, const float *__restrict__ Tv,
+    CacheMap map, int Hkv, int Wk, int Wv, const float *__restrict__ Tk, const float *__restrict__ Tv,
     const float *__restrict__ bk, const float *__restrict__ bv, const CodecTables *__restrict__ tabs,
     const HeadPlan *__restrict__ plans, uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
 {
@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(ENC_TILE) k_encode_simple(
     const int tile = blockIdx.x, h = blockIdx.y;
     const int b = blockIdx.z >> 1, tensor = blockIdx.z & 1;
     const int t = threadIdx.x;
+    const int W = tensor == 0 ? Wk : Wv;   // the tensor's record words
     const T *x = (tensor == 0 ? k : v) + (((size_t)b * Hkv + h) * L_new) * D;
     const float *Tm = (tensor == 0 ? Tk : Tv) + (size_t)h * D * D;
     const float *bias = (tensor == 0 ? bk : bv) + h * D;
@@ -156,7 +157,7 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src)
 template <typename T>
 __global__ void __launch_bounds__(D) k_encode_append(
     const T *__restrict__ k, const T *__restrict__ v, int L_new, int start_pos, const int32_t *row_start,
-    CacheMap map, int Hkv, int W, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
+    CacheMap map, int Hkv, int Wk, int Wv, const float *__restrict__ Tk, const float *__restrict__ Tv, const float *__restrict__ bk,
     const float *__restrict__ bv, const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
     uint32_t *__restrict__ kp, uint32_t *__restrict__ vp, uint32_t *status)
 {
@@ -166,6 +167,7 @@ __global__ void __launch_bounds__(D) k_encode_append(
     __shared__ uint32_t rec[MAX_W];
     const int h = blockIdx.x, tensor = blockIdx.y, b = blockIdx.z, j = threadIdx.x;
     const int ht = h * 2 + tensor;
+    const int W = tensor == 0 ? Wk : Wv;   // the tensor's record words
 
     // handle data only, ahead of the wait
     const float4 *src = reinterpret_cast<const float4 *>((tensor == 0 ? Tk : Tv) + (size_t)h * D * D);
@@ -235,7 +237,8 @@ aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int
 {
     static const size_t smem = (size_t)D * TPAD * sizeof(float);
     auto kern = k_encode_append<T>;
-    AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    aatc_status st = kernel_smem_limit((const void *)kern, smem);
+    if (st != AATC_OK) return st;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(h->Hkv, 2, B);
     cfg.blockDim = dim3(D);
@@ -246,7 +249,7 @@ aatc_status launch_append(const aatc_calib *h, const void *k, const void *v, int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, (const T *)k, (const T *)v, L_new, start_pos, row_start, map, h->Hkv, h->W,
+    AATC_CUDA(cudaLaunchKernelEx(&cfg, kern, (const T *)k, (const T *)v, L_new, start_pos, row_start, map, h->Hkv, h->Wk, h->Wv,
                                  (const float *)h->Tk32, (const float *)h->Tv32, (const float *)h->bk32,
                                  (const float *)h->bv32, (const CodecTables *)h->tab, (const HeadPlan *)h->plan,
                                  kp, vp, h->status));
@@ -264,22 +267,24 @@ aatc_status encode_run(const aatc_calib *h, const void *k, const void *v, int B,
             return launch_append<__nv_bfloat16>(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
         return launch_append<float>(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
     }
-    if (h->dtype == AATC_BF16 && h->tmap_ok && h->W <= 16)
+    if (h->dtype == AATC_BF16 && h->tmap_ok && h->Wk <= 16 && h->Wv <= 16)
         return encode_tc_run(h, k, v, B, L_new, start_pos, row_start, map, kp, vp, s);
     const size_t smem = (size_t)D * D * 4 + (size_t)ENC_TILE * (D + 1) * 4 +
-                        (size_t)ENC_TILE * (h->W + 1) * 4;
+                        (size_t)ENC_TILE * ((h->Wk > h->Wv ? h->Wk : h->Wv) + 1) * 4;
     const dim3 grid((L_new + ENC_TILE - 1) / ENC_TILE, h->Hkv, 2 * B);
     if (h->dtype == AATC_BF16) {
         auto kern = k_encode_simple<__nv_bfloat16>;
-        AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        aatc_status st = kernel_smem_limit((const void *)kern, smem);
+        if (st != AATC_OK) return st;
         kern<<<grid, ENC_TILE, smem, s>>>((const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v, L_new,
-                                          start_pos, row_start, map, h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32,
+                                          start_pos, row_start, map, h->Hkv, h->Wk, h->Wv, h->Tk32, h->Tv32, h->bk32,
                                           h->bv32, h->tab, h->plan, kp, vp, h->status);
     } else {
         auto kern = k_encode_simple<float>;
-        AATC_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        aatc_status st = kernel_smem_limit((const void *)kern, smem);
+        if (st != AATC_OK) return st;
         kern<<<grid, ENC_TILE, smem, s>>>((const float *)k, (const float *)v, L_new, start_pos, row_start, map,
-                                          h->Hkv, h->W, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, h->plan,
+                                          h->Hkv, h->Wk, h->Wv, h->Tk32, h->Tv32, h->bk32, h->bv32, h->tab, h->plan,
                                           kp, vp, h->status);
     }
     AATC_CUDA(cudaGetLastError());

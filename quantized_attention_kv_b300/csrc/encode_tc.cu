@@ -48,7 +48,7 @@ __device__ __forceinline__ int key_word_pos(int i, int w, int W)
 }
 
 struct EncArgs {
-    int B, H, L_new, start_pos, W, nblk, n_items;
+    int B, H, L_new, start_pos, Wk, Wv, nblk, n_items;   // Wk / Wv: record words of keys / values
     const int32_t *row_start;   // [B] first position of each row, or NULL: start_pos
     CacheMap map;               // contiguous or paged cache
     const EncCol *cols;     // [H][2][D]
@@ -64,9 +64,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
     unsigned char *Ts = sm;                              // 3 splits x 2 k-halves x 16 KB
     unsigned char *Xs = Ts + TBYTES;                     // ESTAGES x 32 KB
-    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 W words (tiled)
-    const int W = a.W;
-    EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + NGRP * EB * W);     // [NGRP][D]
+    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 x max(Wk, Wv) words (tiled)
+    const int Wmax = a.Wk > a.Wv ? a.Wk : a.Wv;
+    EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + NGRP * EB * Wmax);  // [NGRP][D]
     __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     // before reading the cache)
     asm volatile("griddepcontrol.launch_dependents;");
     if (tid < 16) {
-        const int r = tid >> 2, nr = min(4, a.W - 4 * r);
+        const int r = tid >> 2, nr = min(4, a.Wk - 4 * r);   // key records only
         wtab[tid] = make_int2(64 * r + 2 * (tid - 4 * r), 2 * nr);
     }
     if (warp == 0) {
@@ -175,11 +175,12 @@ __global__ void __launch_bounds__(ETHREADS, 1)
         const int gt = wq * 32 + lane;             // thread in group = token in block = lane
         const int bar_id = 1 + g;
         EncCol *cols = cols_s + g * D;
-        uint32_t *R = Rs + g * EB * W;
+        uint32_t *R = Rs + g * EB * Wmax;
         int ht_cols = -1;
         for (int n = g; n < count; n += NGRP) {
             const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
             const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
+            const int W = t ? a.Wv : a.Wk;   // the item's tensor's record words
             if (ht != ht_cols) {
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
                 for (int e = gt; e < D; e += 128) cols[e] = a.cols[(size_t)ht * D + e];
@@ -435,15 +436,17 @@ aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int
     a.start_pos = start_pos;
     a.row_start = row_start;
     a.map = map;
-    a.W = h->W;
+    a.Wk = h->Wk;
+    a.Wv = h->Wv;
     a.nblk = (L_new + EB - 1) / EB;
     a.n_items = h->Hkv * 2 * B * a.nblk;
     a.cols = h->enc_cols;
     a.kp = kp;
     a.vp = vp;
     a.status = h->status;
-    const size_t smem = enc_smem(h->W);
-    AATC_CUDA(cudaFuncSetAttribute(k_encode_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    const size_t smem = enc_smem(h->Wk > h->Wv ? h->Wk : h->Wv);
+    aatc_status st = kernel_smem_limit((const void *)k_encode_tc, smem);
+    if (st != AATC_OK) return st;
     int grid = sm_count_enc();
     if (grid > a.n_items) grid = a.n_items;
     k_encode_tc<<<grid, ETHREADS, smem, s>>>(mk, mv, mt, a);

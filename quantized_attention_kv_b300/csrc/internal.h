@@ -17,6 +17,7 @@ enum : uint32_t {
     AATC_DEV_NO_CONVERGENCE = 2u,
     AATC_DEV_TIMEOUT = 4u,        // a bounded wait inside a kernel gave up
     AATC_DEV_RANGE = 8u,          // a cache position or block table entry out of range (access skipped)
+    AATC_DEV_WORKSPACE = 16u,     // a decode workspace's split counters were not zero at entry
 };
 
 // Where the 32-token tiles of the cache of one (batch row b, KV head h) live.
@@ -104,7 +105,11 @@ struct __align__(16) EncCol {
 };
 
 struct aatc_calib {
-    int d, Hkv, Hq, G, Bbits, W;
+    int d, Hkv, Hq, G;
+    int Bk, Bv;               // record bits per token and head of keys / values
+    int Wk, Wv;               // record words (Bk / 32, Bv / 32)
+    int Bpair;                // 2 x the requested budget: what a joint allocation splits
+    bool joint;               // the K/V split follows the attention-aware token weights
     aatc_dtype dtype;
     void *arena;              // one cudaMalloc backing every device array below
     // fp64 calibration results, [H] leading (exported by aatc_export_calib)
@@ -113,6 +118,8 @@ struct aatc_calib {
     double *lam_k, *lam_v, *lam_q;            // [H][d]
     int32_t *bits_k, *bits_v;                 // [H][d]
     float *step_k, *step_v;                   // [H][d]
+    double *alpha;                            // [H][2] token weights alpha_K, alpha_V (joint allocation)
+    int32_t *split;                           // [2] chosen B_K, B_V (joint allocation; device)
     // fp32 operands of the encode / decode kernels
     float *Tk32, *Tv32;       // [H][d][d] transform rows (coefficient i = row i . x)
     float *bk32, *bv32;       // [H][d] T mu
@@ -137,6 +144,10 @@ struct aatc_calib {
 // ---- error reporting (api.cu) ----
 aatc_status aatc_fail(aatc_status st, const char *fmt, ...);
 aatc_status aatc_cuda_fail(cudaError_t e, const char *what);
+// Raise a kernel's dynamic shared memory limit to `bytes` on the current
+// device, with a runtime call only the first time (per device and kernel)
+// or for a larger size.
+aatc_status kernel_smem_limit(const void *kern, size_t bytes);
 #define AATC_CUDA(call)                                                   \
     do {                                                                  \
         cudaError_t _e = (call);                                          \

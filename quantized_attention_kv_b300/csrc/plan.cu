@@ -110,11 +110,11 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
     std::vector<HeadPlan> plans((size_t)h->Hkv * 2);
     bool fast = true;
     for (int hh = 0; hh < h->Hkv; ++hh) {
-        plan_one(bits_k + (size_t)hh * D, h->W, &plans[hh * 2 + 0]);
+        plan_one(bits_k + (size_t)hh * D, h->Wk, &plans[hh * 2 + 0]);
         // values: the same cut into pieces, read per half-word (slot = half-word e,
         // mask in both halves: the pair word holds half-word e of two tokens)
         HeadPlan key_view;
-        plan_one(bits_v + (size_t)hh * D, h->W, &key_view);
+        plan_one(bits_v + (size_t)hh * D, h->Wv, &key_view);
         fast = fast && plans[hh * 2].max_pieces <= AATC_PIECES && key_view.max_pieces <= AATC_PIECES;
         HeadPlan &pv = plans[hh * 2 + 1];
         memcpy(&pv, &key_view, sizeof(HeadPlan));
@@ -128,7 +128,7 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
             // half-word e = bytes 2e (S = 0) and 2e+1 (S = 1); record word e/2 holds
             // them at bytes 2(e%2) and 2(e%2)+1, i.e. in key_view's slot of word e/2:
             // low half (e even) or high half (e odd)
-            for (int e = 0; e < 2 * h->W && e < AATC_PLAN_SLOTS; ++e)
+            for (int e = 0; e < 2 * h->Wv && e < AATC_PLAN_SLOTS; ++e)
                 for (int k = 0; k < 8; ++k) {
                     const int w = e / 2, half = e % 2;
                     const uint32_t m = (key_view.mask[w][k] >> (16 * half)) & 0xFFFFu;
