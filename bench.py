@@ -253,56 +253,12 @@ def run_ours(args, ws, rank, local):
             enc(kc, vc, kps[c], vps[c], 0)
     torch.cuda.synchronize()
 
-    for s_ in range(args.warmup):
-        graphs[s_ % n_rot].replay()
-    torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
-    with ClockSampler(local) as clk:
-        _barrier(ws)
-        torch.cuda.synchronize()
-        w0 = time.perf_counter()
-        e0.record(stream)
-        for s_ in range(args.steps):
-            graphs[s_ % n_rot].replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        _barrier(ws)
-        wall = time.perf_counter() - w0
-        step_ms_dev = e0.elapsed_time(e1) / args.steps
-        # decode and encode alone (same rotation), for the per-kernel rates:
-        # each replay of a graph (one call per cache copy) is timed on its own,
-        # at least 200 calls in all; per-call times are replay time / copies
-        reps = max(10, -(-200 // n_rot))
-
-        def timed(g):
-            g.replay()
-            torch.cuda.synchronize()
-            evs = [(ev(), ev()) for _ in range(reps)]
-            for a_, b_ in evs:
-                a_.record(stream)
-                g.replay()
-                b_.record(stream)
-            torch.cuda.synchronize()
-            return sorted(a_.elapsed_time(b_) / 1e3 / n_rot for a_, b_ in evs)
-
-        dec_t = timed(g_dec)
-        app_t = timed(g_app)
-        enc_t = timed(g_enc)
-
-    def pct(v, q):
-        return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
-
-    dec_call_s = _max_over_ranks(pct(dec_t, 0.5), ws)
-    enc_call_s = _max_over_ranks(pct(enc_t, 0.5), ws)
-    app_call_s = _max_over_ranks(pct(app_t, 0.5), ws)
-    wall = _max_over_ranks(wall, ws)
-    spread = {name: {"p10_us": round(pct(v, 0.1) * 1e6, 3), "median_us": round(pct(v, 0.5) * 1e6, 3),
-                     "p90_us": round(pct(v, 0.9) * 1e6, 3), "calls": len(v) * n_rot, "replays": len(v)}
-              for name, v in (("decode", dec_t), ("append_decode", app_t), ("encode", enc_t))}
-    kp, vp = kps[0], vps[0]
-
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs (query, new key/value token), append + decode, D2H of the output
+    # End to end through the public API with host buffers, measured before the
+    # clock sampler starts: while nvidia-smi samples, and for a while after it
+    # stopped, each call's host path measured about six times as long (about 9
+    # -> 60 us per launch on the B300 machine), an effect of the sampler, not of
+    # the library.  H2D of the step's inputs (query, new key/value token),
+    # append + decode, D2H of the output
     # the step's inputs (query, new key and value token) staged in one pinned
     # buffer and sent by one copy; the device copies are views of one buffer
     parts = [q, kn, vn]
@@ -358,6 +314,54 @@ def run_ours(args, ws, rank, local):
     host = {k_: round(v_ / n_e2e * 1e6, 2) for k_, v_ in host.items()}
     e2e_ms = sorted(e[0].elapsed_time(e[1]) for e in e2e_evs)
     e2e_step_s = _max_over_ranks(e2e_ms[len(e2e_ms) // 2] / 1e3, ws)   # median step
+    for s_ in range(args.warmup):
+        graphs[s_ % n_rot].replay()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    with ClockSampler(local) as clk:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        e0.record(stream)
+        for s_ in range(args.steps):
+            graphs[s_ % n_rot].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        _barrier(ws)
+        wall = time.perf_counter() - w0
+        step_ms_dev = e0.elapsed_time(e1) / args.steps
+        # decode and encode alone (same rotation), for the per-kernel rates:
+        # each replay of a graph (one call per cache copy) is timed on its own,
+        # at least 200 calls in all; per-call times are replay time / copies
+        reps = max(10, -(-200 // n_rot))
+
+        def timed(g):
+            g.replay()
+            torch.cuda.synchronize()
+            evs = [(ev(), ev()) for _ in range(reps)]
+            for a_, b_ in evs:
+                a_.record(stream)
+                g.replay()
+                b_.record(stream)
+            torch.cuda.synchronize()
+            return sorted(a_.elapsed_time(b_) / 1e3 / n_rot for a_, b_ in evs)
+
+        dec_t = timed(g_dec)
+        app_t = timed(g_app)
+        enc_t = timed(g_enc)
+
+    def pct(v, q):
+        return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]
+
+    dec_call_s = _max_over_ranks(pct(dec_t, 0.5), ws)
+    enc_call_s = _max_over_ranks(pct(enc_t, 0.5), ws)
+    app_call_s = _max_over_ranks(pct(app_t, 0.5), ws)
+    wall = _max_over_ranks(wall, ws)
+    spread = {name: {"p10_us": round(pct(v, 0.1) * 1e6, 3), "median_us": round(pct(v, 0.5) * 1e6, 3),
+                     "p90_us": round(pct(v, 0.9) * 1e6, 3), "calls": len(v) * n_rot, "replays": len(v)}
+              for name, v in (("decode", dec_t), ("append_decode", app_t), ("encode", enc_t))}
+    kp, vp = kps[0], vps[0]
+
     h2d = sum(nbytes_in)
     d2h = out_bytes
 

@@ -68,7 +68,8 @@ constexpr float RESCALE_T = 8.f; // the running maximum is raised once a score e
 // unit; units number fewer than the CTAs, so at most MAX_COUNTED) at offset 0,
 // where every call finds them, then the partial slots.
 constexpr int MAX_COUNTED = 256;
-constexpr int MERGE_MIN_SLOTS = 16;   // the merge stages at least this many partial slots at a time
+constexpr int MERGE_MIN_SLOTS = 8;    // the merge stages at least this many partial slots at a time
+constexpr int MERGE_LD = 8;           // ... and at most MERGE_LD float4 loads per thread per chunk
 constexpr int SCR_CBAR = 256;    // epilogue: c [D][8] starts this many floats into the scratch (after the warp maxima and sums)
 constexpr size_t WS_COUNTERS = MAX_COUNTED * sizeof(unsigned);
 
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         {
             const int j = tid & (D - 1), ks = tid >> 7;
             float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 2
+#pragma unroll 8
             for (int k = ks; k < D; k += KS) {
                 const float av = mat_s[k * D + j];
                 const float4 q0 = *reinterpret_cast<const float4 *>(&q_s[k * 8]);
@@ -850,22 +851,27 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         }
     }
     if (!a.single) {
-        // count this split in (the partial is visible device-wide first); the
-        // split counted in last merges the unit and puts the counter back to 0
-        __threadfence();
+        // count this split in: after the barrier, one thread's release
+        // (fence.acq_rel at GPU scope, then the atomic) publishes the partial
+        // the whole CTA wrote; the split counted in last acquires the others'
+        // partials the same way, merges the unit and puts the counter back to 0
         __syncthreads();
         if (tid == 0) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
             const unsigned old = atomicAdd(a.counter + u, 1u);
             if (old >= (unsigned)a.S) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
-            mxi[0] = old == (unsigned)(a.S - 1);
+            const bool last = old == (unsigned)(a.S - 1);
+            if (last) {
+                asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                a.counter[u] = 0u;
+            }
+            mxi[0] = last;
         }
         __syncthreads();
         if (!mxi[0]) {
             mbar_wait(mat_bar, 1);   // (long landed) no copy may be in flight when the CTA exits
             return;
         }
-        __threadfence();
-        if (tid == 0) a.counter[u] = 0u;
         // merge, once per head: c = sum_s 2^(m_s - M) c_s and l likewise.  The
         // unit's partial slots are contiguous: chunks of up to merge_slots of
         // them come into the stages, every thread loading its share at once
@@ -884,9 +890,15 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         float *Ps = reinterpret_cast<float *>(stage_base);
         for (int c0 = 0; c0 < a.S; c0 += a.merge_slots) {
             const int n = min(a.merge_slots, a.S - c0);
-            const int nq = n * HPG * PROW / 4;   // float4 of the chunk
+            const int nq = n * HPG * PROW / 4;   // float4 of the chunk: at most MERGE_LD per thread
             const float4 *src4 = reinterpret_cast<const float4 *>(Pu + (size_t)c0 * HPG * PROW);
-            for (int k = tid; k < nq; k += NTH) reinterpret_cast<float4 *>(Ps)[k] = __ldcg(src4 + k);
+            float4 ld[MERGE_LD];   // every load of the chunk in flight at once
+#pragma unroll
+            for (int k = 0; k < MERGE_LD; ++k)
+                if (tid + k * NTH < nq) ld[k] = __ldcg(src4 + tid + k * NTH);
+#pragma unroll
+            for (int k = 0; k < MERGE_LD; ++k)
+                if (tid + k * NTH < nq) reinterpret_cast<float4 *>(Ps)[tid + k * NTH] = ld[k];
             __syncthreads();
 #pragma unroll
             for (int q = 0; q < EPT; ++q) {
@@ -1389,7 +1401,11 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.AkT = h->AkT32;
         a.part = part;
         a.counter = f.single ? nullptr : (unsigned *)ws;
-        a.merge_slots = (int)(f.stage_region / ((size_t)f.HPG * PROW * 4));
+        {   // slots per merge chunk: what the stages hold, at most MERGE_LD float4 per thread
+            const int fit = (int)(f.stage_region / ((size_t)f.HPG * PROW * 4));
+            const int ld = MERGE_LD * 4 * (f.FW * 32) / (f.HPG * PROW);
+            a.merge_slots = fit < ld ? fit : ld;
+        }
         a.status = h->status;
         a.wait_tries = g_hook_tries.load(std::memory_order_relaxed);
         a.skip_first_copy = g_hook_skip.load(std::memory_order_relaxed);
