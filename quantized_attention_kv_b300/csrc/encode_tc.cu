@@ -14,9 +14,11 @@
 //
 // One persistent CTA per SM works through a contiguous range of (head,
 // tensor, batch row, 128-token block) items:
-//   warp 4, one thread: TMA loads (x tiles: 3 stages; T: once per head and
-//       tensor) and MMA issue into two tensor-memory accumulators;
-//   warps 0-3: epilogue, thread = token = tensor-memory lane: read the 128
+//   warp 16, one thread: TMA loads (x tiles: ESTAGES = 2 stages; T: once per
+//       head and tensor) and MMA issue into NGRP = 4 tensor-memory
+//       accumulators, item n into accumulator n % 4;
+//   warps 0-15: four epilogue groups of four warps; group g takes items
+//       g, g + 4, ..., thread = token = tensor-memory lane: read the 128
 //       accumulators, quantize (v = c inv + off, clamp, round half to even),
 //       pack LSB-first into the record and place the words in the tiled
 //       cache layout in shared memory; full aligned blocks leave by one bulk
