@@ -590,17 +590,9 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         const uint32_t *Kt = reinterpret_cast<const uint32_t *>(my_stage + s * SB);
         const uint32_t *Vt = Kt + TILE * Wk;
 
-        // ---- scores: C[hf][r & 1] rows g / g+8 = tokens 16 hf + 2g / +1, columns 2c / 2c+1 =
-        // head c hi / lo; two chains per half-tile (even and odd key rows)
-        float C[2][2][NT][4];   // chain (hf, rp) starts at row rp, k-step 0 with a zero accumulator
-        if (rows < 2) {         // one key row: the odd chain stays empty
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-                for (int t = 0; t < NT; ++t)
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) C[hf][1][t][k] = 0.f;
-        }
+        // ---- scores: C[hf] rows g / g+8 = tokens 16 hf + 2g / +1, columns 2c / 2c+1 =
+        // head c hi / lo; one accumulator chain per half-tile, the two interleaved
+        float C[2][NT][4];      // chain hf starts at row 0, k-step 0 with a zero accumulator
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             if (r >= rows) break;
@@ -629,8 +621,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
                     const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
-                        if (r < 2 && s4 == 0) mma16816_z(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
-                        else mma16816(C[hf][r & 1][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
+                        if (r == 0 && s4 == 0) mma16816_z(C[hf][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
+                        else mma16816(C[hf][t], A0, A1, A2, A3, bq[t].x, bq[t].y);
                     }
                 }
             }
@@ -644,8 +636,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             float sv[4];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                sv[2 * hf] = (C[hf][0][t][0] + C[hf][0][t][1]) + (C[hf][1][t][0] + C[hf][1][t][1]);
-                sv[2 * hf + 1] = (C[hf][0][t][2] + C[hf][0][t][3]) + (C[hf][1][t][2] + C[hf][1][t][3]);
+                sv[2 * hf] = C[hf][t][0] + C[hf][t][1];
+                sv[2 * hf + 1] = C[hf][t][2] + C[hf][t][3];
             }
             if (!full) {
 #pragma unroll
