@@ -22,7 +22,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Sizes of the arena pieces, in the order they are carved.
 struct Layout {
-    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, dblob, t3, cols, total;
+    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, dblob, dmat, t3, cols, total;
 };
 
 Layout layout_for(int H)
@@ -37,10 +37,11 @@ Layout layout_for(int H)
     L.tabs = up((size_t)H * 2 * sizeof(CodecTables));
     L.plans = up((size_t)H * 2 * sizeof(HeadPlan));
     L.dblob = up((size_t)H * sizeof(DecBlob));
+    L.dmat = up((size_t)H * 4 * D * D * 2);
     L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
     L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
     L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
-              L.plans + L.dblob + L.f32_vec + L.t3 + L.cols + 1024 + 2 * L.f64_vec;
+              L.plans + L.dblob + L.dmat + L.f32_vec + L.t3 + L.cols + 1024 + 2 * L.f64_vec;
     return L;
 }
 
@@ -88,6 +89,7 @@ aatc_status new_handle(int Hkv, int Hq, int Bk, int Bv, aatc_dtype dtype, aatc_c
     h->tab = (CodecTables *)take(L.tabs);
     h->plan = (HeadPlan *)take(L.plans);
     h->dblob = (DecBlob *)take(L.dblob);
+    h->dmat = (uint16_t *)take(L.dmat);
     h->vcst = (float *)take(L.f32_vec);
     p = (char *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);   // T3: TMA source, keep it well aligned
     h->T3 = take(L.t3);

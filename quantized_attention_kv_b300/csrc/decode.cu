@@ -70,7 +70,8 @@ constexpr float RESCALE_T = 8.f; // the running maximum is raised once a score e
 constexpr int MAX_COUNTED = 256;
 constexpr int MERGE_MIN_SLOTS = 8;    // the merge stages at least this many partial slots at a time
 constexpr int MERGE_LD = 8;           // ... and at most MERGE_LD float4 loads per thread per chunk
-constexpr int SCR_CBAR = 256;    // epilogue: c [D][8] starts this many floats into the scratch (after the warp maxima and sums)
+constexpr int SCR_CF = 256;      // epilogue: c [HPG][D] starts this many floats into the scratch (after the warp maxima and sums)
+constexpr int QHS = D + 8;       // halfs per row of the fp16 B operands of the matrix products (padded: no bank conflicts)
 constexpr size_t WS_COUNTERS = MAX_COUNTED * sizeof(unsigned);
 
 // Work split: every (batch row, KV head, head group) is a "unit" of
@@ -107,19 +108,18 @@ FastSmem fast_smem_layout(int FW, int FST, int Wkv, int NT, int ksteps, int grou
     const int HPG = 4 * NT;
     const size_t tiles = (size_t)FW * FST * 128 * Wkv;
     // epilogue in the stage region: the warps' piece sums (packed when a warp's
-    // own stages are too small), later the unit's partial slots (merge) and
-    // the k-quarter partial outputs [4][8][D]
+    // own stages are too small), later the unit's partial slots (merge)
     size_t epi_region = (size_t)FW * 64 * groups * HPG * 4;
-    if (epi_region < (size_t)4 * 8 * D * 4) epi_region = (size_t)4 * 8 * D * 4;
     if (epi_region < (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4) epi_region = (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4;
     m.stages = tiles > epi_region ? tiles : epi_region;
-    m.mat = (size_t)D * D * 4;   // A_k^T, then Uv^T
+    m.mat = (size_t)D * D * 4;   // A_k, then Uv: fp16 hi and lo planes
     m.blob = sizeof(DecBlob);
     m.qtab = (size_t)ksteps * NT * 32 * 8;
     m.pbuf = (size_t)FW * 8 * NT * PSTRIDE * 2;
     m.mbar = (((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15;
-    const size_t pro = ((size_t)D * 8 + (size_t)HPG * D) * 4;   // query rows, q'
-    const size_t epi = ((size_t)SCR_CBAR + D * 8) * 4;           // warp maxima and sums, then c [D][8]
+    const size_t bop = (size_t)NT * 8 * QHS * 2;                     // fp16 B operand: [NT][8][QHS]
+    const size_t pro = (size_t)HPG * D * 4 + bop;                    // q', then the query rows
+    const size_t epi = ((size_t)SCR_CF + (size_t)HPG * D) * 4 + bop;  // warp maxima and sums, c, then c as fp16 hi/lo
     m.scr = pro > epi ? pro : epi;
     m.total = m.stages + m.mat + m.blob + m.qtab + m.pbuf + m.mbar + m.scr;
     return m;
@@ -267,6 +267,24 @@ __device__ __forceinline__ float ex2(float x)
 // Exact power of two 2^e, e in [-126, 127].
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }
 
+// e with 2^e <= x < 2^(e+1) for the bits of a positive normal float x, 0 for
+// x = 0, clamped to [-100, 100].
+__device__ __forceinline__ int pow2_exp(int bits)
+{
+    return bits > 0 ? max(-100, min(100, ((bits >> 23) & 255) - 127)) : 0;
+}
+
+// mma.sync A fragments of the 16 x 16 tile (rows r0.., columns k0..) of a
+// [D][D] fp16 plane stored with 16-byte chunk n of row r at chunk n ^ (r % 8).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&a)[4], const __half *plane, int r0, int k0, int lane)
+{
+    const int q = lane >> 3, r = r0 + (q & 1) * 8 + (lane & 7), ch = (k0 >> 3) + (q >> 1);
+    const __half *p = plane + r * D + ((ch ^ (r & 7)) << 3);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_u32(p)));
+}
+
 struct FastArgs {
     const uint32_t *kp, *vp;
     const int32_t *seq_lens;
@@ -277,9 +295,8 @@ struct FastArgs {
     float *out;             // [B][Hq][D] (single split)
     const float *vcst;      // [Hkv][D] mu_v - Uv (Delta_V o mid) (single split)
     const DecBlob *blob;    // [Hkv]
-    const float *UvT;       // [Hkv][D][D]
+    const __half *mats;     // [Hkv][4][D][D]: A_k hi, lo; Uv hi, lo (the handle's fp16 operand planes)
     const void *q;          // [B][Hq][D] of the handle's dtype
-    const float *AkT;       // [Hkv][D][D]
     float *part;            // [units][S][HPG][PROW]
     unsigned *counter;      // [units] splits counted in so far (0 between calls)
     int merge_slots;        // partial slots the stage region holds at a time (the merge)
@@ -315,14 +332,14 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 
     // shared memory carve-up (as in fast_smem_layout)
     unsigned char *stage_base = smem;
-    float *mat_s = reinterpret_cast<float *>(smem + a.stage_region);   // [D][D]: A_k^T, then Uv^T
-    DecBlob *blob_s = reinterpret_cast<DecBlob *>(mat_s + D * D);
+    unsigned char *mat_s = smem + a.stage_region;   // A_k, then Uv: fp16 [2][D][D] (hi, lo)
+    DecBlob *blob_s = reinterpret_cast<DecBlob *>(mat_s + D * D * 4);
     uint2 *qtab_s = reinterpret_cast<uint2 *>(blob_s + 1);
     __half *pbuf = reinterpret_cast<__half *>(qtab_s + ksteps * NT * 32);
     uint64_t *mbar = reinterpret_cast<uint64_t *>(pbuf + FW * 8 * NT * PSTRIDE);   // [FW][FST], blob, mat
     float *scr = reinterpret_cast<float *>(
         reinterpret_cast<unsigned char *>(mbar) + ((((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15));
-    __shared__ int mxi[8];
+    __shared__ int mxi[8], mxq[8], mxc[8];   // largest |q'|, |q|, |c| per head (float bits)
     __shared__ float cm[8], cl[8];
 
     // ---- this CTA: unit u, split sp, tiles [ta, tb) of the unit
@@ -353,8 +370,14 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         mbar_arrive_expect(blob_bar, (uint32_t)sizeof(DecBlob));
         bulk_g2s(blob_s, a.blob + h, (uint32_t)sizeof(DecBlob), blob_bar);
         mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
-        bulk_g2s(mat_s, a.AkT + (size_t)h * D * D, (uint32_t)(D * D * 4), mat_bar);
+        bulk_g2s(mat_s, a.mats + (size_t)h * 4 * D * D, (uint32_t)(D * D * 4), mat_bar);
     }
+    if (tid < 8) {
+        mxi[tid] = 0;
+        mxq[tid] = 0;
+        mxc[tid] = 0;
+    }
+    __syncthreads();   // (the maxima are zero before any thread raises them)
     // Launched with programmatic dependent launch: everything above reads only
     // the handle; the query, the row lengths, the cache and the workspace may
     // be written by the kernel before this one on the stream.
@@ -447,78 +470,111 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     };
     burst(0, 1);
 
-    float qv[QPER];
-#pragma unroll
-    for (int r = 0; r < QPER; ++r) {
-        uint32_t x;   // bf16 or fp32 bits -> fp32 bits; asm volatile keeps it (the load's first use) after the burst
-        if (sizeof(QT) == 2) asm volatile("shl.b32 %0, %1, 16;" : "=r"(x) : "r"(qraw[r]));
-        else asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(qraw[r]));
-        qv[r] = __uint_as_float(x);
-    }
-
-    // ---- query weights of the head group: q' = (A_k q) o Delta_K / sqrt(d),
-    // scaled per head by a power of two S_i, split into fp16 hi/lo parts and
-    // laid out as mma.sync B fragments.
+    // ---- query weights of the head group: q' = (A_k q) o Delta_K / sqrt(d) on
+    // mma.sync (A = rows of A_k, B = the query rows, both as fp16 hi + lo
+    // parts scaled by powers of two; fp32 accumulation), then scaled per head
+    // by a power of two S_i, split into fp16 hi/lo parts and laid out as
+    // mma.sync B fragments for the tile loop.
     float sc[NT];   // log2-domain score scale of head 4t + c: 2^24 / S_i * log2(e)
     bool ok;
     {
-        float *q_s = scr;              // [D][8] query rows, transposed
-        float *pa = scr + D * 8;       // [HPG][D] q'
+        float *pa = scr;                                          // [HPG][D] q'
+        __half *qh = reinterpret_cast<__half *>(scr + HPG * D);  // [NT][8][QHS]: n-tile t = heads 4t.., hi rows then lo rows
+        float qv[QPER];
+#pragma unroll
+        for (int r = 0; r < QPER; ++r) {
+            uint32_t x;   // bf16 or fp32 bits -> fp32 bits; asm volatile keeps it (the load's first use) after the burst
+            if (sizeof(QT) == 2) asm volatile("shl.b32 %0, %1, 16;" : "=r"(x) : "r"(qraw[r]));
+            else asm volatile("mov.b32 %0, %1;" : "=r"(x) : "r"(qraw[r]));
+            qv[r] = __uint_as_float(x);
+            // a warp's 32 elements belong to one head: its largest |q| per head
+            float mx = fabsf(qv[r]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            const int e = tid + r * NTH;
+            if (lane == 0 && e < HPG * D) atomicMax(&mxq[e >> 7], __float_as_int(mx));
+        }
+        __syncthreads();
+        // B operand: q_i 2^(13 - eq_i), 2^eq_i <= max |q_i| < 2^(eq_i + 1), as fp16 hi + lo
 #pragma unroll
         for (int r = 0; r < QPER; ++r) {
             const int e = tid + r * NTH;
-            if (e < HPG * D) q_s[(e & (D - 1)) * 8 + (e >> 7)] = qv[r];
+            if (e < HPG * D) {
+                const int i = e >> 7, k = e & (D - 1);
+                const float x = qv[r] * pow2i(13 - pow2_exp(mxq[i]));
+                const __half hi = __float2half_rn(x);
+                const __half lo = __float2half_rn(x - __half2float(hi));
+                __half *row = qh + ((i >> 2) * 8 + (i & 3)) * QHS + k;
+                row[0] = hi;
+                row[4 * QHS] = lo;
+            }
         }
-        if (tid < 8) mxi[tid] = 0;
         __syncthreads();
         ok = mbar_wait(mat_bar, 0);
         ok = mbar_wait(blob_bar, 0) && ok;
-        // thread (k-split ks, channel j): sum over rows k = ks, ks + KS, ... of A_k^T[k][j] q_i[k]
-        constexpr int KS = NTH / D;
-        float *red = reinterpret_cast<float *>(pbuf);   // [KS][HPG][D], the P buffers are free until the loop
-        {
-            const int j = tid & (D - 1), ks = tid >> 7;
-            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-            for (int k = ks; k < D; k += KS) {
-                const float av = mat_s[k * D + j];
-                const float4 q0 = *reinterpret_cast<const float4 *>(&q_s[k * 8]);
-                o[0] = fmaf(av, q0.x, o[0]);
-                o[1] = fmaf(av, q0.y, o[1]);
-                o[2] = fmaf(av, q0.z, o[2]);
-                o[3] = fmaf(av, q0.w, o[3]);
-                if (HPG > 4) {
-                    const float4 q1 = *reinterpret_cast<const float4 *>(&q_s[k * 8 + 4]);
-                    o[4] = fmaf(av, q1.x, o[4]);
-                    o[5] = fmaf(av, q1.y, o[5]);
-                    o[6] = fmaf(av, q1.z, o[6]);
-                    o[7] = fmaf(av, q1.w, o[7]);
+        if (warp < 8) {   // warp w: channels 16w .. 16w + 15
+            const __half *Ah = reinterpret_cast<const __half *>(mat_s), *Al = Ah + D * D;
+            float dh[NT][4], dl[NT][4];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t ah[4], al[4];
+                ldsm_x4(ah, Ah, 16 * warp, 16 * ks, lane);
+                ldsm_x4(al, Al, 16 * warp, 16 * ks, lane);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const __half *qb = qh + (t * 8 + g) * QHS + 16 * ks + 2 * c;
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(qb);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(qb + 8);
+                    if (ks == 0) {
+                        mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    } else {
+                        mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    }
                 }
             }
+            // columns 2c, 2c+1: hi parts of heads 4t + 2c, +1 (c < 2) or their lo parts (c >= 2)
+            const int j0 = 16 * warp + g, j1 = j0 + 8;
+            const float k0 = blob_s->ksc[j0], k1 = blob_s->ksc[j1];
 #pragma unroll
-            for (int i = 0; i < HPG; ++i) red[(ks * HPG + i) * D + j] = o[i];
+            for (int t = 0; t < NT; ++t) {
+                float v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    v[q4] = dh[t][q4] + dl[t][q4];
+                    v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
+                }
+                const int i0 = 4 * t + 2 * (c & 1), i1 = i0 + 1;
+                const float s0 = ok ? pow2i(pow2_exp(mxq[i0]) - 13) : 0.f;
+                const float s1 = ok ? pow2i(pow2_exp(mxq[i1]) - 13) : 0.f;
+                const float a00 = v[0] * k0 * s0, a10 = v[1] * k0 * s1, a01 = v[2] * k1 * s0, a11 = v[3] * k1 * s1;
+                if (c < 2) {
+                    pa[i0 * D + j0] = a00;
+                    pa[i1 * D + j0] = a10;
+                    pa[i0 * D + j1] = a01;
+                    pa[i1 * D + j1] = a11;
+                }
+                float m0 = fmaxf(fabsf(a00), fabsf(a01)), m1 = fmaxf(fabsf(a10), fabsf(a11));
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                if (lane < 2) {
+                    atomicMax(&mxi[i0], __float_as_int(m0));
+                    atomicMax(&mxi[i1], __float_as_int(m1));
+                }
+            }
         }
         __syncthreads();
-        // A_k^T is used up: Uv^T comes into the same buffer for the split that
+        // A_k is used up: Uv comes into the same buffer for the split that
         // finishes the unit (the only one, or whichever is counted in last)
         if (tid == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
-            bulk_g2s(mat_s, a.UvT + (size_t)h * D * D, (uint32_t)(D * D * 4), mat_bar);
+            bulk_g2s(mat_s, a.mats + ((size_t)h * 4 + 2) * D * D, (uint32_t)(D * D * 4), mat_bar);
         }
-        // q' = sum over the k-splits, times Delta_K / sqrt(d); largest |q'| per head
-        for (int e = tid; e < HPG * D; e += NTH) {   // a warp's 32 entries share one head
-            const int i = e >> 7, j = e & (D - 1);
-            float v = 0.f;
-            for (int ks = 0; ks < KS; ++ks) v += red[(ks * HPG + i) * D + j];
-            v = ok ? v * blob_s->ksc[j] : 0.f;
-            pa[e] = v;
-            float mx = fabsf(v);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) atomicMax(&mxi[i], __float_as_int(mx));
-        }
-        __syncthreads();
         // S_i = 2^(6 - e_i) with max|q'_i| = f 2^e_i, f in [0.5, 1): weights below 2^(6 + 7)
         auto s_exp = [&](int i) -> int {
             const int bits = mxi[i];
@@ -763,9 +819,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     float *wm = scr;                                          // [FW][HPG]
     float *wl = wm + FW * HPG;                                // [FW][HPG]
     float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG], warp stride wstride
-    const float *UT = mat_s;                                  // [D][D] Uv^T (prefetched)
-    float *cbarT = scr + SCR_CBAR;                            // [D][8] Delta_V o channel sums
-    float *red = reinterpret_cast<float *>(stage_base);       // [4][8][D] k-quarter partial outputs (after the gather)
+    float *cf = scr + SCR_CF;                                 // [HPG][D] c: Delta_V o channel sums
+    __half *ch = reinterpret_cast<__half *>(cf + HPG * D);    // [NT][8][QHS] c as the fp16 B operand
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         float l = l_run[t];
@@ -835,8 +890,12 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         }
         v *= blob_s->vstep[j];
         if (a.single) {
-            cbarT[j * 8 + i] = v;
+            cf[i * D + j] = v;
             if (j == 0) cl[i] = Ls;
+            float mx = fabsf(v);   // a warp's 32 channels share one head
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) atomicMax(&mxc[i], __float_as_int(mx));
         } else {
             Pg[i * PROW + 4 + j] = failed ? 0.f : v;
             if (j < 4) Pg[i * PROW + j] = j == 0 ? (failed ? -INFINITY : M) : j == 1 ? (failed ? 0.f : Ls) : 0.f;
@@ -929,56 +988,81 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             const int e = tid + q * NTH;
             if (e >= HPG * D) break;
             const int i = e >> 7, j = e & (D - 1);
-            cbarT[j * 8 + i] = ar[q];
+            cf[i * D + j] = ar[q];
             if (j == 0) cl[i] = lr[q];
+            float mx = fabsf(ar[q]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) atomicMax(&mxc[i], __float_as_int(mx));
         }
+    }
+    __syncthreads();
+    // ---- o = Uv c / l + (mu_v - Uv (Delta_V o mid)), once per head, on mma.sync:
+    // A = Uv 2^13, B = c_i 2^(13 - ec_i) with 2^ec_i <= max |c_i| < 2^(ec_i + 1),
+    // both as fp16 hi + lo parts, fp32 accumulation
+    for (int e = tid; e < HPG * D; e += NTH) {
+        const int i = e >> 7, k = e & (D - 1);
+        const float x = cf[e] * pow2i(13 - pow2_exp(mxc[i]));
+        const __half hi = __float2half_rn(x);
+        const __half lo = __float2half_rn(x - __half2float(hi));
+        __half *row = ch + ((i >> 2) * 8 + (i & 3)) * QHS + k;
+        row[0] = hi;
+        row[4 * QHS] = lo;
     }
     __syncthreads();
     if (!mbar_wait(mat_bar, 1)) failed = true;
-    {   // thread (k-quarter kq, output j) for every head
-        const int j = tid & (D - 1);
-        for (int kq = tid >> 7; kq < 4; kq += NTH / D) {
-            float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int k = 32 * kq; k < 32 * kq + 32; ++k) {
-                const float uv = UT[k * D + j];
-                const float4 c0 = *reinterpret_cast<const float4 *>(&cbarT[k * 8]);
-                o[0] = fmaf(uv, c0.x, o[0]);
-                o[1] = fmaf(uv, c0.y, o[1]);
-                o[2] = fmaf(uv, c0.z, o[2]);
-                o[3] = fmaf(uv, c0.w, o[3]);
-                if (HPG > 4) {
-                    const float4 c1 = *reinterpret_cast<const float4 *>(&cbarT[k * 8 + 4]);
-                    o[4] = fmaf(uv, c1.x, o[4]);
-                    o[5] = fmaf(uv, c1.y, o[5]);
-                    o[6] = fmaf(uv, c1.z, o[6]);
-                    o[7] = fmaf(uv, c1.w, o[7]);
+    if (warp < 8) {   // warp w: output channels 16w .. 16w + 15
+        const __half *Uh = reinterpret_cast<const __half *>(mat_s), *Ul = Uh + D * D;
+        float dh[NT][4], dl[NT][4];
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t ah[4], al[4];
+            ldsm_x4(ah, Uh, 16 * warp, 16 * ks, lane);
+            ldsm_x4(al, Ul, 16 * warp, 16 * ks, lane);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                const __half *cb = ch + (t * 8 + g) * QHS + 16 * ks + 2 * c;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(cb);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(cb + 8);
+                if (ks == 0) {
+                    mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                    mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                } else {
+                    mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                    mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
                 }
             }
-#pragma unroll
-            for (int i = 0; i < HPG; ++i) red[(kq * 8 + i) * D + j] = o[i];
         }
-    }
-    __syncthreads();
-    // ---- o = Uv c / l + (mu_v - Uv (Delta_V o mid)), once per head
-    {
         const int Hq = a.Hkv * a.G;
-        for (int e = tid; e < HPG * D; e += NTH) {
-            const int i = e >> 7, j = e & (D - 1), gi = hg * HPG + i;
-            const float y = (red[(0 * 8 + i) * D + j] + red[(1 * 8 + i) * D + j]) +
-                            (red[(2 * 8 + i) * D + j] + red[(3 * 8 + i) * D + j]);
-            const float Ls = cl[i];
-            if (gi < a.G)
-                a.out[((size_t)b * Hq + h * a.G + gi) * D + j] =
-                    (Ls > 0.f && !failed) ? y / Ls + a.vcst[h * D + j] : 0.f;
+        const int r0 = 16 * warp + g, r1 = r0 + 8;
+        const float u0 = a.vcst[h * D + r0], u1 = a.vcst[h * D + r1];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            float v[4];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                v[q4] = dh[t][q4] + dl[t][q4];
+                v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
+            }
+            if (c < 2) {   // columns 2c, 2c+1 (hi parts, the lo parts added): heads 4t + 2c, +1
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const int i = 4 * t + 2 * c + (q4 & 1), gi = hg * HPG + i, r = q4 < 2 ? r0 : r1;
+                    const float Ls = cl[i];
+                    if (gi < a.G)
+                        a.out[((size_t)b * Hq + h * a.G + gi) * D + r] =
+                            (Ls > 0.f && !failed) ? v[q4] * pow2i(pow2_exp(mxc[i]) - 26) / Ls + (q4 < 2 ? u0 : u1)
+                                                  : 0.f;
+                }
+            }
         }
     }
 }
 
 // Per-head fast-decoder tables from the plans and codec tables.
 __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTables *__restrict__ tabs, int Wk, int Wv,
-                            const double *__restrict__ Uv, const double *__restrict__ muv, DecBlob *__restrict__ out,
-                            float *__restrict__ vcst)
+                            const double *__restrict__ Ak, const double *__restrict__ Uv, const double *__restrict__ muv,
+                            DecBlob *__restrict__ out, float *__restrict__ vcst, uint16_t *__restrict__ dmat)
 {
     const int h = blockIdx.x, tid = threadIdx.x;
     const HeadPlan &pk = plans[h * 2 + 0];
@@ -1006,8 +1090,39 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
         const int hw = e >> 3, k = e & 7;
         o.vmask[hw][k] = hw < 2 * Wv ? pv.mask[hw][k] : 0u;
     }
-    for (int j = tid; j < D; j += blockDim.x) {
-        o.ksc[j] = tk.bits[j] ? tk.step[j] * 0.08838834764831845f : 0.f;
+    // fp16 operands of the fast decoder's two matrix products, each entry as
+    // an fp16 part and the fp16 rounding of what it leaves (about 22
+    // significant bits): row j of A_k scaled by 2^(13 - e_j), 2^e_j <= its
+    // largest |entry| < 2^(e_j + 1) (the 2^(e_j - 13) goes into ksc_j), and
+    // row j of Uv (entries in [-1, 1]) scaled by 2^13.  16-byte chunk n of a
+    // row r sits at chunk n ^ (r % 8), so that the eight rows an ldmatrix
+    // phase reads fall in distinct shared-memory banks.
+    int e_row[(D + 127) / 128];
+    for (int j = tid, q = 0; j < D; j += blockDim.x, ++q) {
+        const double *ar = Ak + ((size_t)h * D + j) * D;
+        const double *ur = Uv + ((size_t)h * D + j) * D;
+        double mx = 0.0;
+        for (int k = 0; k < D; ++k) mx = fmax(mx, fabs(ar[k]));
+        int ex = 0;
+        if (mx > 0.0) frexp(mx, &ex);
+        const int ej = max(-100, min(100, ex - 1));
+        e_row[q] = ej;
+        const double sa = ldexp(1.0, 13 - ej);
+        uint16_t *Ah = dmat + (size_t)h * 4 * D * D, *Al = Ah + D * D, *Uh = Ah + 2 * D * D, *Ul = Ah + 3 * D * D;
+        for (int k = 0; k < D; ++k) {
+            const int pos = j * D + ((((k >> 3) ^ (j & 7)) << 3) | (k & 7));
+            const double xa = ar[k] * sa, xu = ur[k] * 8192.0;
+            const __half ah = __double2half(xa), uh = __double2half(xu);
+            const __half al = __double2half(xa - (double)__half2float(ah));
+            const __half ul = __double2half(xu - (double)__half2float(uh));
+            Ah[pos] = __half_as_ushort(ah);
+            Al[pos] = __half_as_ushort(al);
+            Uh[pos] = __half_as_ushort(uh);
+            Ul[pos] = __half_as_ushort(ul);
+        }
+    }
+    for (int j = tid, q = 0; j < D; j += blockDim.x, ++q) {
+        o.ksc[j] = tk.bits[j] ? tk.step[j] * 0.08838834764831845f * pow2i(e_row[q] - 13) : 0.f;
         o.vstep[j] = tv.bits[j] ? tv.step[j] : 0.f;
         // value pieces of channel j: row (gr, m4, rr) holds slot 2 m4 + rr / 8 of half-word 8 gr + rr % 8
         int n = 0;
@@ -1337,7 +1452,8 @@ extern "C" aatc_status aatc_test_wait_fault(int skip_tile_copy, int wait_tries)
 
 aatc_status dec_build(aatc_calib *h, cudaStream_t s)
 {
-    k_dec_build<<<h->Hkv, D, 0, s>>>(h->plan, h->tab, h->Wk, h->Wv, h->U_v, h->mu_v, h->dblob, h->vcst);
+    k_dec_build<<<h->Hkv, D, 0, s>>>(h->plan, h->tab, h->Wk, h->Wv, h->A_k, h->U_v, h->mu_v, h->dblob, h->vcst,
+                                     h->dmat);
     AATC_CUDA(cudaGetLastError());
     return AATC_OK;
 }
@@ -1383,14 +1499,13 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         a.single = f.single ? 1 : 0;
         a.out = out;
         a.vcst = h->vcst;
-        a.UvT = h->UvT32;
+        a.mats = reinterpret_cast<const __half *>(h->dmat);
         a.n_tiles = f.n_tiles;
         a.units = f.units;
         a.S = f.S;
         a.tiles_per = f.tiles_per;
         a.blob = h->dblob;
         a.q = q;
-        a.AkT = h->AkT32;
         a.part = part;
         a.counter = f.single ? nullptr : (unsigned *)ws;
         {   // slots per merge chunk: what the stages hold, at most MERGE_LD float4 per thread

@@ -90,7 +90,7 @@ struct HeadPlan {
 struct __align__(16) DecBlob {
     uint32_t kmask[16][8];     // key record word w, slot k: AND mask (0 past the record)
     uint32_t vmask[32][8];     // value half-word e, slot k: AND mask in both halves
-    float ksc[AATC_D];         // Delta_K,j / sqrt(d), 0 for pruned channels
+    float ksc[AATC_D];         // Delta_K,j / sqrt(d) times 2^(e_j - 13) (the row scale of the fp16 A_k rows), 0 for pruned channels
     float vstep[AATC_D];       // Delta_V,j, 0 for pruned channels
     int16_t kslot[16][8][2];   // key piece of (word, slot, half): ch | (ex + 64) << 8, -1 = none
     int16_t vgat[AATC_D][2];   // value channel j: its piece rows, row | (ex + 64) << 8, -1 = none
@@ -129,6 +129,9 @@ struct aatc_calib {
     CodecTables *tab;         // [H][2]
     HeadPlan *plan;           // [H][2] record layout and decode masks
     DecBlob *dblob;           // [H] fast-decoder tables
+    uint16_t *dmat;           // [H][4][d][d] fp16 operands of the fast decoder's matrix products:
+                              // A_k rows scaled by powers of two (hi, lo parts), Uv 2^13 (hi, lo);
+                              // 16-byte chunk n of row r stored at chunk n ^ (r % 8)
     float *vcst;              // [H][d] mu_v - Uv (Delta_V o mid)
     // tensor-core encoder operands (bf16 inputs): T split in three bf16 terms
     // T = T1 + T2 + T3 with rows in record order, [H][2][3][d][d]; and the
