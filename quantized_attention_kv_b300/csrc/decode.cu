@@ -902,20 +902,18 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         }
     }
     if (!a.single) {
-        // count this split in: after the barrier, one thread's release
-        // (fence.acq_rel at GPU scope, then the atomic) publishes the partial
-        // the whole CTA wrote; the split counted in last acquires the others'
-        // partials the same way, merges the unit and puts the counter back to 0
+        // count this split in: after the barrier, one thread's atomic add
+        // with acquire-release semantics at GPU scope publishes the partial the
+        // whole CTA wrote and, for the split counted in last, acquires the
+        // others' partials; that split merges the unit and puts the counter
+        // back to 0
         __syncthreads();
         if (tid == 0) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            const unsigned old = atomicAdd(a.counter + u, 1u);
+            unsigned old;
+            asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counter + u) : "memory");
             if (old >= (unsigned)a.S) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
             const bool last = old == (unsigned)(a.S - 1);
-            if (last) {
-                asm volatile("fence.acq_rel.gpu;" ::: "memory");
-                a.counter[u] = 0u;
-            }
+            if (last) a.counter[u] = 0u;
             mxi[0] = last;
         }
         __syncthreads();
