@@ -37,8 +37,22 @@ from quantized_attention_kv_b300 import synth  # noqa: E402
 
 # decode call: one kernel when every (row, KV head group) has a single split
 # (the call then needs no workspace), else split kernel + combine kernel
-def _decode_kernels_per_call(ws_bytes):
-    return 1 if ws_bytes == 0 else 2
+def _kernel_nodes(g):
+    """Kernel nodes of a captured CUDA graph (kept with keep_graph=True), or None."""
+    try:
+        from cuda.bindings import runtime as rt
+        graph = rt.cudaGraph_t(init_value=int(g.raw_cuda_graph()))
+        err, _, n = rt.cudaGraphGetNodes(graph, 0)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        err, nodes, n = rt.cudaGraphGetNodes(graph, n)
+        if err != rt.cudaError_t.cudaSuccess:
+            return None
+        kinds = [rt.cudaGraphNodeGetType(nd)[1] for nd in nodes[:n]]
+        return sum(1 for k_ in kinds if k_ == rt.cudaGraphNodeType.cudaGraphNodeTypeKernel)
+    except Exception:
+        return None
+
 L2_BYTES = 126 << 20
 ENCODE_KERNELS_PER_CALL = 1
 
@@ -207,9 +221,15 @@ def run_ours(args, ws, rank, local):
             aatc.decode_attention_paged(cal, q_, kp, vp, table, L + 1, out=out, workspace=wsb)
         else:
             aatc.decode_attention(cal, q_, kp, vp, L + 1, out=out, workspace=wsb)
+    def fused(q_, kn_, vn_, kp, vp):
+        """A serving step's append + decode: one fused call (the paged cache: the two calls)."""
+        if args.paged:
+            enc(kn_, vn_, kp, vp, L)
+            dec(q_, kp, vp)
+        else:
+            aatc.append_decode_attention(cal, kn_, vn_, q_, kp, vp, L, out=out, workspace=wsb)
     out = torch.empty(B, Hq, 128, dtype=torch.float32, device=dev)
-    ws_need = aatc.workspace_size(cal, B, L + 1)
-    wsb = aatc.new_workspace(cal, B, L + 1, device=dev)
+    wsb = aatc.new_append_workspace(cal, B, L, 1, device=dev)   # serves the decode-only calls too
     for kp, vp in zip(kps, vps):        # every copy holds a valid cache
         enc(kc, vc, kp, vp, 0)
         enc(kn, vn, kp, vp, L)
@@ -222,10 +242,9 @@ def run_ours(args, ws, rank, local):
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     def step(c):
-        """One step on cache copy c: prefill encode, append one token, decode."""
+        """One step on cache copy c: prefill encode, then a serving step (append one token and decode)."""
         enc(kc, vc, kps[c], vps[c], 0)
-        enc(kn, vn, kps[c], vps[c], L)
-        dec(q, kps[c], vps[c])
+        fused(q, kn, vn, kps[c], vps[c])
 
     # each step is captured once per cache copy into a CUDA graph, so the
     # timed region measures the device, not the Python launch path
@@ -242,11 +261,21 @@ def run_ours(args, ws, rank, local):
     with torch.cuda.graph(g_dec):
         for c in range(n_rot):
             dec(q, kps[c], vps[c])
-    g_app = torch.cuda.CUDAGraph()          # a serving step: append one token, then decode
+    g_app = torch.cuda.CUDAGraph()          # a serving step as two calls: append one token, then decode
     with torch.cuda.graph(g_app):
         for c in range(n_rot):
             enc(kn, vn, kps[c], vps[c], L)
             dec(q, kps[c], vps[c])
+    g_fus = torch.cuda.CUDAGraph()          # a serving step as one call
+    with torch.cuda.graph(g_fus):
+        for c in range(n_rot):
+            fused(q, kn, vn, kps[c], vps[c])
+    # the kernels one timed step launches, counted in a capture of it
+    g_cnt = torch.cuda.CUDAGraph(keep_graph=True)
+    with torch.cuda.graph(g_cnt):
+        step(0)
+    launches_per_step = _kernel_nodes(g_cnt)
+    del g_cnt
     g_enc = torch.cuda.CUDAGraph()          # prefill encode alone, every copy once
     with torch.cuda.graph(g_enc):
         for c in range(n_rot):
@@ -282,18 +311,15 @@ def run_ours(args, ws, rank, local):
         t0 = time.perf_counter()
         dbuf.copy_(hbuf, non_blocking=True)
         t1 = time.perf_counter()
-        enc(knd, vnd, kp, vp, L)
-        t2 = time.perf_counter()
-        dec(qd, kp, vp)
-        t3 = time.perf_counter()
+        fused(qd, knd, vnd, kp, vp)
+        t2 = t3 = time.perf_counter()
         outh.copy_(out, non_blocking=True)
         t4 = time.perf_counter()
         if evs:
             evs[1].record(stream)
         if host is not None:
             host["h2d"] += t1 - t0
-            host["append"] += t2 - t1
-            host["decode"] += t3 - t2
+            host["append_decode"] += t3 - t1
             host["d2h"] += t4 - t3
 
     # warm-up, then at least 100 timed steps: the host path reaches a steady
@@ -303,7 +329,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     n_e2e = max(100, args.steps)
     e2e_evs = [[ev() for _ in range(2)] for _ in range(n_e2e)]
-    host = {"h2d": 0.0, "append": 0.0, "decode": 0.0, "d2h": 0.0}
+    host = {"h2d": 0.0, "append_decode": 0.0, "d2h": 0.0}
     w0 = time.perf_counter()
     for s in range(n_e2e):
         e2e_step(e2e_evs[s], c=s, host=host)
@@ -348,6 +374,7 @@ def run_ours(args, ws, rank, local):
 
         dec_t = timed(g_dec)
         app_t = timed(g_app)
+        fus_t = timed(g_fus)
         enc_t = timed(g_enc)
 
     def pct(v, q):
@@ -356,10 +383,12 @@ def run_ours(args, ws, rank, local):
     dec_call_s = _max_over_ranks(pct(dec_t, 0.5), ws)
     enc_call_s = _max_over_ranks(pct(enc_t, 0.5), ws)
     app_call_s = _max_over_ranks(pct(app_t, 0.5), ws)
+    fus_call_s = _max_over_ranks(pct(fus_t, 0.5), ws)
     wall = _max_over_ranks(wall, ws)
     spread = {name: {"p10_us": round(pct(v, 0.1) * 1e6, 3), "median_us": round(pct(v, 0.5) * 1e6, 3),
                      "p90_us": round(pct(v, 0.9) * 1e6, 3), "calls": len(v) * n_rot, "replays": len(v)}
-              for name, v in (("decode", dec_t), ("append_decode", app_t), ("encode", enc_t))}
+              for name, v in (("decode", dec_t), ("append_decode", app_t), ("append_decode_fused", fus_t),
+                              ("encode", enc_t))}
     kp, vp = kps[0], vps[0]
 
     h2d = sum(nbytes_in)
@@ -401,11 +430,13 @@ def run_ours(args, ws, rank, local):
                                  2)},
         "decode_us": round(per_launch_s * 1e6, 3),
         "append_decode_us": round(app_call_s * 1e6, 3),
+        "append_decode_fused_us": round(fus_call_s * 1e6, 3),
         "call_times": spread,
         "calibrate_ms": round(calib_ms, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic(decode_bytes),
-                     "kernel": "decode_attention call (k_decode_fast%s)" % ("" if ws_need == 0 else " + k_decode_combine_fast"),
+                     "kernel": "decode_attention call (%s)" % ("k_decode_fast, one launch" if cal.decode_launches() == 1
+                                                               else "query prep + splits + combine"),
                      "peak_kind": peak_kind},
         "e2e": {"value": round(decode_bytes * ws / e2e_step_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -413,9 +444,11 @@ def run_ours(args, ws, rank, local):
                 "steps": n_e2e, "host_us_per_call": host,
                 "what": "median over steps of the device time from before the H2D copy of the step's query "
                         "and new key/value token (one pinned buffer) to after the D2H copy of the output, "
-                        "through the Python API (append encode, decode attention); calls are enqueued back "
+                        "through the Python API (append_decode_attention: the new token encoded and the "
+                        "decode attention, one call); calls are enqueued back "
                         "to back"},
-        "gpu_launches": args.steps * (2 * ENCODE_KERNELS_PER_CALL + _decode_kernels_per_call(ws_need)),
+        "gpu_launches": args.steps * (launches_per_step if launches_per_step is not None
+                                      else ENCODE_KERNELS_PER_CALL + cal.decode_launches() + (1 if args.paged else 0)),
         "n_cache_copies": n_rot,
         "clocks": clk.summary(),
     }

@@ -17,6 +17,9 @@
  *          weighted by the query, value error by the attention weights).
  *   [IMPL] same page, "End-to-End Implementation" (calibrate, rotate,
  *          quantize per channel).
+ *   [SERVE] same page, "Deployment Guide: Integrating AATC with vLLM"
+ *          (offline calibration, then a serving engine's decode steps on
+ *          the compressed cache).
  *   [NOVA] "Spend Bits Where Queries Look: KV Cache Vector Quantization with
  *          Attention-Preserving Transforms", Abstract: non-orthogonal key
  *          transform (generalized Parseval), fixed per-token bit count,
@@ -215,7 +218,34 @@ aatc_status aatc_decode_attention_static(const aatc_calib *calib, const void *q,
                                          int L_cap, const int32_t *seq_lens, int L, int B,
                                          float *out, void *stream);
 
-/* Paged cache ([IMPL] serving integration; the layout is this library's).
+/* One decode step of a serving engine in one launch ([SERVE]: the cache
+ * grows by each step's new tokens and every step reads it once).  Equivalent to
+ *   aatc_encode(calib, k_new, v_new, B, n_new, L_old, L_cap, k_packed, v_packed, stream);
+ *   aatc_decode_attention(calib, q, k_packed, v_packed, L_cap, NULL, L_old + n_new, B, out, ...);
+ * (the same records written, the same output up to fp32 rounding order),
+ * done by one kernel: the decode splits attend the L_old cached tokens while
+ * extra CTAs of the same launch encode each (row, KV head)'s n_new tokens
+ * (k_new, v_new: device [B][H_kv][n_new][128] of the handle's dtype), write
+ * their records at positions L_old .. L_old + n_new - 1, and add the new
+ * tokens' attention to the merge as one more partial; no CTA waits for
+ * another.  workspace: aatc_append_decode_workspace_size(calib, B, L_old,
+ * n_new) bytes, zeroed before its first use (as for aatc_decode_attention;
+ * the two may share one workspace).  Shapes the fused kernel does not serve
+ * (n_new > 16, records that take the general decode path, more than 256
+ * (row, KV head group) pairs) run the two calls above instead.  n_new = 0
+ * is aatc_decode_attention over L_old tokens.
+ * Errors: as aatc_encode and aatc_decode_attention; CAPACITY if
+ * L_old + n_new > L_cap. */
+aatc_status aatc_append_decode_attention(const aatc_calib *calib, const void *k_new, const void *v_new, int n_new,
+                                         const void *q, uint32_t *k_packed, uint32_t *v_packed, int L_cap,
+                                         int L_old, int B, float *out, void *workspace, size_t ws_bytes,
+                                         void *stream);
+
+/* Bytes of workspace aatc_append_decode_attention needs (0 on invalid
+ * arguments or when it needs none). */
+size_t aatc_append_decode_workspace_size(const aatc_calib *calib, int B, int L_old, int n_new);
+
+/* Paged cache ([SERVE]; the layout is this library's).
  * A pool holds n_blocks blocks.  Block p holds block_tokens tokens (32
  * times a power of two: 32, 64, 128, ...) of every KV head: head h of block p is the
  * block_tokens*W words starting at word (p*H_kv + h)*block_tokens*W, tiled
@@ -258,6 +288,13 @@ aatc_status aatc_encode_paged(const aatc_calib *calib, const void *k, const void
 aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, const uint32_t *k_pool,
                                         const uint32_t *v_pool, const aatc_pages *pages, const int32_t *seq_lens,
                                         int L, int B, float *out, void *workspace, size_t ws_bytes, void *stream);
+
+/* Kernels one aatc_decode_attention (or _paged, or _static) call of this
+ * handle launches when it has tokens to attend: 1 on the fast path, 3 on the
+ * general path (query prep, splits, combine); 0 for a NULL handle.  An
+ * aatc_append_decode_attention call launches 1 when its fused kernel serves
+ * it. */
+int aatc_decode_launches(const aatc_calib *calib);
 
 /* Testing hook (no counterpart in the method): makes a bounded wait inside
  * the decode kernels give up, to exercise the TIMEOUT report without

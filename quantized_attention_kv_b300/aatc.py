@@ -29,7 +29,8 @@ BLOB_MAGIC, BLOB_VERSION = 0x43544141, 2
 EXPORTED = ["aatc_calibrate", "aatc_encode", "aatc_decode_attention", "aatc_decode_workspace_size",
             "aatc_encode_paged", "aatc_decode_attention_paged",
             "aatc_record_words", "aatc_record_words_kv", "aatc_export_calib", "aatc_import_calib", "aatc_check",
-            "aatc_free", "aatc_last_error", "aatc_test_wait_fault"]
+            "aatc_free", "aatc_last_error", "aatc_test_wait_fault", "aatc_append_decode_attention",
+            "aatc_append_decode_workspace_size", "aatc_decode_launches"]
 
 
 class AatcError(RuntimeError):
@@ -76,6 +77,9 @@ def lib():
             "aatc_free": (None, [P]),
             "aatc_last_error": (ctypes.c_char_p, []),
             "aatc_test_wait_fault": (I, [I, I]),
+            "aatc_append_decode_attention": (I, [P, P, P, I, P, P, P, I, I, I, P, P, S, P]),
+            "aatc_append_decode_workspace_size": (S, [P, I, I, I]),
+            "aatc_decode_launches": (I, [P]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -168,6 +172,10 @@ class Calib:
 
     def check(self):
         _check(lib().aatc_check(self.handle))
+
+    def decode_launches(self) -> int:
+        """Kernels one decode_attention call launches (1: fast path, 3: general path)."""
+        return int(lib().aatc_decode_launches(self.handle))
 
     def export(self) -> dict:
         """The calibration as numpy arrays (via aatc_export_calib)."""
@@ -304,6 +312,36 @@ def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_pa
     _check(lib().aatc_decode_attention(calib.handle, _ptr(q), _ptr(k_packed), _ptr(v_packed), k_packed.shape[2],
                                        _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
+    return out
+
+
+def append_workspace_size(calib: Calib, B: int, L_old: int, n_new: int) -> int:
+    return int(lib().aatc_append_decode_workspace_size(calib.handle, B, L_old, n_new))
+
+
+def new_append_workspace(calib: Calib, B: int, L_old: int, n_new: int, device="cuda") -> torch.Tensor:
+    """A zeroed workspace for append_decode_attention (it may also serve decode_attention)."""
+    n = max(append_workspace_size(calib, B, L_old, n_new), workspace_size(calib, B, L_old + n_new), 16)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def append_decode_attention(calib: Calib, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+                            k_packed: torch.Tensor, v_packed: torch.Tensor, L_old: int,
+                            out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            stream=None) -> torch.Tensor:
+    """aatc_append_decode_attention: one decode step in one launch -- the
+    n_new tokens k_new, v_new [B][H_kv][n_new][128] are encoded into positions
+    L_old.. of the caches and q [B][H_q][128] attends all L_old + n_new tokens."""
+    B, H, n_new, _ = k_new.shape
+    _check_cache(calib, B, k_packed, v_packed)
+    if out is None:
+        out = torch.empty(B, calib.n_q_heads, D, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = new_append_workspace(calib, B, L_old, n_new, q.device)
+    _check(lib().aatc_append_decode_attention(calib.handle, _ptr(k_new), _ptr(v_new), n_new, _ptr(q),
+                                              _ptr(k_packed), _ptr(v_packed), k_packed.shape[2], int(L_old), B,
+                                              _ptr(out), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                              _stream(stream, q.device)))
     return out
 
 

@@ -40,7 +40,7 @@ Layout layout_for(int H)
     L.dmat = up((size_t)H * 4 * D * D * 2);
     L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
     L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
-    L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 4 * L.f32_mat + L.tabs +
+    L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 6 * L.f32_mat + L.tabs +
               L.plans + L.dblob + L.dmat + L.f32_vec + L.t3 + L.cols + 1024 + 2 * L.f64_vec;
     return L;
 }
@@ -86,6 +86,7 @@ aatc_status new_handle(int Hkv, int Hq, int Bk, int Bv, aatc_dtype dtype, aatc_c
     h->Tv32 = (float *)take(L.f32_mat);
     h->AkT32 = (float *)take(L.f32_mat);
     h->UvT32 = (float *)take(L.f32_mat);
+    h->TkvT32 = (float *)take(2 * L.f32_mat);
     h->tab = (CodecTables *)take(L.tabs);
     h->plan = (HeadPlan *)take(L.plans);
     h->dblob = (DecBlob *)take(L.dblob);
@@ -348,6 +349,36 @@ aatc_status aatc_decode_attention(const aatc_calib *calib, const void *q, const 
         return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);
     return decode_run(calib, q, k_packed, v_packed, contiguous_map(L_cap), seq_lens, L, B, out, workspace,
                       ws_bytes, (cudaStream_t)stream);
+}
+
+aatc_status aatc_append_decode_attention(const aatc_calib *calib, const void *k_new, const void *v_new, int n_new,
+                                         const void *q, uint32_t *k_packed, uint32_t *v_packed, int L_cap,
+                                         int L_old, int B, float *out, void *workspace, size_t ws_bytes,
+                                         void *stream)
+{
+    g_err[0] = 0;
+    if (!calib) return aatc_fail(AATC_ERR_INVALID_ARG, "calib is NULL");
+    if (n_new < 0 || L_old < 0) return aatc_fail(AATC_ERR_INVALID_ARG, "negative size");
+    if (B > 32767 || n_new > (1 << 28) || L_old > (1 << 28)) return aatc_fail(AATC_ERR_INVALID_ARG, "size too large");
+    const int L = L_old + n_new;
+    aatc_status st = decode_check_args(calib, q, k_packed, v_packed, L_cap, nullptr, L, B, out);
+    if (st != AATC_OK || B == 0) return st;
+    if (n_new > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "k_new and v_new must be non-NULL and 16-byte aligned");
+    const size_t need = n_new > 0 ? append_decode_ws_bytes(calib, B, L_old, n_new) : decode_ws_bytes(calib, B, L);
+    if (need > 0 && (!workspace || !aligned16(workspace) || ws_bytes < need))
+        return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes (16-byte aligned) required", need);
+    if (n_new == 0)
+        return decode_run(calib, q, k_packed, v_packed, contiguous_map(L_cap), nullptr, L, B, out, workspace,
+                          ws_bytes, (cudaStream_t)stream);
+    return append_decode_run(calib, k_new, v_new, n_new, q, k_packed, v_packed, contiguous_map(L_cap), L_old, B,
+                             out, workspace, ws_bytes, (cudaStream_t)stream);
+}
+
+size_t aatc_append_decode_workspace_size(const aatc_calib *calib, int B, int L_old, int n_new)
+{
+    if (!calib || B < 0 || L_old < 0 || n_new < 0 || L_old > (1 << 28) || n_new > (1 << 28)) return 0;
+    return n_new > 0 ? append_decode_ws_bytes(calib, B, L_old, n_new) : decode_ws_bytes(calib, B, L_old);
 }
 
 aatc_status aatc_decode_attention_paged(const aatc_calib *calib, const void *q, const uint32_t *k_pool,

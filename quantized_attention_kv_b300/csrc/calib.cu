@@ -778,6 +778,14 @@ __global__ void k_to_f32_t(const double *__restrict__ x, float *__restrict__ y)
     y[((size_t)h * D + c) * D + r] = (float)x[((size_t)h * D + r) * D + c];
 }
 
+// y[h][t][c][r] = T_t[h][r][c] in fp32: each head's two transforms, transposed, side by side
+__global__ void k_to_f32_t2(const double *__restrict__ Tk, const double *__restrict__ Tv, float *__restrict__ y)
+{
+    const int h = blockIdx.y, t = blockIdx.z, r = blockIdx.x, c = threadIdx.x;
+    const double *x = t ? Tv : Tk;
+    y[(((size_t)h * 2 + t) * D + c) * D + r] = (float)x[((size_t)h * D + r) * D + c];
+}
+
 __global__ void k_to_f32(const double *__restrict__ x, float *__restrict__ y, size_t n)
 {
     size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -957,6 +965,7 @@ aatc_status calib_derive(aatc_calib *h, cudaStream_t s)
     k_to_f32<<<blocks, 256, 0, s>>>(h->T_v, h->Tv32, n);
     k_to_f32_t<<<dim3(D, H), D, 0, s>>>(h->A_k, h->AkT32);
     k_to_f32_t<<<dim3(D, H), D, 0, s>>>(h->U_v, h->UvT32);
+    k_to_f32_t2<<<dim3(D, H, 2), D, 0, s>>>(h->T_k, h->T_v, h->TkvT32);
     k_to_f32<<<(H * D + 255) / 256, 256, 0, s>>>(h->mu_v, h->muv32, (size_t)H * D);
     k_tables<<<dim3(H, 2), D, 0, s>>>(h->bits_k, h->bits_v, h->step_k, h->step_v, h->T_k, h->T_v,
                                       h->mu_k, h->mu_v, h->tab, h->bk32, h->bv32);

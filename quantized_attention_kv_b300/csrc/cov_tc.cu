@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(128, 1) k_cov_tc(const __grid_constant__ CUten
                                                    int nchunk, float *__restrict__ part, uint32_t *status)
 {
     extern __shared__ unsigned char sm_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned in the shared window; derived from sm_raw by pointer arithmetic so that
+    // every access through it compiles to a shared-memory instruction
+    unsigned char *sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     __shared__ __align__(8) uint64_t full[2], empty[2], done;
     __shared__ uint32_t tmem_base;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -72,6 +72,14 @@ constexpr int MERGE_MIN_SLOTS = 8;    // the merge stages at least this many par
 constexpr int MERGE_LD = 8;           // ... and at most MERGE_LD float4 loads per thread per chunk
 constexpr int SCR_CF = 256;      // epilogue: c [HPG][D] starts this many floats into the scratch (after the warp maxima and sums)
 constexpr int QHS = D + 8;       // halfs per row of the fp16 B operands of the matrix products (padded: no bank conflicts)
+// appender CTAs (fused append): tokens per row, padded row of T, record words
+constexpr int APP_MAX = 4;
+constexpr int APP_PAIRS = 4;      // (KV head, row) pairs per appender CTA at most
+constexpr int APP_TAILS = 64;     // units an appender may have to finish (APP_PAIRS x head groups)
+constexpr int APP_RW = FAST_MAX_W;
+constexpr size_t APP_TT = (size_t)2 * D * D * 4;   // the two transposed transforms, in the stage region
+constexpr size_t APP_PB = (size_t)2 * APP_MAX * D * 4 + 8 * APP_MAX * 4 + (size_t)2 * APP_MAX * D * 2 +
+                          (size_t)2 * APP_MAX * APP_RW * 4;   // tokens, scores, codes, records, in the P buffers
 constexpr size_t WS_COUNTERS = MAX_COUNTED * sizeof(unsigned);
 
 // Work split: every (batch row, KV head, head group) is a "unit" of
@@ -92,6 +100,8 @@ struct FastGeom {
     int units;       // B * Hkv * HG
     int S;           // splits (CTAs, partial slots) per unit
     int tiles_per;   // tiles per split
+    int n_app;       // appender CTAs after the splits' (fused append; 0 otherwise)
+    int grid;        // CTAs: units * S + n_app
     size_t stage_bytes, stage_region, smem, ws_total;
     bool single;     // one split per unit: the split kernel writes the output itself
 };
@@ -159,7 +169,63 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.tiles_per = f.n_tiles > 0 ? (f.n_tiles + f.S - 1) / f.S : 1;
     f.S = f.n_tiles > 0 ? (f.n_tiles + f.tiles_per - 1) / f.tiles_per : 1;
     f.ws_total = f.single ? 0 : WS_COUNTERS + ((((size_t)f.units * f.S * f.HPG * PROW * 4) + 255) & ~(size_t)255);
+    f.n_app = 0;
+    f.grid = f.units * f.S;
     return f;
+}
+
+// Fused append + decode: the splits of a plain decode over the L_old cached
+// tokens and appender CTAs on the SMs left over, each taking a contiguous run
+// of the (KV head, row) pairs; one more partial slot per unit for the new
+// tokens.  An appender takes about 5 us per pair, so it must not outlast the
+// splits: with fewer SMs left over than pairs, the appenders keep several
+// pairs each only when the splits have at least 64 tiles each per pair (about
+// 8 us); otherwise the splits give up SMs so that every pair has an appender,
+// if at least two splits per unit remain (n_app = 0: the shape is not fused).
+// S = 0 (no split CTAs) when L_old = 0.
+FastGeom fast_geom_append(const aatc_calib *h, int B, int L_old)
+{
+    FastGeom f = fast_geom(h, B, L_old > 0 ? L_old : 1);
+    f.n_tiles = (L_old + TILE - 1) / TILE;
+    const int per_sm = fast_ctas_per_sm(f.GMAX, f.NT, f.FW, f.smem);
+    const int C = sm_count() * per_sm, pairs = B * h->Hkv;
+    if (f.n_tiles == 0) {
+        f.S = 0;
+        f.tiles_per = 1;
+        f.n_app = min(pairs, C);
+    } else {
+        const int left = C - f.units * f.S;
+        const int ppa = left > 0 ? (pairs + left - 1) / left : pairs;
+        if (left >= pairs) {
+            f.n_app = pairs;
+        } else if (left > 0 && f.tiles_per >= 64 * ppa) {
+            f.n_app = left;
+        } else {
+            const int S2 = min((C - pairs) / f.units, f.n_tiles);
+            f.n_app = 0;
+            if (S2 >= 2) {
+                f.tiles_per = (f.n_tiles + S2 - 1) / S2;
+                f.S = (f.n_tiles + f.tiles_per - 1) / f.tiles_per;
+                f.n_app = pairs;
+            }
+        }
+    }
+    f.grid = f.units * f.S + f.n_app;
+    f.ws_total = WS_COUNTERS + ((((size_t)f.units * (f.S + 1) * f.HPG * PROW * 4) + 255) & ~(size_t)255);
+    return f;
+}
+
+// The appender CTAs need their staging in the stage region, the unit counters
+// and at most APP_MAX new tokens per row.
+// and at most APP_MAX new tokens per row.  The fused kernel pays where the
+// splits' merge is there anyway (several splits per unit, or no cached tokens)
+// and each appender takes at most APP_PAIRS pairs, so that the appenders finish
+// inside the splits' time.
+bool fused_append_fits(const aatc_calib *h, const FastGeom &f, int B, int n_new)
+{
+    const size_t pbuf = (size_t)f.FW * 8 * f.NT * PSTRIDE * 2;
+    return n_new >= 1 && n_new <= APP_MAX && f.stage_region >= APP_TT && pbuf >= APP_PB && f.units <= MAX_COUNTED &&
+           (long)B * f.HG <= 65535 && f.S != 1 && f.n_app > 0 && (long)B * h->Hkv <= (long)APP_PAIRS * f.n_app;
 }
 
 bool fast_ok(const aatc_calib *h) { return h->Wk <= FAST_MAX_W && h->Wv <= FAST_MAX_W && h->fast_layout; }
@@ -274,6 +340,13 @@ __device__ __forceinline__ int pow2_exp(int bits)
     return bits > 0 ? max(-100, min(100, ((bits >> 23) & 255) - 127)) : 0;
 }
 
+// Tile word of record word w of token i (0..31) of a key tile of W-word records.
+__device__ __forceinline__ int key_tile_word(int i, int w, int W)
+{
+    const int r = w >> 2, nr = min(4, W - 4 * r), ii = i & 15;
+    return 16 * W * (i >> 4) + 64 * r + (ii >> 1) * 2 * nr + 2 * (w - 4 * r) + (ii & 1);
+}
+
 // mma.sync A fragments of the 16 x 16 tile (rows r0.., columns k0..) of a
 // [D][D] fp16 plane stored with 16-byte chunk n of row r at chunk n ^ (r % 8).
 __device__ __forceinline__ void ldsm_x4(uint32_t (&a)[4], const __half *plane, int r0, int k0, int lane)
@@ -287,9 +360,21 @@ __device__ __forceinline__ void ldsm_x4(uint32_t (&a)[4], const __half *plane, i
 
 struct FastArgs {
     const uint32_t *kp, *vp;
+    uint32_t *kw, *vw;      // the same caches, written by the appender CTAs (fused append)
     const int32_t *seq_lens;
     CacheMap map;           // contiguous or paged cache
     int L, Wk, Wv, rows, groups, Hkv, G, HG, FST, n_tiles, units, S, tiles_per;   // Wk / Wv: record words
+    int S_slots;            // partial slots per unit: S, or S + 1 when appender CTAs add one
+    int n_dec;              // CTAs of the decode splits (blockIdx below n_dec); the rest are appenders
+    // fused append (appender CTAs): the n_new tokens of row b and KV head h
+    // at positions L_old .. L_old + n_new - 1 (the splits attend the L = L_old
+    // tokens before them)
+    int B, n_new, L_old;
+    const void *k_new, *v_new;   // [B][Hkv][n_new][D] of the handle's dtype
+    const float *TT;             // [Hkv][2][D][D] transforms T_k, T_v transposed ([k][j], fp32)
+    const float *bk, *bv;        // [Hkv][D] T mu (fp32)
+    const CodecTables *tabs;     // [Hkv][2]
+    const HeadPlan *plans;       // [Hkv][2]
     uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
     int single;             // one split per unit (S = 1): finish here and write out
     float *out;             // [B][Hq][D] (single split)
@@ -339,8 +424,215 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     uint64_t *mbar = reinterpret_cast<uint64_t *>(pbuf + FW * 8 * NT * PSTRIDE);   // [FW][FST], blob, mat
     float *scr = reinterpret_cast<float *>(
         reinterpret_cast<unsigned char *>(mbar) + ((((size_t)FW * FST + 2) * 8 + 15) & ~(size_t)15));
+    uint64_t *blob_bar = mbar + FW * FST;
+    uint64_t *mat_bar = blob_bar + 1;   // splits: phase 0 the A_k planes, phase 1 the Uv planes
     __shared__ int mxi[8], mxq[8], mxc[8];   // largest |q'|, |q|, |c| per head (float bits)
     __shared__ float cm[8], cl[8];
+    float *qpa = scr;                                          // [HPG][D] q'
+    __half *qh = reinterpret_cast<__half *>(scr + HPG * D);   // [NT][8][QHS]: n-tile t = heads 4t.., hi rows then lo rows
+    float *cf = scr + SCR_CF;                                 // [HPG][D] c: Delta_V o channel sums
+    __half *ch = reinterpret_cast<__half *>(cf + HPG * D);    // [NT][8][QHS] c as the fp16 B operand
+    // q'_i = (A_k q_i) o Delta_K / sqrt(d) for the head group on mma.sync, from
+    // the A_k planes in mat_s and the query rows in qh (fp16 hi + lo, head i
+    // scaled by 2^(13 - e(mxq_i))); into qpa, the largest |q'_i| into mxi
+    // merge of a unit's nslots partial slots at Pu, once per head: c = sum_s
+    // 2^(m_s - M) c_s and l likewise, into cf, cl and mxc (zero at entry)
+    auto merge_unit = [&](const float *Pu, int nslots) {
+        // merge, once per head: c = sum_s 2^(m_s - M) c_s and l likewise.  The
+        // unit's partial slots are contiguous: chunks of up to merge_slots of
+        // them come into the stages, every thread loading its share at once
+        // from L2 (ld.global.cg: no stale L1 line), one round trip per chunk;
+        // thread (head i, channel j) merges from shared memory, rescaling its
+        // running sums between chunks.
+        constexpr int EPT = (HPG * D + NTH - 1) / NTH;
+        float Mr[EPT], ar[EPT], lr[EPT];
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+            Mr[q] = -INFINITY;
+            ar[q] = 0.f;
+            lr[q] = 0.f;
+        }
+        float *Ps = reinterpret_cast<float *>(stage_base);
+        for (int c0 = 0; c0 < nslots; c0 += a.merge_slots) {
+            const int n = min(a.merge_slots, nslots - c0);
+            const int nq = n * HPG * PROW / 4;   // float4 of the chunk: at most MERGE_LD per thread
+            const float4 *src4 = reinterpret_cast<const float4 *>(Pu + (size_t)c0 * HPG * PROW);
+            float4 ld[MERGE_LD];   // every load of the chunk in flight at once
+#pragma unroll
+            for (int k = 0; k < MERGE_LD; ++k)
+                if (tid + k * NTH < nq) ld[k] = __ldcg(src4 + tid + k * NTH);
+#pragma unroll
+            for (int k = 0; k < MERGE_LD; ++k)
+                if (tid + k * NTH < nq) reinterpret_cast<float4 *>(Ps)[tid + k * NTH] = ld[k];
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < EPT; ++q) {
+                const int e = tid + q * NTH;
+                if (e >= HPG * D) break;
+                const int i = e >> 7, j = e & (D - 1);
+                const float *pi = Ps + i * PROW;
+                const int sstep = HPG * PROW;
+                float M = Mr[q];
+                for (int s2 = 0; s2 < n; ++s2) M = fmaxf(M, pi[s2 * sstep]);
+                const float r = Mr[q] == -INFINITY ? 0.f : ex2(Mr[q] - M);
+                float a0 = ar[q] * r, a1 = 0.f, l0 = lr[q] * r, l1 = 0.f;
+                int s2 = 0;
+                for (; s2 + 2 <= n; s2 += 2) {
+                    const float m0 = pi[s2 * sstep], m1 = pi[(s2 + 1) * sstep];
+                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
+                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
+                    a1 = fmaf(w1, pi[(s2 + 1) * sstep + 4 + j], a1);
+                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
+                    l1 = fmaf(w1, pi[(s2 + 1) * sstep + 1], l1);
+                }
+                if (s2 < n) {
+                    const float m0 = pi[s2 * sstep];
+                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
+                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
+                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
+                }
+                Mr[q] = M;
+                ar[q] = a0 + a1;
+                lr[q] = l0 + l1;
+            }
+            __syncthreads();   // the chunk's stage is refilled by the next one
+        }
+#pragma unroll
+        for (int q = 0; q < EPT; ++q) {
+            const int e = tid + q * NTH;
+            if (e >= HPG * D) break;
+            const int i = e >> 7, j = e & (D - 1);
+            cf[i * D + j] = ar[q];
+            if (j == 0) cl[i] = lr[q];
+            float mx = fabsf(ar[q]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            if (lane == 0) atomicMax(&mxc[i], __float_as_int(mx));
+        }
+    };
+    // out = Uv c / l + (mu_v - Uv (Delta_V o mid)) for head group hgg of (row bb,
+    // KV head hh) from cf, cl and mxc, with the Uv planes landing in mat_s
+    // (phase `parity` of mat_bar)
+    auto apply_uv = [&](int bb, int hh, int hgg, bool fail, uint32_t parity) {
+        __syncthreads();
+        // ---- o = Uv c / l + (mu_v - Uv (Delta_V o mid)), once per head, on mma.sync:
+        // A = Uv 2^13, B = c_i 2^(13 - ec_i) with 2^ec_i <= max |c_i| < 2^(ec_i + 1),
+        // both as fp16 hi + lo parts, fp32 accumulation
+        for (int e = tid; e < HPG * D; e += NTH) {
+            const int i = e >> 7, k = e & (D - 1);
+            const float x = cf[e] * pow2i(13 - pow2_exp(mxc[i]));
+            const __half hi = __float2half_rn(x);
+            const __half lo = __float2half_rn(x - __half2float(hi));
+            __half *row = ch + ((i >> 2) * 8 + (i & 3)) * QHS + k;
+            row[0] = hi;
+            row[4 * QHS] = lo;
+        }
+        __syncthreads();
+        if (!mbar_wait(mat_bar, parity)) fail = true;
+        if (warp < 8) {   // warp w: output channels 16w .. 16w + 15
+            const __half *Uh = reinterpret_cast<const __half *>(mat_s), *Ul = Uh + D * D;
+            float dh[NT][4], dl[NT][4];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t ah[4], al[4];
+                ldsm_x4(ah, Uh, 16 * warp, 16 * ks, lane);
+                ldsm_x4(al, Ul, 16 * warp, 16 * ks, lane);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const __half *cb = ch + (t * 8 + g) * QHS + 16 * ks + 2 * c;
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(cb);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(cb + 8);
+                    if (ks == 0) {
+                        mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    } else {
+                        mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    }
+                }
+            }
+            const int Hq = a.Hkv * a.G;
+            const int r0 = 16 * warp + g, r1 = r0 + 8;
+            const float u0 = a.vcst[hh * D + r0], u1 = a.vcst[hh * D + r1];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    v[q4] = dh[t][q4] + dl[t][q4];
+                    v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
+                }
+                if (c < 2) {   // columns 2c, 2c+1 (hi parts, the lo parts added): heads 4t + 2c, +1
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int i = 4 * t + 2 * c + (q4 & 1), gi = hgg * HPG + i, r = q4 < 2 ? r0 : r1;
+                        const float Ls = cl[i];
+                        if (gi < a.G)
+                            a.out[((size_t)bb * Hq + hh * a.G + gi) * D + r] =
+                                (Ls > 0.f && !fail) ? v[q4] * pow2i(pow2_exp(mxc[i]) - 26) / Ls + (q4 < 2 ? u0 : u1)
+                                                      : 0.f;
+                    }
+                }
+            }
+        }
+    };
+    auto qprime_mma = [&](bool ok) {
+        if (warp < 8) {   // warp w: channels 16w .. 16w + 15
+            const __half *Ah = reinterpret_cast<const __half *>(mat_s), *Al = Ah + D * D;
+            float dh[NT][4], dl[NT][4];
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                uint32_t ah[4], al[4];
+                ldsm_x4(ah, Ah, 16 * warp, 16 * ks, lane);
+                ldsm_x4(al, Al, 16 * warp, 16 * ks, lane);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    const __half *qb = qh + (t * 8 + g) * QHS + 16 * ks + 2 * c;
+                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(qb);
+                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(qb + 8);
+                    if (ks == 0) {
+                        mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    } else {
+                        mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
+                        mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
+                    }
+                }
+            }
+            // columns 2c, 2c+1: hi parts of heads 4t + 2c, +1 (c < 2) or their lo parts (c >= 2)
+            const int j0 = 16 * warp + g, j1 = j0 + 8;
+            const float k0 = blob_s->ksc[j0], k1 = blob_s->ksc[j1];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float v[4];
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    v[q4] = dh[t][q4] + dl[t][q4];
+                    v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
+                }
+                const int i0 = 4 * t + 2 * (c & 1), i1 = i0 + 1;
+                const float s0 = ok ? pow2i(pow2_exp(mxq[i0]) - 13) : 0.f;
+                const float s1 = ok ? pow2i(pow2_exp(mxq[i1]) - 13) : 0.f;
+                const float a00 = v[0] * k0 * s0, a10 = v[1] * k0 * s1, a01 = v[2] * k1 * s0, a11 = v[3] * k1 * s1;
+                if (c < 2) {
+                    qpa[i0 * D + j0] = a00;
+                    qpa[i1 * D + j0] = a10;
+                    qpa[i0 * D + j1] = a01;
+                    qpa[i1 * D + j1] = a11;
+                }
+                float m0 = fmaxf(fabsf(a00), fabsf(a01)), m1 = fmaxf(fabsf(a10), fabsf(a11));
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+                }
+                if (lane < 2) {
+                    atomicMax(&mxi[i0], __float_as_int(m0));
+                    atomicMax(&mxi[i1], __float_as_int(m1));
+                }
+            }
+        }
+    };
 
     // ---- this CTA: unit u, split sp, tiles [ta, tb) of the unit
     const int u = blockIdx.x / a.S, sp = blockIdx.x % a.S;
@@ -350,8 +642,6 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // first tile of this (row, KV head) in a contiguous cache, in tiles of 32 tokens
     const size_t slab_t = paged ? 0 : ((size_t)b * a.Hkv + h) * (size_t)(a.map.L_cap / TILE);
     uint64_t *my_mbar = mbar + warp * FST;
-    uint64_t *blob_bar = mbar + FW * FST;
-    uint64_t *mat_bar = blob_bar + 1;   // phase 0: A_k^T, phase 1: Uv^T
     unsigned char *my_stage = stage_base + (size_t)warp * FST * SB;
 
     // Barriers first (the init fence waits for the thread's outstanding memory
@@ -366,6 +656,234 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
+    if (blockIdx.x >= a.n_dec) {
+        // ======================================================== appenders
+        // Appender i takes the pairs i P / n_app .. (i + 1) P / n_app - 1 of the
+        // P = B H_kv (KV head, row) pairs (pair p: head p / B, row p % B), so that
+        // consecutive pairs share a head and its tables stay in shared memory.
+        // For each pair it encodes the n_new new tokens as the append encoder
+        // does (fp32 transform, the same operation order), writes their records
+        // into the cache, and leaves their attention -- in the form of a split's
+        // partial -- in slot S of each of the pair's units, counting it in; the
+        // last to count a unit in merges it.  No CTA waits for another.
+        float *TT = reinterpret_cast<float *>(stage_base);                     // [2][D][D]: T_k, T_v as [k][j]
+        float *xs = reinterpret_cast<float *>(pbuf);                           // [2][APP_MAX][D] new keys, values
+        float *ssc = xs + 2 * APP_MAX * D;                                     // [HPG][APP_MAX] scores (log2 domain)
+        int16_t *cod = reinterpret_cast<int16_t *>(ssc + 8 * APP_MAX);         // [2][APP_MAX][D] codes
+        uint32_t *rec = reinterpret_cast<uint32_t *>(cod + 2 * APP_MAX * D);   // [2][APP_MAX][APP_RW] records
+        __shared__ int s_tail[APP_TAILS], s_ntail;   // units this CTA counted in last, finished at the end
+        uint64_t *t_bar = mbar;       // warp 0's first stage barrier: the transforms
+        uint32_t tph = 0, bph = 0, mph = 0;   // next phases of t_bar, blob_bar and mat_bar
+        bool ok = true, bad = false, range = false;
+        const int Hq = a.Hkv * a.G, P = a.B * a.Hkv, n_app = gridDim.x - a.n_dec, ai = blockIdx.x - a.n_dec;
+        const int p0 = (int)((long long)ai * P / n_app), p1 = (int)((long long)(ai + 1) * P / n_app);
+        constexpr int QPA = (HPG * D + NTH - 1) / NTH;
+        // heads whose transforms (TT), table blob and A_k planes (mat_s) are in
+        // shared memory, -1 for none (a merge stages partials over TT; the Uv
+        // planes replace the A_k planes)
+        int hT = -1, hB = -1, hA = -1;
+        auto load = [&](int hh) {   // thread 0: the copies the pair of head hh still needs
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the generic reads of these buffers
+            if (hh != hT) {
+                mbar_arrive_expect(t_bar, (uint32_t)(2 * D * D * 4));
+                bulk_g2s(TT, a.TT + (size_t)hh * 2 * D * D, (uint32_t)(2 * D * D * 4), t_bar);
+            }
+            if (hh != hB) {
+                mbar_arrive_expect(blob_bar, (uint32_t)sizeof(DecBlob));
+                bulk_g2s(blob_s, a.blob + hh, (uint32_t)sizeof(DecBlob), blob_bar);
+            }
+            if (hh != hA) {
+                mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
+                bulk_g2s(mat_s, a.mats + (size_t)hh * 4 * D * D, (uint32_t)(D * D * 4), mat_bar);
+            }
+        };
+        // the first pair's tables are handle data: requested ahead of the wait
+        if (tid == 0) {
+            s_ntail = 0;
+            if (p0 < p1) load(p0 / a.B);
+        }
+        // the new tokens, the query and the cache may be written by the kernel before this one
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        for (int p = p0; p < p1; ++p) {
+            const int ph = p / a.B, pb = p % a.B;
+            if (p > p0 && tid == 0) load(ph);
+            // the pair's new keys and values
+            for (int e = tid; e < 2 * a.n_new * D; e += NTH) {
+                const int t = e / (a.n_new * D), r = e % (a.n_new * D);
+                const QT *x = reinterpret_cast<const QT *>(t ? a.v_new : a.k_new) + ((size_t)pb * a.Hkv + ph) * a.n_new * D;
+                const float xv = to_f32(x[r]);
+                bad |= !isfinite(xv);
+                xs[t * APP_MAX * D + r] = xv;
+            }
+            for (int e = tid; e < 2 * APP_MAX * APP_RW; e += NTH) rec[e] = 0u;
+            __syncthreads();
+            if (ph != hT) {
+                ok = mbar_wait(t_bar, tph) && ok;
+                tph ^= 1u;
+            }
+            if (ph != hB) {
+                ok = mbar_wait(blob_bar, bph) && ok;
+                bph ^= 1u;
+            }
+            if (ph != hA) {
+                ok = mbar_wait(mat_bar, mph) && ok;
+                mph ^= 1u;
+            }
+            hT = hB = hA = ph;
+            if (tid < 2 * D) {   // thread (tensor, channel j): c = T x - T mu, quantized, ORed into the record
+                const int tensor = tid >> 7, j = tid & (D - 1);
+                const CodecTables &tb = a.tabs[ph * 2 + tensor];
+                const float bias = (tensor ? a.bv : a.bk)[ph * D + j];
+                const float inv = tb.inv_step[j], mid = tb.mid[j], top = tb.top[j];
+                const int bits = tb.bits[j], off = a.plans[ph * 2 + tensor].off[j];
+                const float *Tt = TT + (size_t)tensor * D * D;
+                for (int n = 0; n < a.n_new; ++n) {
+                    const float *xr = xs + (tensor * APP_MAX + n) * D;
+                    float acc = 0.f;
+#pragma unroll 8
+                    for (int k = 0; k < D; ++k) acc = fmaf(Tt[k * D + j], xr[k], acc);
+                    uint32_t uq = 0u;
+                    if (bits > 0) {
+                        float vq = fmaf(acc - bias, inv, mid);
+                        vq = fminf(fmaxf(rintf(vq), 0.f), top);
+                        uq = (uint32_t)vq;
+                        uint32_t *rw = rec + (tensor * APP_MAX + n) * APP_RW;
+                        const int sh = off & 31;
+                        atomicOr(&rw[off >> 5], uq << sh);
+                        if (sh + bits > 32) atomicOr(&rw[(off >> 5) + 1], uq >> (32 - sh));
+                    }
+                    cod[(tensor * APP_MAX + n) * D + j] = (int16_t)uq;
+                }
+            }
+            __syncthreads();
+            // the records into the cache, placed as the encoders place them
+            for (int e = tid; e < a.n_new * 3 * (Wk > Wv ? Wk : Wv); e += NTH) {
+                // keys: W_k words per token; values: 2 W_v half-words per token
+                const int per = 3 * (Wk > Wv ? Wk : Wv), n = e / per, r = e % per;
+                const int pos = a.L_old + n;
+                if (r < Wk) {
+                    const long long tw = cache_tile_word(a.map, pb, ph, a.Hkv, Wk, pos >> 5);
+                    if (tw < 0) range = true;
+                    else a.kw[tw + key_tile_word(pos & 31, r, Wk)] = rec[n * APP_RW + r];
+                } else if (r - Wk < 2 * Wv) {
+                    const int jj = r - Wk;
+                    const long long tw = cache_tile_word(a.map, pb, ph, a.Hkv, Wv, pos >> 5);
+                    if (tw < 0) {
+                        range = true;
+                    } else {
+                        const long long word = tw + 16 * jj + ((pos & 31) >> 1);
+                        reinterpret_cast<uint16_t *>(a.vw)[2 * word + (pos & 1)] =
+                            (uint16_t)(rec[(APP_MAX + n) * APP_RW + (jj >> 1)] >> (16 * (jj & 1)));
+                    }
+                }
+            }
+            const int16_t *uk = cod, *uv = cod + APP_MAX * D;
+            for (int hgp = 0; hgp < a.HG; ++hgp) {
+                const int uu = (pb * a.Hkv + ph) * a.HG + hgp;
+                if (tid < 8) {
+                    mxi[tid] = 0;
+                    mxq[tid] = 0;
+                }
+                __syncthreads();
+                // the head group's query rows as the fp16 B operand of q' (as in the splits)
+                float qv[QPA];
+#pragma unroll
+                for (int r = 0; r < QPA; ++r) {
+                    const int e = tid + r * NTH, i = e >> 7, gi = hgp * HPG + i;
+                    qv[r] = (e < HPG * D && gi < a.G)
+                                ? to_f32(reinterpret_cast<const QT *>(a.q)[((size_t)pb * Hq + ph * a.G + gi) * D + (e & (D - 1))])
+                                : 0.f;
+                    float mx = fabsf(qv[r]);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0 && e < HPG * D) atomicMax(&mxq[i], __float_as_int(mx));
+                }
+                __syncthreads();
+#pragma unroll
+                for (int r = 0; r < QPA; ++r) {
+                    const int e = tid + r * NTH;
+                    if (e < HPG * D) {
+                        const int i = e >> 7, k = e & (D - 1);
+                        const float xq = qv[r] * pow2i(13 - pow2_exp(mxq[i]));
+                        const __half hi = __float2half_rn(xq);
+                        const __half lo = __float2half_rn(xq - __half2float(hi));
+                        __half *row = qh + ((i >> 2) * 8 + (i & 3)) * QHS + k;
+                        row[0] = hi;
+                        row[4 * QHS] = lo;
+                    }
+                }
+                __syncthreads();
+                qprime_mma(ok);
+                __syncthreads();
+                // scores of the new tokens in the log2 domain, q'_i . u_n log2(e) (the splits' scale)
+                for (int e = tid; e < HPG * a.n_new; e += NTH) {
+                    const int i = e / a.n_new, n = e % a.n_new;
+                    float sacc = 0.f;
+                    for (int j = 0; j < D; ++j) sacc = fmaf(qpa[i * D + j], (float)uk[n * D + j], sacc);
+                    ssc[i * APP_MAX + n] = sacc * LOG2E;
+                }
+                __syncthreads();
+                // their partial, as a split leaves one: m_i, l_i = sum_n 2^(s_n - m_i + PSH),
+                // c_ij = Delta_V,j sum_n 2^(s_n - m_i + PSH) u_nj
+                float *Pg = a.part + ((size_t)uu * a.S_slots + (a.S_slots - 1)) * HPG * PROW;
+                for (int e = tid; e < HPG * D; e += NTH) {
+                    const int i = e >> 7, j = e & (D - 1);
+                    float M = -INFINITY;
+                    for (int n = 0; n < a.n_new; ++n) M = fmaxf(M, ssc[i * APP_MAX + n]);
+                    float l = 0.f, cacc = 0.f;
+                    for (int n = 0; n < a.n_new; ++n) {
+                        const float pn = ex2(ssc[i * APP_MAX + n] - M + (float)PSH);
+                        l += pn;
+                        cacc = fmaf(pn, (float)uv[n * D + j], cacc);
+                    }
+                    Pg[i * PROW + 4 + j] = ok ? cacc * blob_s->vstep[j] : 0.f;
+                    if (j < 4) Pg[i * PROW + j] = j == 0 ? (ok ? M : -INFINITY) : j == 1 ? (ok ? l : 0.f) : 0.f;
+                }
+                __syncthreads();
+                if (tid == 0) {
+                    unsigned old;
+                    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counter + uu) : "memory");
+                    if (old >= (unsigned)a.S_slots) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
+                    if (old == (unsigned)(a.S_slots - 1)) {   // (read back only after the last pair)
+                        a.counter[uu] = 0u;
+                        if (s_ntail < APP_TAILS) s_tail[s_ntail++] = uu;
+                        else atomicOr(a.status, AATC_DEV_WORKSPACE);
+                    }
+                }
+            }
+            __syncthreads();   // the next pair's copies overwrite what this one read
+        }
+        // the units this CTA counted in last: merge them, Uv of each head into mat_s
+        // (the merge stages partials over TT)
+        const int ntail = s_ntail;
+        int hU = -1;   // the head whose Uv planes mat_s holds
+        for (int k = 0; k < ntail; ++k) {
+            const int uu = s_tail[k], hgp = uu % a.HG, ph = (uu / a.HG) % a.Hkv, pb = uu / (a.HG * a.Hkv);
+            if (ph != hU) {
+                if (tid == 0) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive_expect(mat_bar, (uint32_t)(D * D * 4));
+                    bulk_g2s(mat_s, a.mats + ((size_t)ph * 4 + 2) * D * D, (uint32_t)(D * D * 4), mat_bar);
+                }
+                mph ^= 1u;
+                hU = ph;
+            }
+            if (tid < 8) mxc[tid] = 0;
+            __syncthreads();
+            merge_unit(a.part + (size_t)uu * a.S_slots * HPG * PROW, a.S_slots);
+            apply_uv(pb, ph, hgp, !ok, mph ^ 1u);
+            __syncthreads();
+        }
+        if (!ok) {   // a wait gave up: its copy lands before the shared memory is given back
+            mbar_wait(t_bar, tph ^ 1u);
+            mbar_wait(blob_bar, bph ^ 1u);
+            mbar_wait(mat_bar, mph ^ 1u);
+        }
+        if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, AATC_DEV_NONFINITE);
+        if (range) atomicOr(a.status, AATC_DEV_RANGE);
+        if (!ok && tid == 0) atomicOr(a.status, AATC_DEV_TIMEOUT);
+        return;
+    }
     if (tid == 0) {
         mbar_arrive_expect(blob_bar, (uint32_t)sizeof(DecBlob));
         bulk_g2s(blob_s, a.blob + h, (uint32_t)sizeof(DecBlob), blob_bar);
@@ -478,8 +996,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     float sc[NT];   // log2-domain score scale of head 4t + c: 2^24 / S_i * log2(e)
     bool ok;
     {
-        float *pa = scr;                                          // [HPG][D] q'
-        __half *qh = reinterpret_cast<__half *>(scr + HPG * D);  // [NT][8][QHS]: n-tile t = heads 4t.., hi rows then lo rows
+        float *pa = qpa;
         float qv[QPER];
 #pragma unroll
         for (int r = 0; r < QPER; ++r) {
@@ -512,61 +1029,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         __syncthreads();
         ok = mbar_wait(mat_bar, 0);
         ok = mbar_wait(blob_bar, 0) && ok;
-        if (warp < 8) {   // warp w: channels 16w .. 16w + 15
-            const __half *Ah = reinterpret_cast<const __half *>(mat_s), *Al = Ah + D * D;
-            float dh[NT][4], dl[NT][4];
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                uint32_t ah[4], al[4];
-                ldsm_x4(ah, Ah, 16 * warp, 16 * ks, lane);
-                ldsm_x4(al, Al, 16 * warp, 16 * ks, lane);
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const __half *qb = qh + (t * 8 + g) * QHS + 16 * ks + 2 * c;
-                    const uint32_t b0 = *reinterpret_cast<const uint32_t *>(qb);
-                    const uint32_t b1 = *reinterpret_cast<const uint32_t *>(qb + 8);
-                    if (ks == 0) {
-                        mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
-                        mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
-                    } else {
-                        mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
-                        mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
-                    }
-                }
-            }
-            // columns 2c, 2c+1: hi parts of heads 4t + 2c, +1 (c < 2) or their lo parts (c >= 2)
-            const int j0 = 16 * warp + g, j1 = j0 + 8;
-            const float k0 = blob_s->ksc[j0], k1 = blob_s->ksc[j1];
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                float v[4];
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    v[q4] = dh[t][q4] + dl[t][q4];
-                    v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
-                }
-                const int i0 = 4 * t + 2 * (c & 1), i1 = i0 + 1;
-                const float s0 = ok ? pow2i(pow2_exp(mxq[i0]) - 13) : 0.f;
-                const float s1 = ok ? pow2i(pow2_exp(mxq[i1]) - 13) : 0.f;
-                const float a00 = v[0] * k0 * s0, a10 = v[1] * k0 * s1, a01 = v[2] * k1 * s0, a11 = v[3] * k1 * s1;
-                if (c < 2) {
-                    pa[i0 * D + j0] = a00;
-                    pa[i1 * D + j0] = a10;
-                    pa[i0 * D + j1] = a01;
-                    pa[i1 * D + j1] = a11;
-                }
-                float m0 = fmaxf(fabsf(a00), fabsf(a01)), m1 = fmaxf(fabsf(a10), fabsf(a11));
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-                }
-                if (lane < 2) {
-                    atomicMax(&mxi[i0], __float_as_int(m0));
-                    atomicMax(&mxi[i1], __float_as_int(m1));
-                }
-            }
-        }
+        qprime_mma(ok);
         __syncthreads();
         // A_k is used up: Uv comes into the same buffer for the split that
         // finishes the unit (the only one, or whichever is counted in last)
@@ -819,8 +1282,6 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     float *wm = scr;                                          // [FW][HPG]
     float *wl = wm + FW * HPG;                                // [FW][HPG]
     float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG], warp stride wstride
-    float *cf = scr + SCR_CF;                                 // [HPG][D] c: Delta_V o channel sums
-    __half *ch = reinterpret_cast<__half *>(cf + HPG * D);    // [NT][8][QHS] c as the fp16 B operand
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         float l = l_run[t];
@@ -858,7 +1319,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // channel's pieces: c_ij = Delta_V,j sum_w 2^(m_w - M) sum_t p_t u_tj
     // (both sides carry 2^PSH), straight to the partial slot (several splits)
     // or to shared memory (the unit's only split); l likewise
-    float *Pg = a.part + ((size_t)u * a.S + sp) * HPG * PROW;
+    float *Pg = a.part + ((size_t)u * a.S_slots + sp) * HPG * PROW;
     for (int e = tid; e < HPG * D; e += NTH) {
         const int i = e >> 7, j = e & (D - 1);
         float M = -INFINITY;
@@ -911,8 +1372,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         if (tid == 0) {
             unsigned old;
             asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(a.counter + u) : "memory");
-            if (old >= (unsigned)a.S) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
-            const bool last = old == (unsigned)(a.S - 1);
+            if (old >= (unsigned)a.S_slots) atomicOr(a.status, AATC_DEV_WORKSPACE);   // counters were not zero
+            const bool last = old == (unsigned)(a.S_slots - 1);
             if (last) a.counter[u] = 0u;
             mxi[0] = last;
         }
@@ -921,140 +1382,9 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             mbar_wait(mat_bar, 1);   // (long landed) no copy may be in flight when the CTA exits
             return;
         }
-        // merge, once per head: c = sum_s 2^(m_s - M) c_s and l likewise.  The
-        // unit's partial slots are contiguous: chunks of up to merge_slots of
-        // them come into the stages, every thread loading its share at once
-        // from L2 (ld.global.cg: no stale L1 line), one round trip per chunk;
-        // thread (head i, channel j) merges from shared memory, rescaling its
-        // running sums between chunks.
-        constexpr int EPT = (HPG * D + NTH - 1) / NTH;
-        float Mr[EPT], ar[EPT], lr[EPT];
-#pragma unroll
-        for (int q = 0; q < EPT; ++q) {
-            Mr[q] = -INFINITY;
-            ar[q] = 0.f;
-            lr[q] = 0.f;
-        }
-        const float *Pu = a.part + (size_t)u * a.S * HPG * PROW;
-        float *Ps = reinterpret_cast<float *>(stage_base);
-        for (int c0 = 0; c0 < a.S; c0 += a.merge_slots) {
-            const int n = min(a.merge_slots, a.S - c0);
-            const int nq = n * HPG * PROW / 4;   // float4 of the chunk: at most MERGE_LD per thread
-            const float4 *src4 = reinterpret_cast<const float4 *>(Pu + (size_t)c0 * HPG * PROW);
-            float4 ld[MERGE_LD];   // every load of the chunk in flight at once
-#pragma unroll
-            for (int k = 0; k < MERGE_LD; ++k)
-                if (tid + k * NTH < nq) ld[k] = __ldcg(src4 + tid + k * NTH);
-#pragma unroll
-            for (int k = 0; k < MERGE_LD; ++k)
-                if (tid + k * NTH < nq) reinterpret_cast<float4 *>(Ps)[tid + k * NTH] = ld[k];
-            __syncthreads();
-#pragma unroll
-            for (int q = 0; q < EPT; ++q) {
-                const int e = tid + q * NTH;
-                if (e >= HPG * D) break;
-                const int i = e >> 7, j = e & (D - 1);
-                const float *pi = Ps + i * PROW;
-                const int sstep = HPG * PROW;
-                float M = Mr[q];
-                for (int s2 = 0; s2 < n; ++s2) M = fmaxf(M, pi[s2 * sstep]);
-                const float r = Mr[q] == -INFINITY ? 0.f : ex2(Mr[q] - M);
-                float a0 = ar[q] * r, a1 = 0.f, l0 = lr[q] * r, l1 = 0.f;
-                int s2 = 0;
-                for (; s2 + 2 <= n; s2 += 2) {
-                    const float m0 = pi[s2 * sstep], m1 = pi[(s2 + 1) * sstep];
-                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M), w1 = m1 == -INFINITY ? 0.f : ex2(m1 - M);
-                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
-                    a1 = fmaf(w1, pi[(s2 + 1) * sstep + 4 + j], a1);
-                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
-                    l1 = fmaf(w1, pi[(s2 + 1) * sstep + 1], l1);
-                }
-                if (s2 < n) {
-                    const float m0 = pi[s2 * sstep];
-                    const float w0 = m0 == -INFINITY ? 0.f : ex2(m0 - M);
-                    a0 = fmaf(w0, pi[s2 * sstep + 4 + j], a0);
-                    l0 = fmaf(w0, pi[s2 * sstep + 1], l0);
-                }
-                Mr[q] = M;
-                ar[q] = a0 + a1;
-                lr[q] = l0 + l1;
-            }
-            __syncthreads();   // the chunk's stage is refilled by the next one
-        }
-#pragma unroll
-        for (int q = 0; q < EPT; ++q) {
-            const int e = tid + q * NTH;
-            if (e >= HPG * D) break;
-            const int i = e >> 7, j = e & (D - 1);
-            cf[i * D + j] = ar[q];
-            if (j == 0) cl[i] = lr[q];
-            float mx = fabsf(ar[q]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-            if (lane == 0) atomicMax(&mxc[i], __float_as_int(mx));
-        }
+        merge_unit(a.part + (size_t)u * a.S_slots * HPG * PROW, a.S_slots);
     }
-    __syncthreads();
-    // ---- o = Uv c / l + (mu_v - Uv (Delta_V o mid)), once per head, on mma.sync:
-    // A = Uv 2^13, B = c_i 2^(13 - ec_i) with 2^ec_i <= max |c_i| < 2^(ec_i + 1),
-    // both as fp16 hi + lo parts, fp32 accumulation
-    for (int e = tid; e < HPG * D; e += NTH) {
-        const int i = e >> 7, k = e & (D - 1);
-        const float x = cf[e] * pow2i(13 - pow2_exp(mxc[i]));
-        const __half hi = __float2half_rn(x);
-        const __half lo = __float2half_rn(x - __half2float(hi));
-        __half *row = ch + ((i >> 2) * 8 + (i & 3)) * QHS + k;
-        row[0] = hi;
-        row[4 * QHS] = lo;
-    }
-    __syncthreads();
-    if (!mbar_wait(mat_bar, 1)) failed = true;
-    if (warp < 8) {   // warp w: output channels 16w .. 16w + 15
-        const __half *Uh = reinterpret_cast<const __half *>(mat_s), *Ul = Uh + D * D;
-        float dh[NT][4], dl[NT][4];
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            uint32_t ah[4], al[4];
-            ldsm_x4(ah, Uh, 16 * warp, 16 * ks, lane);
-            ldsm_x4(al, Ul, 16 * warp, 16 * ks, lane);
-#pragma unroll
-            for (int t = 0; t < NT; ++t) {
-                const __half *cb = ch + (t * 8 + g) * QHS + 16 * ks + 2 * c;
-                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(cb);
-                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(cb + 8);
-                if (ks == 0) {
-                    mma16816_z(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
-                    mma16816_z(dl[t], al[0], al[1], al[2], al[3], b0, b1);
-                } else {
-                    mma16816(dh[t], ah[0], ah[1], ah[2], ah[3], b0, b1);
-                    mma16816(dl[t], al[0], al[1], al[2], al[3], b0, b1);
-                }
-            }
-        }
-        const int Hq = a.Hkv * a.G;
-        const int r0 = 16 * warp + g, r1 = r0 + 8;
-        const float u0 = a.vcst[h * D + r0], u1 = a.vcst[h * D + r1];
-#pragma unroll
-        for (int t = 0; t < NT; ++t) {
-            float v[4];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                v[q4] = dh[t][q4] + dl[t][q4];
-                v[q4] += __shfl_xor_sync(0xffffffffu, v[q4], 2);
-            }
-            if (c < 2) {   // columns 2c, 2c+1 (hi parts, the lo parts added): heads 4t + 2c, +1
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    const int i = 4 * t + 2 * c + (q4 & 1), gi = hg * HPG + i, r = q4 < 2 ? r0 : r1;
-                    const float Ls = cl[i];
-                    if (gi < a.G)
-                        a.out[((size_t)b * Hq + h * a.G + gi) * D + r] =
-                            (Ls > 0.f && !failed) ? v[q4] * pow2i(pow2_exp(mxc[i]) - 26) / Ls + (q4 < 2 ? u0 : u1)
-                                                  : 0.f;
-                }
-            }
-        }
-    }
+    apply_uv(b, h, hg, failed, 1u);
 }
 
 // Per-head fast-decoder tables from the plans and codec tables.
@@ -1411,7 +1741,7 @@ aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a,
     // programmatic dependent launch: the prologue that reads only the handle
     // overlaps the tail of the previous kernel on the stream
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(f.units * f.S);
+    cfg.gridDim = dim3(f.grid);
     cfg.blockDim = dim3(FW * 32);
     cfg.dynamicSmemBytes = f.smem;
     cfg.stream = s;
@@ -1439,7 +1769,78 @@ aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cud
 std::atomic<int> g_hook_skip{0};
 std::atomic<int> g_hook_tries{WAIT_TRIES};
 
+
+// Arguments of k_decode_fast for geometry f (a plain decode; the fused append
+// fills in its fields afterwards).
+FastArgs fast_args(const aatc_calib *h, const FastGeom &f, const void *q, const uint32_t *kp, const uint32_t *vp,
+                   const CacheMap &map, const int32_t *seq_lens, int L, int B, float *out, void *ws)
+{
+    FastArgs a;
+    a.kp = kp;
+    a.vp = vp;
+    a.kw = a.vw = nullptr;
+    a.seq_lens = seq_lens;
+    a.L = L;
+    a.map = map;
+    a.Wk = h->Wk;
+    a.Wv = h->Wv;
+    a.rows = f.rows;
+    a.groups = f.groups;
+    a.Hkv = h->Hkv;
+    a.G = h->G;
+    a.HG = f.HG;
+    a.FST = f.FST;
+    a.stage_region = (uint32_t)f.stage_region;
+    a.single = f.single ? 1 : 0;
+    a.out = out;
+    a.vcst = h->vcst;
+    a.mats = reinterpret_cast<const __half *>(h->dmat);
+    a.n_tiles = f.n_tiles;
+    a.units = f.units;
+    a.S = f.S > 0 ? f.S : 1;
+    a.S_slots = f.S;
+    a.n_dec = f.units * f.S;
+    a.B = B;
+    a.n_new = 0;
+    a.L_old = L;
+    a.k_new = a.v_new = nullptr;
+    a.TT = a.bk = a.bv = nullptr;
+    a.tabs = nullptr;
+    a.plans = nullptr;
+    a.tiles_per = f.tiles_per;
+    a.blob = h->dblob;
+    a.q = q;
+    a.part = f.single ? nullptr : (float *)((char *)ws + WS_COUNTERS);
+    a.counter = f.single ? nullptr : (unsigned *)ws;
+    {   // slots per merge chunk: what the stages hold, at most MERGE_LD float4 per thread
+        const int fit = (int)(f.stage_region / ((size_t)f.HPG * PROW * 4));
+        const int ld = MERGE_LD * 4 * (f.FW * 32) / (f.HPG * PROW);
+        a.merge_slots = fit < ld ? fit : ld;
+    }
+    a.status = h->status;
+    a.wait_tries = g_hook_tries.load(std::memory_order_relaxed);
+    a.skip_first_copy = g_hook_skip.load(std::memory_order_relaxed);
+    return a;
+}
+
+aatc_status launch_fast_any(const aatc_calib *h, const FastGeom &f, const FastArgs &a, cudaStream_t s)
+{
+    if (f.NT == 1) {
+        if (f.GMAX == 2) return launch_fast<2, 1, 16>(f, a, h->dtype, s);
+        if (f.GMAX == 3) return launch_fast<3, 1, 16>(f, a, h->dtype, s);
+        return launch_fast<4, 1, 16>(f, a, h->dtype, s);
+    }
+    if (f.GMAX == 2) return launch_fast<2, 2, 12>(f, a, h->dtype, s);
+    if (f.GMAX == 3) return launch_fast<3, 2, 12>(f, a, h->dtype, s);
+    return launch_fast<4, 2, 12>(f, a, h->dtype, s);
+}
+
 }  // namespace
+
+extern "C" int aatc_decode_launches(const aatc_calib *calib)
+{
+    return !calib ? 0 : fast_ok(calib) ? 1 : 3;
+}
 
 extern "C" aatc_status aatc_test_wait_fault(int skip_tile_copy, int wait_tries)
 {
@@ -1478,53 +1879,8 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
         }
         if (!f.single && f.units > MAX_COUNTED)
             return aatc_fail(AATC_ERR_UNSUPPORTED, "%d units with several splits each", f.units);
-        float *part = f.single ? nullptr : (float *)((char *)ws + WS_COUNTERS);
-        FastArgs a;
-        a.kp = kp;
-        a.vp = vp;
-        a.seq_lens = seq_lens;
-        a.L = L;
-        a.map = map;
-        a.Wk = h->Wk;
-        a.Wv = h->Wv;
-        a.rows = f.rows;
-        a.groups = f.groups;
-        a.Hkv = h->Hkv;
-        a.G = h->G;
-        a.HG = f.HG;
-        a.FST = f.FST;
-        a.stage_region = (uint32_t)f.stage_region;
-        a.single = f.single ? 1 : 0;
-        a.out = out;
-        a.vcst = h->vcst;
-        a.mats = reinterpret_cast<const __half *>(h->dmat);
-        a.n_tiles = f.n_tiles;
-        a.units = f.units;
-        a.S = f.S;
-        a.tiles_per = f.tiles_per;
-        a.blob = h->dblob;
-        a.q = q;
-        a.part = part;
-        a.counter = f.single ? nullptr : (unsigned *)ws;
-        {   // slots per merge chunk: what the stages hold, at most MERGE_LD float4 per thread
-            const int fit = (int)(f.stage_region / ((size_t)f.HPG * PROW * 4));
-            const int ld = MERGE_LD * 4 * (f.FW * 32) / (f.HPG * PROW);
-            a.merge_slots = fit < ld ? fit : ld;
-        }
-        a.status = h->status;
-        a.wait_tries = g_hook_tries.load(std::memory_order_relaxed);
-        a.skip_first_copy = g_hook_skip.load(std::memory_order_relaxed);
-        aatc_status st;
-        if (f.NT == 1) {
-            if (f.GMAX == 2) st = launch_fast<2, 1, 16>(f, a, h->dtype, s);
-            else if (f.GMAX == 3) st = launch_fast<3, 1, 16>(f, a, h->dtype, s);
-            else st = launch_fast<4, 1, 16>(f, a, h->dtype, s);
-        } else {
-            if (f.GMAX == 2) st = launch_fast<2, 2, 12>(f, a, h->dtype, s);
-            else if (f.GMAX == 3) st = launch_fast<3, 2, 12>(f, a, h->dtype, s);
-            else st = launch_fast<4, 2, 12>(f, a, h->dtype, s);
-        }
-        return st;
+        const FastArgs a = fast_args(h, f, q, kp, vp, map, seq_lens, L, B, out, ws);
+        return launch_fast_any(h, f, a, s);
     }
     if (h->Wk > GEN_MAX_W || h->Wv > GEN_MAX_W)
         return aatc_fail(AATC_ERR_UNSUPPORTED, "records of %d / %d words", h->Wk, h->Wv);
@@ -1544,4 +1900,44 @@ aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, c
                                                   h->muv32, out);
     AATC_CUDA(cudaGetLastError());
     return AATC_OK;
+}
+
+size_t append_decode_ws_bytes(const aatc_calib *h, int B, int L_old, int n_new)
+{
+    if (fast_ok(h)) {
+        const FastGeom f = fast_geom_append(h, B, L_old);
+        if (fused_append_fits(h, f, B, n_new)) return f.ws_total;
+    }
+    return decode_ws_bytes(h, B, L_old + n_new);
+}
+
+aatc_status append_decode_run(const aatc_calib *h, const void *k_new, const void *v_new, int n_new, const void *q,
+                              uint32_t *kp, uint32_t *vp, const CacheMap &map, int L_old, int B, float *out,
+                              void *ws, size_t ws_bytes, cudaStream_t s)
+{
+    if (B == 0) return AATC_OK;
+    if (fast_ok(h)) {
+        const FastGeom f = fast_geom_append(h, B, L_old);
+        if (fused_append_fits(h, f, B, n_new)) {
+            FastArgs a = fast_args(h, f, q, kp, vp, map, nullptr, L_old, B, out, ws);
+            a.single = 0;
+            a.S_slots = f.S + 1;
+            a.kw = kp;
+            a.vw = vp;
+            a.n_new = n_new;
+            a.L_old = L_old;
+            a.k_new = k_new;
+            a.v_new = v_new;
+            a.TT = h->TkvT32;
+            a.bk = h->bk32;
+            a.bv = h->bv32;
+            a.tabs = h->tab;
+            a.plans = h->plan;
+            return launch_fast_any(h, f, a, s);
+        }
+    }
+    // the two steps as separate calls: the append encoder, then decode over all tokens
+    aatc_status st = encode_run(h, k_new, v_new, B, n_new, L_old, nullptr, map, kp, vp, s);
+    if (st != AATC_OK) return st;
+    return decode_run(h, q, kp, vp, map, nullptr, L_old + n_new, B, out, ws, ws_bytes, s);
 }

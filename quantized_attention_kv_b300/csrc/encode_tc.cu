@@ -63,7 +63,9 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 const __grid_constant__ CUtensorMap mt, EncArgs a)
 {
     extern __shared__ unsigned char sm_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>(((uintptr_t)sm_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned in the shared window; derived from sm_raw by pointer arithmetic so that
+    // every access through it compiles to a shared-memory instruction
+    unsigned char *sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     unsigned char *Ts = sm;                              // 3 splits x 2 k-halves x 16 KB
     unsigned char *Xs = Ts + TBYTES;                     // ESTAGES x 32 KB
     uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 x max(Wk, Wv) words (tiled)
@@ -203,51 +205,55 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             const int kb = (ii & 15) >> 1;
             float fin = 0.f;
             uint32_t lo = 0;
-            int nb = 0, w = 0;
+            int w = 0;
             const uint32_t row_addr = tmem + ((uint32_t)(wq * 32) << 16) + g * D;
             // Pruned channels come last in record order with a zero range: they add no
             // bits.  A non-finite input makes every coefficient non-finite (T is dense),
-            // so two coefficients per token are checked.  The next 16 accumulator
-            // columns are in flight while the current 16 are quantized.
+            // so two coefficients per token are checked.  Eight coefficients are
+            // quantized at a time (independent chains), then ORed into the record
+            // at the bit positions the column table gives, a word leaving for the
+            // staging buffer wherever the table marks a word end.
             auto quantize16 = [&](const uint32_t (&r)[16], int c0) {
 #pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const EncCol col = cols[c0 + q];
-                    const float c = __uint_as_float(r[q]);
-                    float v = fmaf(c, col.inv, col.off);
-                    v = fminf(fmaxf(v, 0.f), col.top);
-                    // adding 1.5 * 2^23 rounds to the nearest integer, ties to even
-                    const uint32_t u = __float_as_uint(v + 12582912.f) & 0xFFu;
-                    lo |= u << nb;
-                    const int nb2 = nb + col.bits;
-                    if (nb2 >= 32) {
-                        if (t == 0) {
-                            const int2 wt = wtab[w];
-                            Rk[wt.x + kb * wt.y] = lo;
-                        } else {
-                            Rt16[64 * w + ii] = (uint16_t)lo;   // half-words 2w, 2w+1 of token ii
-                            Rt16[64 * w + 32 + ii] = (uint16_t)(lo >> 16);
+                for (int h8 = 0; h8 < 16; h8 += 8) {
+                    uint32_t uq[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const EncCol col = cols[c0 + h8 + q];
+                        const float c = __uint_as_float(r[h8 + q]);
+                        float v = fmaf(c, col.inv, col.off);
+                        v = fminf(fmaxf(v, 0.f), col.top);
+                        // adding 1.5 * 2^23 rounds to the nearest integer, ties to even
+                        uq[q] = __float_as_uint(v + 12582912.f) & 0xFFu;
+                    }
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int pk = cols[c0 + h8 + q].pack;
+                        const uint32_t u = uq[q];
+                        lo |= __funnelshift_l(0u, u, pk);   // u << shift
+                        if (pk & ENC_WORD_END) {
+                            if (t == 0) {
+                                const int2 wt = wtab[w];
+                                Rk[wt.x + kb * wt.y] = lo;
+                            } else {
+                                Rt16[64 * w + ii] = (uint16_t)lo;   // half-words 2w, 2w+1 of token ii
+                                Rt16[64 * w + 32 + ii] = (uint16_t)(lo >> 16);
+                            }
+                            lo = __funnelshift_l(u, 0u, pk);   // u >> (32 - shift): the part past the word
+                            ++w;
                         }
-                        lo = nb2 > 32 ? (u >> (32 - nb)) : 0u;
-                        nb = nb2 - 32;
-                        ++w;
-                    } else {
-                        nb = nb2;
                     }
                 }
             };
-            uint32_t ra[16], rb[16];
-            tmem_ld16(row_addr, ra);
-            tmem_wait_ld(ra);
-            fin = __uint_as_float(ra[0]) + __uint_as_float(ra[1]);
+            // one 16-column load in flight per warp at a time (a second buffer
+            // doubles the unrolled code and costs more in instruction fetch)
+            uint32_t ra[16];
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                tmem_ld16(row_addr + c0 + 16, rb);
-                quantize16(ra, c0);
-                tmem_wait_ld(rb);
-                if (c0 + 32 < D) tmem_ld16(row_addr + c0 + 32, ra);
-                quantize16(rb, c0 + 16);
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                tmem_ld16(row_addr + c0, ra);
                 tmem_wait_ld(ra);
+                if (c0 == 0) fin = __uint_as_float(ra[0]) + __uint_as_float(ra[1]);
+                quantize16(ra, c0);
             }
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
@@ -340,12 +346,15 @@ __global__ void k_enc_build(const double *__restrict__ T_k, const double *__rest
             c.inv = tb.inv_step[j];
             c.off = fmaf(-bias, tb.inv_step[j], tb.mid[j]);
             c.top = tb.top[j];
-            c.bits = tb.bits[j];
+            int nb = 0;   // bit position of column n in its record word
+            for (int m = 0; m < n; ++m) nb += tb.bits[pl.order[m]];
+            nb &= 31;
+            c.pack = nb | ((nb + tb.bits[j] >= 32) ? ENC_WORD_END : 0);
         } else {
             c.inv = 0.f;
             c.off = 0.f;
             c.top = 0.f;
-            c.bits = 0;
+            c.pack = 0;
         }
         cols[(size_t)(h * 2 + t) * D + n] = c;
     }

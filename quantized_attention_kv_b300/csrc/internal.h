@@ -98,11 +98,12 @@ struct __align__(16) DecBlob {
 
 // Encoder epilogue constants of one record-order column n (channel order[n]):
 // v = c * inv + off is the quantizer input c/Delta + mid with the bias T mu
-// folded in; codes are clamp(rint(v), 0, top); bits = 0 past n_coded.
+// folded in; codes are clamp(rint(v), 0, top); past n_coded the range is zero (no bits).
 struct __align__(16) EncCol {
     float inv, off, top;
-    int32_t bits;
+    int32_t pack;   // bit position of the code in its record word (0..31), | ENC_WORD_END if the word ends with it
 };
+constexpr int32_t ENC_WORD_END = 256;
 
 struct aatc_calib {
     int d, Hkv, Hq, G;
@@ -122,6 +123,7 @@ struct aatc_calib {
     int32_t *split;                           // [2] chosen B_K, B_V (joint allocation; device)
     // fp32 operands of the encode / decode kernels
     float *Tk32, *Tv32;       // [H][d][d] transform rows (coefficient i = row i . x)
+    float *TkvT32;            // [H][2][d][d] T_k, T_v transposed ([k][i] = row i, column k), fp32
     float *bk32, *bv32;       // [H][d] T mu
     float *AkT32;             // [H][d][d] (Tk^{-T})^T: q'_j = sum_k AkT32[k][j] q_k
     float *UvT32;             // [H][d][d] Uv^T: o_j = sum_k UvT32[k][j] c_k
@@ -207,6 +209,10 @@ aatc_status decode_check_args(const aatc_calib *calib, const void *q, const uint
                               const uint32_t *v_packed, int L_cap, const int32_t *seq_lens, int L, int B,
                               const float *out);
 size_t decode_ws_bytes(const aatc_calib *h, int B, int L);
+size_t append_decode_ws_bytes(const aatc_calib *h, int B, int L_old, int n_new);
+aatc_status append_decode_run(const aatc_calib *h, const void *k_new, const void *v_new, int n_new, const void *q,
+                              uint32_t *kp, uint32_t *vp, const CacheMap &map, int L_old, int B, float *out,
+                              void *ws, size_t ws_bytes, cudaStream_t s);
 aatc_status decode_run(const aatc_calib *h, const void *q, const uint32_t *kp, const uint32_t *vp,
                        const CacheMap &map, const int32_t *seq_lens, int L, int B, float *out, void *ws,
                        size_t ws_bytes, cudaStream_t s);
