@@ -372,10 +372,15 @@ def run_ours(args, ws, rank, local):
             torch.cuda.synchronize()
             return sorted(a_.elapsed_time(b_) / 1e3 / n_rot for a_, b_ in evs)
 
-        dec_t = timed(g_dec)
-        app_t = timed(g_app)
-        fus_t = timed(g_fus)
-        enc_t = timed(g_enc)
+        # NVTX ranges name the calls for a profiler (ncu --nvtx --nvtx-include "decode_calls/")
+        with torch.cuda.nvtx.range("decode_calls"):
+            dec_t = timed(g_dec)
+        with torch.cuda.nvtx.range("append_decode_calls"):
+            app_t = timed(g_app)
+        with torch.cuda.nvtx.range("fused_step_calls"):
+            fus_t = timed(g_fus)
+        with torch.cuda.nvtx.range("encode_calls"):
+            enc_t = timed(g_enc)
 
     def pct(v, q):
         return v[min(len(v) - 1, int(round(q * (len(v) - 1))))]

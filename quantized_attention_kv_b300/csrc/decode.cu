@@ -95,7 +95,8 @@ struct FastGeom {
     int FST;         // tiles in flight per warp
     int rows;        // key rows of 4 record words
     int groups;      // value groups of 8 half-words
-    int ksteps;      // 4 rows
+    int KP;          // key pieces per byte the plan reads (4 or 8)
+    int ksteps;      // KP rows
     int n_tiles;     // tiles per unit
     int units;       // B * Hkv * HG
     int S;           // splits (CTAs, partial slots) per unit
@@ -148,7 +149,8 @@ FastGeom fast_geom(const aatc_calib *h, int B, int L)
     f.groups = (2 * h->Wv + 7) / 8;
     f.GMAX = f.groups <= 2 ? 2 : (f.groups <= 3 ? 3 : 4);
     f.FW = f.NT == 2 ? 12 : 16;
-    f.ksteps = 4 * f.rows;
+    f.KP = h->kpieces == AATC_KEY_PIECES ? AATC_KEY_PIECES : AATC_PIECES;
+    f.ksteps = f.KP * f.rows;
     f.FST = 3;
     FastSmem m = fast_smem_layout(f.FW, f.FST, h->Wk + h->Wv, f.NT, f.ksteps, f.groups);
     if (m.total > (size_t)sm_limit_bytes()) {
@@ -228,7 +230,13 @@ bool fused_append_fits(const aatc_calib *h, const FastGeom &f, int B, int n_new)
            (long)B * f.HG <= 65535 && f.S != 1 && f.n_app > 0 && (long)B * h->Hkv <= (long)APP_PAIRS * f.n_app;
 }
 
-bool fast_ok(const aatc_calib *h) { return h->Wk <= FAST_MAX_W && h->Wv <= FAST_MAX_W && h->fast_layout; }
+// 8 key pieces per byte are served with GQA groups up to 4 (one n-tile: the
+// kernel variant with two n-tiles has no registers to spare for the masks)
+bool fast_ok(const aatc_calib *h)
+{
+    return h->Wk <= FAST_MAX_W && h->Wv <= FAST_MAX_W && h->fast_layout &&
+           (h->kpieces == AATC_PIECES || h->G <= 4);
+}
 
 // ---- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void *p)
@@ -402,7 +410,7 @@ struct FastArgs {
 // Each tile's P.V starts from zero and is added to the running sums in
 // fp32, so the tensor-core accumulation (which does not round to nearest)
 // never carries more than one tile.
-template <int GMAX, int NT, int FW, typename QT, bool PAGED>
+template <int GMAX, int NT, int FW, int KP, typename QT, bool PAGED>
 __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int g = lane >> 2, c = lane & 3;
     const int Wk = a.Wk, Wv = a.Wv, rows = a.rows, groups = a.groups, FST = a.FST;
-    const int ksteps = rows * 4;
+    const int ksteps = rows * KP;
     const uint32_t SB = 128u * (Wk + Wv), kbytes = 128u * Wk, vbytes = 128u * Wv;   // stage = K tile, V tile
 
     // shared memory carve-up (as in fast_smem_layout)
@@ -1045,11 +1053,11 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             return max(-100, min(100, 6 - e));
         };
         // B fragments: entry (kstep, n-tile t, lane) = (b0, b1), column n = 8t + lane/4 =
-        // (head n/2, hi if n even else lo), k-step (r, s4) from record word 4r + lane%4,
+        // (head n/2, hi if n even else lo), k-step (r, s4 < KP) from record word 4r + lane%4,
         // slots 2 s4 (b0) and 2 s4 + 1 (b1), low half first; weight = q'_ch * 2^ex * S
         for (int en = tid; en < ksteps * NT * 32; en += NTH) {
             const int ln = en & 31, t = (en >> 5) % NT, ks = (en >> 5) / NT;
-            const int r = ks >> 2, s4 = ks & 3;
+            const int r = ks / KP, s4 = ks % KP;
             const int n = 8 * t + (ln >> 2), i = n >> 1, part = n & 1;
             const int w = 4 * r + (ln & 3);
             const bool live = hg * HPG + i < a.G;
@@ -1116,9 +1124,15 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         for (int r = 0; r < 4; ++r) {
             if (r >= rows) break;
             const int nr = min(4, Wk - 4 * r);
-            const uint4 mA = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][0]);
-            const uint4 mB = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][4]);
-            const uint32_t mk[8] = {mA.x, mA.y, mA.z, mA.w, mB.x, mB.y, mB.z, mB.w};
+            uint32_t mk[2 * KP];
+#pragma unroll
+            for (int m4 = 0; m4 < KP / 2; ++m4) {
+                const uint4 mm = *reinterpret_cast<const uint4 *>(&blob_s->kmask[4 * r + c][4 * m4]);
+                mk[4 * m4] = mm.x;
+                mk[4 * m4 + 1] = mm.y;
+                mk[4 * m4 + 2] = mm.z;
+                mk[4 * m4 + 3] = mm.w;
+            }
             uint32_t x0[2], x1[2], y0[2], y1[2];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
@@ -1129,13 +1143,13 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
                 y1[hf] = kw.y >> 8;
             }
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4) {
+            for (int s4 = 0; s4 < KP; ++s4) {
                 uint2 bq[NT];
 #pragma unroll
-                for (int t = 0; t < NT; ++t) bq[t] = qtab_s[((r * 4 + s4) * NT + t) * 32 + lane];
+                for (int t = 0; t < NT; ++t) bq[t] = qtab_s[((r * KP + s4) * NT + t) * 32 + lane];
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
-                    const uint32_t sa = s4 < 2 ? x0[hf] : y0[hf], sb = s4 < 2 ? x1[hf] : y1[hf];
+                    const uint32_t sa = s4 < KP / 2 ? x0[hf] : y0[hf], sb = s4 < KP / 2 ? x1[hf] : y1[hf];
                     const uint32_t A0 = sa & mk[2 * s4], A1 = sb & mk[2 * s4];
                     const uint32_t A2 = sa & mk[2 * s4 + 1], A3 = sb & mk[2 * s4 + 1];
 #pragma unroll
@@ -1406,8 +1420,8 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
     }
     DecBlob &o = out[h];
     const int rows_tot = 64 * ((2 * Wv + 7) / 8);
-    for (int e = tid; e < 16 * 8; e += blockDim.x) {
-        const int w = e >> 3, k = e & 7;
+    for (int e = tid; e < 16 * 16; e += blockDim.x) {
+        const int w = e >> 4, k = e & 15;
         o.kmask[w][k] = w < Wk ? pk.mask[w][k] : 0u;
         for (int half = 0; half < 2; ++half) {
             const int ch = w < Wk ? pk.ch[w][k][half] : -1;
@@ -1468,9 +1482,10 @@ __global__ void k_dec_build(const HeadPlan *__restrict__ plans, const CodecTable
 template <int GMAX, int NT, int FW>
 int occupancy_of(size_t smem)
 {
-    auto kern = k_decode_fast<GMAX, NT, FW, __nv_bfloat16, false>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-        return 1;
+    auto kern = k_decode_fast<GMAX, NT, FW, AATC_PIECES, __nv_bfloat16, false>;   // (the KP = 8 variants use as many registers)
+    // through the raise-only helper: setting the attribute directly could lower it
+    // below what an earlier launch of this variant, with more shared memory, relies on
+    if (kernel_smem_limit((const void *)kern, smem) != AATC_OK) return 1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, FW * 32, smem) != cudaSuccess || n < 1) n = 1;
     return n;
@@ -1754,15 +1769,15 @@ aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a,
     return AATC_OK;
 }
 
-template <int GMAX, int NT, int FW>
+template <int GMAX, int NT, int FW, int KP>
 aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s)
 {
     if (a.map.table) {
-        if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16, true>, FW, f, a, s);
-        return launch_variant(k_decode_fast<GMAX, NT, FW, float, true>, FW, f, a, s);
+        if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, true>, FW, f, a, s);
+        return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, true>, FW, f, a, s);
     }
-    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, __nv_bfloat16, false>, FW, f, a, s);
-    return launch_variant(k_decode_fast<GMAX, NT, FW, float, false>, FW, f, a, s);
+    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, false>, FW, f, a, s);
+    return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, false>, FW, f, a, s);
 }
 
 // Test hook state (aatc_test_wait_fault): read at every fast-path launch.
@@ -1825,14 +1840,19 @@ FastArgs fast_args(const aatc_calib *h, const FastGeom &f, const void *q, const 
 
 aatc_status launch_fast_any(const aatc_calib *h, const FastGeom &f, const FastArgs &a, cudaStream_t s)
 {
-    if (f.NT == 1) {
-        if (f.GMAX == 2) return launch_fast<2, 1, 16>(f, a, h->dtype, s);
-        if (f.GMAX == 3) return launch_fast<3, 1, 16>(f, a, h->dtype, s);
-        return launch_fast<4, 1, 16>(f, a, h->dtype, s);
+    if (f.NT == 1 && f.KP == AATC_KEY_PIECES) {
+        if (f.GMAX == 2) return launch_fast<2, 1, 16, AATC_KEY_PIECES>(f, a, h->dtype, s);
+        if (f.GMAX == 3) return launch_fast<3, 1, 16, AATC_KEY_PIECES>(f, a, h->dtype, s);
+        return launch_fast<4, 1, 16, AATC_KEY_PIECES>(f, a, h->dtype, s);
     }
-    if (f.GMAX == 2) return launch_fast<2, 2, 12>(f, a, h->dtype, s);
-    if (f.GMAX == 3) return launch_fast<3, 2, 12>(f, a, h->dtype, s);
-    return launch_fast<4, 2, 12>(f, a, h->dtype, s);
+    if (f.NT == 1) {
+        if (f.GMAX == 2) return launch_fast<2, 1, 16, AATC_PIECES>(f, a, h->dtype, s);
+        if (f.GMAX == 3) return launch_fast<3, 1, 16, AATC_PIECES>(f, a, h->dtype, s);
+        return launch_fast<4, 1, 16, AATC_PIECES>(f, a, h->dtype, s);
+    }
+    if (f.GMAX == 2) return launch_fast<2, 2, 12, AATC_PIECES>(f, a, h->dtype, s);
+    if (f.GMAX == 3) return launch_fast<3, 2, 12, AATC_PIECES>(f, a, h->dtype, s);
+    return launch_fast<4, 2, 12, AATC_PIECES>(f, a, h->dtype, s);
 }
 
 }  // namespace

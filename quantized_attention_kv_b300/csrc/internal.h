@@ -64,35 +64,37 @@ struct CodecTables {
 // (plan.cu).  Codes are stored whole, LSB first, channels in the order of
 // the record-order rule; off[j] is the record bit offset of channel j.
 //
-// For the fast decoder every byte of the record is cut into at most
-// AATC_PIECES pieces (the parts of codes lying in it).  A 32-bit word x of
-// a record (keys) or a pair word holding the same half-word of two tokens
-// (values) is read through 8 masks: slot k < 4 is x & mask[k] (piece k of
-// bytes 0 and 2 of x, or of byte 0 of both half-words), slot k >= 4 is
-// (x >> 8) & mask[k] (piece k-4 of bytes 1 and 3).  Each masked 16-bit half
-// is a piece value times 2^p, p its bit position in its byte, and read as an
-// fp16 it equals piece * 2^(p-24) exactly (exponent field 0).
+// For the fast decoder every byte of the record is cut into its pieces (the
+// parts of codes lying in it): at most AATC_PIECES of them for values, at
+// most KP (4 or AATC_KEY_PIECES) for keys.  A 32-bit word x of a record
+// (keys) or a pair word holding the same half-word of two tokens (values) is
+// read through 2 KP masks (KP = 4 for values): slot k < KP is x & mask[k]
+// (piece k of bytes 0 and 2 of x, or of byte 0 of both half-words), slot
+// k >= KP is (x >> 8) & mask[k] (piece k - KP of bytes 1 and 3).  Each masked
+// 16-bit half is a piece value times 2^p, p its bit position in its byte, and
+// read as an fp16 it equals piece * 2^(p-24) exactly (exponent field 0).
 #define AATC_PIECES 4
+#define AATC_KEY_PIECES 8         // a byte holds at most 8 pieces (each at least one bit)
 #define AATC_PLAN_SLOTS 32    // record words (keys) or half-words (values) covered
 struct HeadPlan {
     int16_t off[AATC_D];                  // record bit offset of each code, -1 if pruned
     int16_t order[AATC_D];                // channels in record order (first n_coded entries)
     int32_t n_coded;                      // channels with b_j > 0
     int32_t max_pieces;                   // largest number of pieces in one byte
-    uint32_t mask[AATC_PLAN_SLOTS][8];    // keys: per record word; values: per half-word
-    int8_t ch[AATC_PLAN_SLOTS][8][2];     // channel of the piece in the low/high half, -1 = none
-    int8_t ex[AATC_PLAN_SLOTS][8][2];     // code bit offset of the piece minus p
+    uint32_t mask[AATC_PLAN_SLOTS][16];   // keys: per record word; values: per half-word (8 slots)
+    int8_t ch[AATC_PLAN_SLOTS][16][2];    // channel of the piece in the low/high half, -1 = none
+    int8_t ex[AATC_PLAN_SLOTS][16][2];    // code bit offset of the piece minus p
 };
 
 // Per-KV-head tables of the fast decoder, laid out as they sit in shared
 // memory (one bulk copy per CTA).  Built on the device from the plans and
 // codec tables (decode.cu).
 struct __align__(16) DecBlob {
-    uint32_t kmask[16][8];     // key record word w, slot k: AND mask (0 past the record)
+    uint32_t kmask[16][16];    // key record word w, slot k < 2 KP: AND mask (0 past the record)
     uint32_t vmask[32][8];     // value half-word e, slot k: AND mask in both halves
     float ksc[AATC_D];         // Delta_K,j / sqrt(d) times 2^(e_j - 13) (the row scale of the fp16 A_k rows), 0 for pruned channels
     float vstep[AATC_D];       // Delta_V,j, 0 for pruned channels
-    int16_t kslot[16][8][2];   // key piece of (word, slot, half): ch | (ex + 64) << 8, -1 = none
+    int16_t kslot[16][16][2];  // key piece of (word, slot, half): ch | (ex + 64) << 8, -1 = none
     int16_t vgat[AATC_D][2];   // value channel j: its piece rows, row | (ex + 64) << 8, -1 = none
 };
 
@@ -142,7 +144,8 @@ struct aatc_calib {
     EncCol *enc_cols;
     alignas(64) unsigned char tmap_T3[128];   // CUtensorMap over T3 (rows x 128 bf16)
     bool tmap_ok;
-    bool fast_layout;         // every record byte of every head holds <= AATC_PIECES pieces
+    bool fast_layout;         // every value byte holds <= AATC_PIECES pieces (key bytes: at most 8 anyway)
+    int kpieces;              // KP: key pieces per byte the fast decoder reads (4, or 8 when a key byte holds more than 4)
     uint32_t *status;         // device status word
 };
 
@@ -181,7 +184,7 @@ aatc_status calib_derive(aatc_calib *h, cudaStream_t s);
 // and upload them to h->plan.  Synchronous.
 aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits_v);
 // Host-side plan of one bit allocation (exposed for the ABI tests).
-void plan_one(const int32_t *bits, int W, HeadPlan *out);
+void plan_one(const int32_t *bits, int W, int kp, HeadPlan *out);
 
 // Build T3, enc_cols and the T3 tensor map (after the plans are on the device).
 aatc_status enc_build(aatc_calib *h, cudaStream_t s);

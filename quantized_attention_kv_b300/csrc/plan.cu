@@ -55,12 +55,14 @@ int record_order(const int32_t *bits, int *order)
 
 }  // namespace
 
-void plan_one(const int32_t *bits, int W, HeadPlan *out)
+// kp: pieces per byte the read plan provides (4 or 8); no masks when a byte
+// holds more
+void plan_one(const int32_t *bits, int W, int kp, HeadPlan *out)
 {
     memset(out, 0, sizeof(*out));
     for (int j = 0; j < D; ++j) out->off[j] = -1;
     for (int s = 0; s < AATC_PLAN_SLOTS; ++s)
-        for (int k = 0; k < 8; ++k) out->ch[s][k][0] = out->ch[s][k][1] = -1;
+        for (int k = 0; k < 16; ++k) out->ch[s][k][0] = out->ch[s][k][1] = -1;
 
     int order[D];
     const int n = record_order(bits, order);
@@ -85,7 +87,7 @@ void plan_one(const int32_t *bits, int W, HeadPlan *out)
     int mp = 0;
     for (int b = 0; b < nbytes; ++b) mp = (int)by[b].size() > mp ? (int)by[b].size() : mp;
     out->max_pieces = mp;
-    if (mp > AATC_PIECES) return;   // the fast decoder does not serve this layout
+    if (mp > kp) return;   // no read plan at kp pieces per byte
 
     auto piece = [&](int byte, int k) -> const Piece * {
         return (byte < nbytes && k < (int)by[byte].size()) ? &by[byte][k] : nullptr;
@@ -93,11 +95,11 @@ void plan_one(const int32_t *bits, int W, HeadPlan *out)
     auto fmask = [](const Piece *pc) -> uint32_t {
         return pc ? (((1u << pc->n) - 1u) << pc->p) : 0u;
     };
-    // keys: record word w, slot k; low half from byte 4w (+1 for S slots),
-    // high half from byte 4w+2 (+1)
+    // keys: record word w, slot k < 2 kp; low half from byte 4w (+1 for
+    // slots k >= kp), high half from byte 4w+2 (+1)
     for (int w = 0; w < W && w < AATC_PLAN_SLOTS; ++w)
-        for (int k = 0; k < 8; ++k) {
-            const int sb = k < 4 ? 0 : 1, pk = k & 3;
+        for (int k = 0; k < 2 * kp; ++k) {
+            const int sb = k < kp ? 0 : 1, pk = k % kp;
             const Piece *lo = piece(4 * w + sb, pk), *hi = piece(4 * w + 2 + sb, pk);
             out->mask[w][k] = fmask(lo) | (fmask(hi) << 16);
             if (lo) { out->ch[w][k][0] = (int8_t)lo->ch; out->ex[w][k][0] = (int8_t)(lo->o - lo->p); }
@@ -109,17 +111,24 @@ aatc_status plan_build(aatc_calib *h, const int32_t *bits_k, const int32_t *bits
 {
     std::vector<HeadPlan> plans((size_t)h->Hkv * 2);
     bool fast = true;
+    // keys: 4 pieces per byte, or 8 for every head when a key byte of some head holds more than 4
+    int kp = AATC_PIECES;
     for (int hh = 0; hh < h->Hkv; ++hh) {
-        plan_one(bits_k + (size_t)hh * D, h->Wk, &plans[hh * 2 + 0]);
+        plan_one(bits_k + (size_t)hh * D, h->Wk, AATC_PIECES, &plans[hh * 2 + 0]);
+        if (plans[hh * 2].max_pieces > AATC_PIECES) kp = AATC_KEY_PIECES;
+    }
+    h->kpieces = kp;
+    for (int hh = 0; hh < h->Hkv; ++hh) {
+        if (kp != AATC_PIECES) plan_one(bits_k + (size_t)hh * D, h->Wk, kp, &plans[hh * 2 + 0]);
         // values: the same cut into pieces, read per half-word (slot = half-word e,
         // mask in both halves: the pair word holds half-word e of two tokens)
         HeadPlan key_view;
-        plan_one(bits_v + (size_t)hh * D, h->Wv, &key_view);
-        fast = fast && plans[hh * 2].max_pieces <= AATC_PIECES && key_view.max_pieces <= AATC_PIECES;
+        plan_one(bits_v + (size_t)hh * D, h->Wv, AATC_PIECES, &key_view);
+        fast = fast && plans[hh * 2].max_pieces <= kp && key_view.max_pieces <= AATC_PIECES;
         HeadPlan &pv = plans[hh * 2 + 1];
         memcpy(&pv, &key_view, sizeof(HeadPlan));
         for (int s = 0; s < AATC_PLAN_SLOTS; ++s)
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < 16; ++k) {
                 pv.mask[s][k] = 0;
                 pv.ch[s][k][0] = pv.ch[s][k][1] = -1;
                 pv.ex[s][k][0] = pv.ex[s][k][1] = 0;

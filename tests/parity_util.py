@@ -97,5 +97,6 @@ def synthetic_calibration(G, bits_k, bits_v, seed=0, H=1):
     cal["step_k"] = rep(oracle.steps(lam_k, bits_k))
     cal["step_v"] = rep(oracle.steps(lam_v, bits_v))
     cal["W"] = int(np.sum(bits_k)) // 32
+    cal["W_k"], cal["W_v"] = cal["W"], int(np.sum(bits_v)) // 32
     cal["G"] = G
     return cal

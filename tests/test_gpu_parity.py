@@ -308,18 +308,21 @@ def test_decode_matches_oracle_from_identical_codes(lens):
 _synthetic_calibration = synthetic_calibration
 
 
-@pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "bits2", "bits4", "bits8"])
+@pytest.mark.parametrize("case", ["G1", "G7", "G8", "wide_W20", "many_pieces", "key_pieces8", "key_pieces8_G8",
+                                  "bits2", "bits4", "bits8"])
 def test_decode_paths_match_oracle(case):
-    """Fast path (GQA groups of 1..8, 2.0..4.0 bits) and the general path
-    (records above 16 words up to the 32-word maximum, bytes holding more than
-    four code pieces); each also through a paged pool on shuffled 32-token
-    blocks, which must give the contiguous output exactly."""
+    """Fast path (GQA groups of 1..8, 2.0..4.0 bits, key bytes of up to eight
+    code pieces) and the general path (records above 16 words up to the
+    32-word maximum, value bytes holding more than four code pieces, key bytes
+    of more than four pieces with GQA groups above 4); each also through a
+    paged pool on shuffled 32-token blocks, which must give the contiguous
+    output exactly."""
     lam = 0.95 ** np.arange(128)
     G, B_bits = 4, 352
     if case == "G1":
         G = 1
-    elif case in ("G7", "G8"):
-        G = int(case[1:])
+    elif case in ("G7", "G8", "key_pieces8_G8"):
+        G = int(case[-1:])
     elif case == "wide_W20":
         B_bits = 640
     elif case == "bits2":
@@ -335,8 +338,10 @@ def test_decode_paths_match_oracle(case):
         # codes eight to a byte, beyond what the fast decoder reads
         bk = np.array([2] * 96 + [1] * 32, dtype=np.int32)
         bv = bk.copy()
+    if case.startswith("key_pieces8"):
+        # the same key record (eight 1-bit codes to a byte at its end), values of 11 words
+        bk = np.array([2] * 96 + [1] * 32, dtype=np.int32)
     cal = _synthetic_calibration(G, bk, bv)
-    W = cal["W"]
     L, Bsz = 333, 2
     rng = np.random.default_rng(1)
     kp = np.stack([[oracle.pack(rng.integers(0, 2 ** np.maximum(bk, 1)) * (bk > 0), bk) for _ in range(L)]
@@ -356,9 +361,9 @@ def test_decode_paths_match_oracle(case):
     perm = torch.randperm(Bsz * bpr + 5, generator=torch.Generator().manual_seed(3))
     table = perm[:Bsz * bpr].reshape(Bsz, bpr).to(torch.int32).cuda()
     pools = []
-    for c in (kc, vc):
-        pool = aatc.alloc_pool(g, Bsz * bpr + 5, 32)
-        pool[table.long()] = c.reshape(Bsz, 1, bpr, 32, W).permute(0, 2, 1, 3, 4)
+    for c, t in ((kc, "k"), (vc, "v")):
+        pool = aatc.alloc_pool(g, Bsz * bpr + 5, 32, tensor=t)
+        pool[table.long()] = c.reshape(Bsz, 1, bpr, 32, c.shape[-1]).permute(0, 2, 1, 3, 4)
         pools.append(pool)
     out_p = aatc.decode_attention_paged(g, q, pools[0], pools[1], table, L)
     assert torch.equal(out_p, out), case
@@ -484,3 +489,28 @@ def test_end_to_end_qwen_128k():
 @pytest.mark.parametrize("bits", [2.0, 2.75, 4.0])
 def test_end_to_end_stack_layer_budgets(bits):
     _end_to_end(WL["llama_stack"], sample=[(0, h) for h in range(8)], layer=31, seq_len=4096, bits=bits)
+
+
+def test_kernel_variant_reused_with_more_shared_memory():
+    """Two record widths served by one decode kernel variant, the narrower
+    (less shared memory) planned after the wider had launched: the wider must
+    still launch (sizing a new shape must not lower the variant's
+    shared-memory limit below what an earlier launch set)."""
+    rng = np.random.default_rng(5)
+    lam = 0.95 ** np.arange(128)
+    bv, _ = oracle.allocate_bits(0.93 ** np.arange(128), 352)
+    outs = []
+    for bk_bits in (352, 224, 352):     # 11/11 words, then 7/11, then 11/11 again
+        bk, _ = oracle.allocate_bits(lam, bk_bits)
+        cal = _synthetic_calibration(4, bk, bv)
+        L, Bsz = 2000, 1
+        kp = np.stack([[oracle.pack(rng.integers(0, 2 ** np.maximum(bk, 1)) * (bk > 0), bk) for _ in range(L)]])[:, None]
+        vp = np.stack([[oracle.pack(rng.integers(0, 2 ** np.maximum(bv, 1)) * (bv > 0), bv) for _ in range(L)]])[:, None]
+        q = torch.from_numpy(rng.standard_normal((Bsz, 4, 128)).astype(np.float32)).cuda()
+        g = aatc.import_calib(cal, 4, torch.float32)
+        L_cap = aatc.cache_capacity(L)
+        out = aatc.decode_attention(g, q, _upload(kp, oracle.KEYS, L_cap), _upload(vp, oracle.VALUES, L_cap), L)
+        ref = oracle.decode_attention(to_np64(q), kp, vp, cal)
+        assert attn_rel_err(out.cpu().numpy(), ref) <= ATTN_RTOL, bk_bits
+        g.check()
+        outs.append(out)
