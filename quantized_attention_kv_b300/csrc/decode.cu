@@ -120,7 +120,7 @@ FastSmem fast_smem_layout(int FW, int FST, int Wkv, int NT, int ksteps, int grou
     const size_t tiles = (size_t)FW * FST * 128 * Wkv;
     // epilogue in the stage region: the warps' piece sums (packed when a warp's
     // own stages are too small), later the unit's partial slots (merge)
-    size_t epi_region = (size_t)FW * 64 * groups * HPG * 4;
+    size_t epi_region = (size_t)FW * 64 * groups * (HPG + 1) * 4;
     if (epi_region < (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4) epi_region = (size_t)MERGE_MIN_SLOTS * HPG * PROW * 4;
     m.stages = tiles > epi_region ? tiles : epi_region;
     m.mat = (size_t)D * D * 4;   // A_k, then Uv: fp16 hi and lo planes
@@ -1295,7 +1295,11 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     const int rows_tot = 64 * groups;
     float *wm = scr;                                          // [FW][HPG]
     float *wl = wm + FW * HPG;                                // [FW][HPG]
-    float *wacc = reinterpret_cast<float *>(stage_base);      // [FW][rows_tot][HPG], warp stride wstride
+    // [FW][rows_tot][HPG + 1], warp stride wstride: rows padded to an odd number of
+    // floats, so that the gather's reads of one head's rows for 32 channels fall in
+    // distinct banks (with HPG floats per row they would share HPG-aligned banks)
+    constexpr int WROW = HPG + 1;
+    float *wacc = reinterpret_cast<float *>(stage_base);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         float l = l_run[t];
@@ -1310,8 +1314,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     // the warps' piece sums (unscaled, each against its own running maximum):
     // in the warp's own stages when they hold them (the warp is done with them),
     // else packed over all stages once every warp is out of its loop
-    const bool own = (size_t)rows_tot * HPG * 4 <= (size_t)FST * SB;
-    const int wstride = own ? (int)(FST * SB / 4) : rows_tot * HPG;   // floats between warps
+    const bool own = (size_t)rows_tot * WROW * 4 <= (size_t)FST * SB;
+    const int wstride = own ? (int)(FST * SB / 4) : rows_tot * WROW;   // floats between warps
     if (!own) __syncthreads();
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -1322,8 +1326,8 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 #pragma unroll
             for (int m4 = 0; m4 < 4; ++m4) {
                 const int row = (gr * 4 + m4) * 16 + g;
-                wacc[(size_t)warp * wstride + row * HPG + i] = acc[gr][m4][t][0];
-                wacc[(size_t)warp * wstride + (row + 8) * HPG + i] = acc[gr][m4][t][1];
+                wacc[(size_t)warp * wstride + row * WROW + i] = acc[gr][m4][t][0];
+                wacc[(size_t)warp * wstride + (row + 8) * WROW + i] = acc[gr][m4][t][1];
             }
         }
     }
@@ -1352,7 +1356,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         for (int q2 = 0; q2 < 2; ++q2) {
             const int vg = blob_s->vgat[j][q2];
             if (vg >= 0) {
-                const float *src = wacc + (size_t)(vg & 255) * HPG + i;
+                const float *src = wacc + (size_t)(vg & 255) * WROW + i;
                 float s0 = 0.f, s1 = 0.f;
 #pragma unroll
                 for (int w = 0; w < FW; w += 2) {
