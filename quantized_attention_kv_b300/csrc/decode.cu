@@ -410,7 +410,10 @@ struct FastArgs {
 // Each tile's P.V starts from zero and is added to the running sums in
 // fp32, so the tensor-core accumulation (which does not round to nearest)
 // never carries more than one tile.
-template <int GMAX, int NT, int FW, int KP, typename QT, bool PAGED>
+// WK, WV, FSTC > 0: the record widths and the pipeline depth as compile-time
+// constants (the common widths: record addressing, row and group counts fold
+// away, about 5-9 % of the call at 2.75 bits); 0: read from the arguments.
+template <int GMAX, int NT, int FW, int KP, typename QT, bool PAGED, int WK = 0, int WV = 0, int FSTC = 0>
 __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
 {
     constexpr int NTH = FW * 32;
@@ -419,7 +422,9 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, tid = threadIdx.x;
     const int g = lane >> 2, c = lane & 3;
-    const int Wk = a.Wk, Wv = a.Wv, rows = a.rows, groups = a.groups, FST = a.FST;
+    const int Wk = WK > 0 ? WK : a.Wk, Wv = WV > 0 ? WV : a.Wv;
+    const int rows = WK > 0 ? (WK + 3) / 4 : a.rows, groups = WV > 0 ? (2 * WV + 7) / 8 : a.groups;
+    const int FST = FSTC > 0 ? FSTC : a.FST;
     const int ksteps = rows * KP;
     const uint32_t SB = 128u * (Wk + Wv), kbytes = 128u * Wk, vbytes = 128u * Wv;   // stage = K tile, V tile
 
@@ -1773,15 +1778,31 @@ aatc_status launch_variant(K kern, int FW, const FastGeom &f, const FastArgs &a,
     return AATC_OK;
 }
 
-template <int GMAX, int NT, int FW, int KP>
+template <int GMAX, int NT, int FW, int KP, int WK = 0, int WV = 0, int FSTC = 0>
 aatc_status launch_fast(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s)
 {
     if (a.map.table) {
-        if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, true>, FW, f, a, s);
-        return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, true>, FW, f, a, s);
+        if (dt == AATC_BF16)
+            return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, true, WK, WV, FSTC>, FW, f, a, s);
+        return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, true, WK, WV, FSTC>, FW, f, a, s);
     }
-    if (dt == AATC_BF16) return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, false>, FW, f, a, s);
-    return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, false>, FW, f, a, s);
+    if (dt == AATC_BF16)
+        return launch_variant(k_decode_fast<GMAX, NT, FW, KP, __nv_bfloat16, false, WK, WV, FSTC>, FW, f, a, s);
+    return launch_variant(k_decode_fast<GMAX, NT, FW, KP, float, false, WK, WV, FSTC>, FW, f, a, s);
+}
+
+// The kernel with the widths as constants, for the equal K/V widths of 2.0,
+// 2.75 and 4.0 bits per element (their pipeline depth as fast_geom picks it);
+// false when f is another shape.
+template <int NT, int FW>
+bool launch_fast_common(const FastGeom &f, const FastArgs &a, aatc_dtype dt, cudaStream_t s, aatc_status *st)
+{
+    if (f.KP != AATC_PIECES || a.Wk != a.Wv) return false;
+    if (a.Wk == 8 && f.FST == 3 && f.GMAX == 2) *st = launch_fast<2, NT, FW, AATC_PIECES, 8, 8, 3>(f, a, dt, s);
+    else if (a.Wk == 11 && f.FST == 3 && f.GMAX == 3) *st = launch_fast<3, NT, FW, AATC_PIECES, 11, 11, 3>(f, a, dt, s);
+    else if (a.Wk == 16 && f.FST == 2 && f.GMAX == 4) *st = launch_fast<4, NT, FW, AATC_PIECES, 16, 16, 2>(f, a, dt, s);
+    else return false;
+    return true;
 }
 
 // Test hook state (aatc_test_wait_fault): read at every fast-path launch.
@@ -1844,6 +1865,9 @@ FastArgs fast_args(const aatc_calib *h, const FastGeom &f, const void *q, const 
 
 aatc_status launch_fast_any(const aatc_calib *h, const FastGeom &f, const FastArgs &a, cudaStream_t s)
 {
+    aatc_status st;
+    if (f.NT == 1 ? launch_fast_common<1, 16>(f, a, h->dtype, s, &st) : launch_fast_common<2, 12>(f, a, h->dtype, s, &st))
+        return st;
     if (f.NT == 1 && f.KP == AATC_KEY_PIECES) {
         if (f.GMAX == 2) return launch_fast<2, 1, 16, AATC_KEY_PIECES>(f, a, h->dtype, s);
         if (f.GMAX == 3) return launch_fast<3, 1, 16, AATC_KEY_PIECES>(f, a, h->dtype, s);
