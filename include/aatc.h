@@ -245,6 +245,15 @@ aatc_status aatc_append_decode_attention(const aatc_calib *calib, const void *k_
  * arguments or when it needs none). */
 size_t aatc_append_decode_workspace_size(const aatc_calib *calib, int B, int L_old, int n_new);
 
+/* When aatc_append_decode_attention uses its fused kernel (process-wide):
+ * 1 (default) when it pays -- the cache is empty, or the decode splits are
+ * long enough (48 tiles of 32 tokens per split per (row, KV head) pair an
+ * appender CTA takes) that the appenders finish inside them; 2 whenever the
+ * shape fits the kernel (for tests); 0 never (append then decode).
+ * Workspace sizes follow the mode: size workspaces after setting it.
+ * Errors: INVALID_ARG for another mode. */
+aatc_status aatc_set_fused_step(int mode);
+
 /* Paged cache ([SERVE]; the layout is this library's).
  * A pool holds n_blocks blocks.  Block p holds block_tokens tokens (32
  * times a power of two: 32, 64, 128, ...) of every KV head: head h of block p is the

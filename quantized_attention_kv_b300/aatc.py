@@ -30,7 +30,7 @@ EXPORTED = ["aatc_calibrate", "aatc_encode", "aatc_decode_attention", "aatc_deco
             "aatc_encode_paged", "aatc_decode_attention_paged",
             "aatc_record_words", "aatc_record_words_kv", "aatc_export_calib", "aatc_import_calib", "aatc_check",
             "aatc_free", "aatc_last_error", "aatc_test_wait_fault", "aatc_append_decode_attention",
-            "aatc_append_decode_workspace_size", "aatc_decode_launches"]
+            "aatc_append_decode_workspace_size", "aatc_decode_launches", "aatc_set_fused_step"]
 
 
 class AatcError(RuntimeError):
@@ -80,6 +80,7 @@ def lib():
             "aatc_append_decode_attention": (I, [P, P, P, I, P, P, P, I, I, I, P, P, S, P]),
             "aatc_append_decode_workspace_size": (S, [P, I, I, I]),
             "aatc_decode_launches": (I, [P]),
+            "aatc_set_fused_step": (I, [I]),
         }
         for name, (res, args) in sig.items():
             f = getattr(L, name)
@@ -313,6 +314,11 @@ def decode_attention(calib: Calib, q: torch.Tensor, k_packed: torch.Tensor, v_pa
                                        _ptr(seq_lens), int(L), B, _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream, q.device)))
     return out
+
+
+def set_fused_step(mode: int):
+    """aatc_set_fused_step: 0 never fuse the serving step, 1 when it pays (default), 2 whenever it fits."""
+    _check(lib().aatc_set_fused_step(int(mode)))
 
 
 def append_workspace_size(calib: Calib, B: int, L_old: int, n_new: int) -> int:

@@ -75,6 +75,7 @@ constexpr int QHS = D + 8;       // halfs per row of the fp16 B operands of the 
 // appender CTAs (fused append): tokens per row, padded row of T, record words
 constexpr int APP_MAX = 4;
 constexpr int APP_PAIRS = 4;      // (KV head, row) pairs per appender CTA at most
+constexpr int APP_TILES = 48;     // tiles per split per appender pair for the fused kernel to pay
 constexpr int APP_TAILS = 64;     // units an appender may have to finish (APP_PAIRS x head groups)
 constexpr int APP_RW = FAST_MAX_W;
 constexpr size_t APP_TT = (size_t)2 * D * D * 4;   // the two transposed transforms, in the stage region
@@ -102,6 +103,7 @@ struct FastGeom {
     int S;           // splits (CTAs, partial slots) per unit
     int tiles_per;   // tiles per split
     int n_app;       // appender CTAs after the splits' (fused append; 0 otherwise)
+    bool fuse_pays;  // fused append: the appenders finish inside the splits' time
     int grid;        // CTAs: units * S + n_app
     size_t stage_bytes, stage_region, smem, ws_total;
     bool single;     // one split per unit: the split kernel writes the output itself
@@ -191,6 +193,7 @@ FastGeom fast_geom_append(const aatc_calib *h, int B, int L_old)
     f.n_tiles = (L_old + TILE - 1) / TILE;
     const int per_sm = fast_ctas_per_sm(f.GMAX, f.NT, f.FW, f.smem);
     const int C = sm_count() * per_sm, pairs = B * h->Hkv;
+    f.fuse_pays = true;
     if (f.n_tiles == 0) {
         f.S = 0;
         f.tiles_per = 1;
@@ -200,7 +203,8 @@ FastGeom fast_geom_append(const aatc_calib *h, int B, int L_old)
         const int ppa = left > 0 ? (pairs + left - 1) / left : pairs;
         if (left >= pairs) {
             f.n_app = pairs;
-        } else if (left > 0 && f.tiles_per >= 64 * ppa) {
+            f.fuse_pays = f.tiles_per >= APP_TILES;
+        } else if (left > 0 && f.tiles_per >= APP_TILES * ppa) {
             f.n_app = left;
         } else {
             const int S2 = min((C - pairs) / f.units, f.n_tiles);
@@ -209,13 +213,18 @@ FastGeom fast_geom_append(const aatc_calib *h, int B, int L_old)
                 f.tiles_per = (f.n_tiles + S2 - 1) / S2;
                 f.S = (f.n_tiles + f.tiles_per - 1) / f.tiles_per;
                 f.n_app = pairs;
+                f.fuse_pays = f.tiles_per >= APP_TILES;
             }
         }
     }
     f.grid = f.units * f.S + f.n_app;
+    f.single = false;   // every unit has the appenders' slot: partials and counters always
     f.ws_total = WS_COUNTERS + ((((size_t)f.units * (f.S + 1) * f.HPG * PROW * 4) + 255) & ~(size_t)255);
     return f;
 }
+
+// aatc_set_fused_step: 0 never fuse, 1 when it pays (default), 2 whenever the shape fits
+std::atomic<int> g_fuse_mode{1};
 
 // The appender CTAs need their staging in the stage region, the unit counters
 // and at most APP_MAX new tokens per row.
@@ -226,8 +235,10 @@ FastGeom fast_geom_append(const aatc_calib *h, int B, int L_old)
 bool fused_append_fits(const aatc_calib *h, const FastGeom &f, int B, int n_new)
 {
     const size_t pbuf = (size_t)f.FW * 8 * f.NT * PSTRIDE * 2;
-    return n_new >= 1 && n_new <= APP_MAX && f.stage_region >= APP_TT && pbuf >= APP_PB && f.units <= MAX_COUNTED &&
-           (long)B * f.HG <= 65535 && f.S != 1 && f.n_app > 0 && (long)B * h->Hkv <= (long)APP_PAIRS * f.n_app;
+    const int mode = g_fuse_mode.load(std::memory_order_relaxed);
+    return n_new >= 1 && n_new <= APP_MAX && f.stage_region >= APP_TT / 2 && pbuf >= APP_PB && f.units <= MAX_COUNTED &&
+           (long)B * f.HG <= 65535 && f.S != 1 && f.n_app > 0 && (long)B * h->Hkv <= (long)APP_PAIRS * f.n_app &&
+           (mode == 2 || (mode == 1 && f.fuse_pays));
 }
 
 // 8 key pieces per byte are served with GQA groups up to 4 (one n-tile: the
@@ -383,6 +394,7 @@ struct FastArgs {
     const float *bk, *bv;        // [Hkv][D] T mu (fp32)
     const CodecTables *tabs;     // [Hkv][2]
     const HeadPlan *plans;       // [Hkv][2]
+    int app_one_t;               // the stage region holds one transform at a time (below 2 D^2 floats)
     uint32_t stage_region;  // bytes before the tables: the tile stages, reused by the epilogue
     int single;             // one split per unit (S = 1): finish here and write out
     float *out;             // [B][Hq][D] (single split)
@@ -697,7 +709,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
         int hT = -1, hB = -1, hA = -1;
         auto load = [&](int hh) {   // thread 0: the copies the pair of head hh still needs
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // after the generic reads of these buffers
-            if (hh != hT) {
+            if (!a.app_one_t && hh != hT) {   // (one-slot mode: each transform in turn, below)
                 mbar_arrive_expect(t_bar, (uint32_t)(2 * D * D * 4));
                 bulk_g2s(TT, a.TT + (size_t)hh * 2 * D * D, (uint32_t)(2 * D * D * 4), t_bar);
             }
@@ -730,7 +742,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
             }
             for (int e = tid; e < 2 * APP_MAX * APP_RW; e += NTH) rec[e] = 0u;
             __syncthreads();
-            if (ph != hT) {
+            if (!a.app_one_t && ph != hT) {
                 ok = mbar_wait(t_bar, tph) && ok;
                 tph ^= 1u;
             }
@@ -743,13 +755,27 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
                 mph ^= 1u;
             }
             hT = hB = hA = ph;
-            if (tid < 2 * D) {   // thread (tensor, channel j): c = T x - T mu, quantized, ORed into the record
-                const int tensor = tid >> 7, j = tid & (D - 1);
+            // thread (tensor, channel j): c = T x - T mu, quantized, ORed into the record;
+            // both tensors at once, or (one-slot mode) keys then values, each transform
+            // brought into the single slot in turn
+            for (int phz = 0; phz < (a.app_one_t ? 2 : 1); ++phz) {
+                if (a.app_one_t) {
+                    if (phz == 1) __syncthreads();   // the key transform's last reads
+                    if (tid == 0) {
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        mbar_arrive_expect(t_bar, (uint32_t)(D * D * 4));
+                        bulk_g2s(TT, a.TT + ((size_t)ph * 2 + phz) * D * D, (uint32_t)(D * D * 4), t_bar);
+                    }
+                    ok = mbar_wait(t_bar, tph) && ok;
+                    tph ^= 1u;
+                }
+                if (a.app_one_t ? tid >= D : tid >= 2 * D) continue;
+                const int tensor = a.app_one_t ? phz : tid >> 7, j = tid & (D - 1);
                 const CodecTables &tb = a.tabs[ph * 2 + tensor];
                 const float bias = (tensor ? a.bv : a.bk)[ph * D + j];
                 const float inv = tb.inv_step[j], mid = tb.mid[j], top = tb.top[j];
                 const int bits = tb.bits[j], off = a.plans[ph * 2 + tensor].off[j];
-                const float *Tt = TT + (size_t)tensor * D * D;
+                const float *Tt = TT + (a.app_one_t ? 0 : (size_t)tensor * D * D);
                 for (int n = 0; n < a.n_new; ++n) {
                     const float *xr = xs + (tensor * APP_MAX + n) * D;
                     float acc = 0.f;
@@ -768,6 +794,7 @@ __global__ void __launch_bounds__(FW * 32, 1) k_decode_fast(FastArgs a)
                     cod[(tensor * APP_MAX + n) * D + j] = (int16_t)uq;
                 }
             }
+            if (a.app_one_t) hT = -1;   // the slot holds the value transform
             __syncthreads();
             // the records into the cache, placed as the encoders place them
             for (int e = tid; e < a.n_new * 3 * (Wk > Wv ? Wk : Wv); e += NTH) {
@@ -1845,6 +1872,7 @@ FastArgs fast_args(const aatc_calib *h, const FastGeom &f, const void *q, const 
     a.L_old = L;
     a.k_new = a.v_new = nullptr;
     a.TT = a.bk = a.bv = nullptr;
+    a.app_one_t = 0;
     a.tabs = nullptr;
     a.plans = nullptr;
     a.tiles_per = f.tiles_per;
@@ -1884,6 +1912,13 @@ aatc_status launch_fast_any(const aatc_calib *h, const FastGeom &f, const FastAr
 }
 
 }  // namespace
+
+extern "C" aatc_status aatc_set_fused_step(int mode)
+{
+    if (mode < 0 || mode > 2) return aatc_fail(AATC_ERR_INVALID_ARG, "fused-step mode %d is not 0, 1 or 2", mode);
+    g_fuse_mode.store(mode);
+    return AATC_OK;
+}
 
 extern "C" int aatc_decode_launches(const aatc_calib *calib)
 {
@@ -1977,6 +2012,9 @@ aatc_status append_decode_run(const aatc_calib *h, const void *k_new, const void
             a.k_new = k_new;
             a.v_new = v_new;
             a.TT = h->TkvT32;
+            a.app_one_t = f.stage_region < APP_TT ? 1 : 0;
+            if (!a.part || !a.counter || ws_bytes < f.ws_total)
+                return aatc_fail(AATC_ERR_INVALID_ARG, "workspace of %zu bytes required", f.ws_total);
             a.bk = h->bk32;
             a.bv = h->bv32;
             a.tabs = h->tab;

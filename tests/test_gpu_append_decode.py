@@ -23,8 +23,10 @@ pytestmark = pytest.mark.gpu
 SAME_CODES_RTOL = 2e-4
 
 # (workload, batch rows, cached tokens, new tokens per row).  The fused
-# kernel serves shapes whose plain decode has several splits per (row, KV
-# head group) or no cached tokens; the others run append then decode.
+# kernel fits shapes whose plain decode has several splits per (row, KV head
+# group) or no cached tokens; the others run append then decode.  Each case
+# runs with the kernel used whenever it fits and with the default rule (used
+# where it pays).
 CASES = [
     ("tiny", 1, 0, 1),          # an empty cache: the new token alone (appenders only, two head groups)
     ("tiny", 1, 5, 1),          # one split per unit: the two calls
@@ -58,8 +60,15 @@ def _caches(cal, B, L_cap, kc, vc, L_old):
     return kp, vp
 
 
+@pytest.fixture(params=[2, 1], ids=["fused_whenever_it_fits", "fused_when_it_pays"])
+def fuse_mode(request):
+    aatc.set_fused_step(request.param)
+    yield request.param
+    aatc.set_fused_step(1)
+
+
 @pytest.mark.parametrize("name,B,L_old,n_new", CASES)
-def test_fused_step_matches_append_then_decode_and_oracle(name, B, L_old, n_new):
+def test_fused_step_matches_append_then_decode_and_oracle(name, B, L_old, n_new, fuse_mode):
     assert torch.cuda.is_available(), "GPU test needs a CUDA device"
     wl, cal = _cal(name)
     L = L_old + n_new
@@ -84,6 +93,12 @@ def test_fused_step_matches_append_then_decode_and_oracle(name, B, L_old, n_new)
     rv = records(vpa, gcal["W_v"], oracle.VALUES, L)
     ref = oracle.decode_attention(to_np64(qd), rk, rv, gcal)
     assert attn_rel_err(out_f.cpu().numpy(), ref) <= ATTN_RTOL
+
+
+def test_fused_step_mode_argument():
+    with pytest.raises(aatc.AatcError) as e:
+        aatc.set_fused_step(3)
+    assert e.value.status == aatc.ERR_INVALID_ARG
 
 
 def test_fused_steps_in_a_row_share_one_workspace():
