@@ -22,7 +22,7 @@ bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Sizes of the arena pieces, in the order they are carved.
 struct Layout {
-    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, dblob, dmat, t3, cols, total;
+    size_t f64_vec, f64_mat, i32_vec, f32_vec, f32_mat, tabs, plans, dblob, dmat, t3, cols, wfix, total;
 };
 
 Layout layout_for(int H)
@@ -40,8 +40,9 @@ Layout layout_for(int H)
     L.dmat = up((size_t)H * 4 * D * D * 2);
     L.t3 = up((size_t)H * 2 * 3 * D * D * 2);
     L.cols = up((size_t)H * 2 * D * sizeof(EncCol));
+    L.wfix = up((size_t)H * 2 * ENC_MAX_WORDS * sizeof(uint32_t));
     L.total = 5 * L.f64_vec + 5 * L.f64_mat + 2 * L.i32_vec + 5 * L.f32_vec + 6 * L.f32_mat + L.tabs +
-              L.plans + L.dblob + L.dmat + L.f32_vec + L.t3 + L.cols + 1024 + 2 * L.f64_vec;
+              L.plans + L.dblob + L.dmat + L.f32_vec + L.t3 + L.cols + L.wfix + 1024 + 2 * L.f64_vec;
     return L;
 }
 
@@ -95,6 +96,7 @@ aatc_status new_handle(int Hkv, int Hq, int Bk, int Bv, aatc_dtype dtype, aatc_c
     p = (char *)(((uintptr_t)p + 1023) & ~(uintptr_t)1023);   // T3: TMA source, keep it well aligned
     h->T3 = take(L.t3);
     h->enc_cols = (EncCol *)take(L.cols);
+    h->enc_wfix = (uint32_t *)take(L.wfix);
     h->alpha = (double *)take(L.f64_vec);    // [H][2] (fits: H * 128 doubles)
     h->split = (int32_t *)take(256);
     h->status = (uint32_t *)take(256);

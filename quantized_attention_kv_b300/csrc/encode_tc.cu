@@ -23,12 +23,20 @@
 //       pack LSB-first into the record and place the words in the tiled
 //       cache layout in shared memory; full aligned blocks leave by one bulk
 //       store, other blocks by per-token stores.
+// Packing: rounding adds 1.5 * 2^23, after which the float's bit pattern is
+// 0x4B400000 + code.  That pattern, times 2^(bit position), is added into the
+// record word as it is (one integer multiply-add per code); the constant
+// parts add up to a per-word constant fixed by the bit plan (wfix), taken off
+// as the word leaves.  A code that crosses into the next word carries its
+// high part over by a high multiply (the constant's high part is in the next
+// word's wfix).
 // Every wait is bounded; a wait that gives up sets the handle's TIMEOUT bit.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "internal.h"
 #include "tc_util.h"
+#include <type_traits>
 
 namespace {
 
@@ -54,6 +62,7 @@ struct EncArgs {
     const int32_t *row_start;   // [B] first position of each row, or NULL: start_pos
     CacheMap map;               // contiguous or paged cache
     const EncCol *cols;     // [H][2][D]
+    const uint32_t *wfix;   // [H][2][ENC_MAX_WORDS]
     uint32_t *kp, *vp;
     uint32_t *status;
 };
@@ -71,6 +80,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 x max(Wk, Wv) words (tiled)
     const int Wmax = a.Wk > a.Wv ? a.Wk : a.Wv;
     EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + NGRP * EB * Wmax);  // [NGRP][D]
+    uint32_t *wfix_s = reinterpret_cast<uint32_t *>(cols_s + NGRP * D);    // [NGRP][ENC_MAX_WORDS]
     __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
@@ -179,6 +189,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
         const int gt = wq * 32 + lane;             // thread in group = token in block = lane
         const int bar_id = 1 + g;
         EncCol *cols = cols_s + g * D;
+        uint32_t *wfix = wfix_s + g * ENC_MAX_WORDS;
         uint32_t *R = Rs + g * EB * Wmax;
         int ht_cols = -1;
         for (int n = g; n < count; n += NGRP) {
@@ -188,6 +199,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             if (ht != ht_cols) {
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
                 for (int e = gt; e < D; e += 128) cols[e] = a.cols[(size_t)ht * D + e];
+                if (gt < ENC_MAX_WORDS) wfix[gt] = a.wfix[(size_t)ht * ENC_MAX_WORDS + gt];
                 asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(128));
                 ht_cols = ht;
             }
@@ -210,51 +222,60 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             // Pruned channels come last in record order with a zero range: they add no
             // bits.  A non-finite input makes every coefficient non-finite (T is dense),
             // so two coefficients per token are checked.  Eight coefficients are
-            // quantized at a time (independent chains), then ORed into the record
-            // at the bit positions the column table gives, a word leaving for the
-            // staging buffer wherever the table marks a word end.
-            auto quantize16 = [&](const uint32_t (&r)[16], int c0) {
+            // quantized at a time (independent chains; their column constants held in
+            // registers), then added into the record word, a word leaving for the
+            // staging buffer wherever the column marks a word end.
+            auto quantize16 = [&](const uint32_t (&r)[16], int c0, auto tk) {
+                constexpr int TT = decltype(tk)::value;
 #pragma unroll
                 for (int h8 = 0; h8 < 16; h8 += 8) {
+                    int4 cw[8];   // inv, off, top, mul
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) cw[q] = *reinterpret_cast<const int4 *>(&cols[c0 + h8 + q]);
                     uint32_t uq[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const EncCol col = cols[c0 + h8 + q];
                         const float c = __uint_as_float(r[h8 + q]);
-                        float v = fmaf(c, col.inv, col.off);
-                        v = fminf(fmaxf(v, 0.f), col.top);
+                        float v = fmaf(c, __int_as_float(cw[q].x), __int_as_float(cw[q].y));
+                        v = fminf(fmaxf(v, 0.f), fabsf(__int_as_float(cw[q].z)));
                         // adding 1.5 * 2^23 rounds to the nearest integer, ties to even
-                        uq[q] = __float_as_uint(v + 12582912.f) & 0xFFu;
+                        uq[q] = __float_as_uint(v + 12582912.f);
                     }
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
-                        const int pk = cols[c0 + h8 + q].pack;
-                        const uint32_t u = uq[q];
-                        lo |= __funnelshift_l(0u, u, pk);   // u << shift
-                        if (pk & ENC_WORD_END) {
-                            if (t == 0) {
+                        const uint32_t mul = (uint32_t)cw[q].w, u = uq[q];
+                        lo = u * mul + lo;
+                        if (cw[q].z < 0) {   // the word ends with this code
+                            lo -= wfix[w];
+                            if constexpr (TT == 0) {
                                 const int2 wt = wtab[w];
                                 Rk[wt.x + kb * wt.y] = lo;
                             } else {
                                 Rt16[64 * w + ii] = (uint16_t)lo;   // half-words 2w, 2w+1 of token ii
                                 Rt16[64 * w + 32 + ii] = (uint16_t)(lo >> 16);
                             }
-                            lo = __funnelshift_l(u, 0u, pk);   // u >> (32 - shift): the part past the word
+                            lo = __umulhi(u, mul);   // the part past the word
                             ++w;
                         }
                     }
                 }
             };
             // one 16-column load in flight per warp at a time (a second buffer
-            // doubles the unrolled code and costs more in instruction fetch)
+            // doubles the unrolled code and costs more in instruction fetch);
+            // the loop is compiled once for keys and once for values, so that
+            // the word placement is fixed in each
             uint32_t ra[16];
+            auto run = [&](auto tk) {
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
-                tmem_ld16(row_addr + c0, ra);
-                tmem_wait_ld(ra);
-                if (c0 == 0) fin = __uint_as_float(ra[0]) + __uint_as_float(ra[1]);
-                quantize16(ra, c0);
-            }
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    tmem_ld16(row_addr + c0, ra);
+                    tmem_wait_ld(ra);
+                    if (c0 == 0) fin = __uint_as_float(ra[0]) + __uint_as_float(ra[1]);
+                    quantize16(ra, c0, tk);
+                }
+            };
+            if (t == 0) run(std::integral_constant<int, 0>{});
+            else run(std::integral_constant<int, 1>{});
             asm volatile("tcgen05.fence::before_thread_sync;");
             __syncwarp();
             if (lane == 0) mbar_arrive(&d_empty[g]);
@@ -322,7 +343,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
 __global__ void k_enc_build(const double *__restrict__ T_k, const double *__restrict__ T_v,
                             const float *__restrict__ bk32, const float *__restrict__ bv32,
                             const CodecTables *__restrict__ tabs, const HeadPlan *__restrict__ plans,
-                            __nv_bfloat16 *__restrict__ T3, EncCol *__restrict__ cols)
+                            __nv_bfloat16 *__restrict__ T3, EncCol *__restrict__ cols, uint32_t *__restrict__ wfix)
 {
     const int h = blockIdx.x, t = blockIdx.y, n = blockIdx.z, k = threadIdx.x;
     const HeadPlan &pl = plans[h * 2 + t];
@@ -345,18 +366,33 @@ __global__ void k_enc_build(const double *__restrict__ T_k, const double *__rest
             const float bias = (t ? bv32 : bk32)[h * D + j];
             c.inv = tb.inv_step[j];
             c.off = fmaf(-bias, tb.inv_step[j], tb.mid[j]);
-            c.top = tb.top[j];
             int nb = 0;   // bit position of column n in its record word
             for (int m = 0; m < n; ++m) nb += tb.bits[pl.order[m]];
             nb &= 31;
-            c.pack = nb | ((nb + tb.bits[j] >= 32) ? ENC_WORD_END : 0);
+            c.top = (nb + tb.bits[j] >= 32) ? -tb.top[j] : tb.top[j];   // top >= 1 for a coded channel
+            c.mul = 1u << nb;
         } else {
             c.inv = 0.f;
             c.off = 0.f;
             c.top = 0.f;
-            c.pack = 0;
+            c.mul = 0u;
         }
         cols[(size_t)(h * 2 + t) * D + n] = c;
+    }
+    if (n == 0 && k < ENC_MAX_WORDS) {
+        // word k's constant: the 0x4B400000 parts of the codes that start in it,
+        // shifted to their positions (mod 2^32), plus the high parts of those
+        // that end past the word before it
+        uint32_t fix = 0;
+        int pos = 0;
+        for (int m = 0; m < pl.n_coded; ++m) {
+            const int b = tb.bits[pl.order[m]], wd = pos >> 5, sh = pos & 31;
+            const unsigned long long part = 0x4B400000ull << sh;
+            if (wd == k) fix += (uint32_t)part;
+            if (wd + 1 == k && sh + b >= 32) fix += (uint32_t)(part >> 32);
+            pos += b;
+        }
+        wfix[(h * 2 + t) * ENC_MAX_WORDS + k] = fix;
     }
 }
 
@@ -397,7 +433,11 @@ bool encode_tma(CUtensorMap *m, const void *base, unsigned long long inner, unsi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t enc_smem(int W) { return 1024 + TBYTES + ESTAGES * XBYTES + NGRP * (size_t)EB * W * 4 + NGRP * D * sizeof(EncCol); }
+size_t enc_smem(int W)
+{
+    return 1024 + TBYTES + ESTAGES * XBYTES + NGRP * (size_t)EB * W * 4 + NGRP * D * sizeof(EncCol) +
+           NGRP * ENC_MAX_WORDS * sizeof(uint32_t);
+}
 
 int sm_count_enc()
 {
@@ -423,7 +463,7 @@ bool tma_map_bf16(void *map128, const void *base, unsigned long long inner, unsi
 aatc_status enc_build(aatc_calib *h, cudaStream_t s)
 {
     k_enc_build<<<dim3(h->Hkv, 2, D), D, 0, s>>>(h->T_k, h->T_v, h->bk32, h->bv32, h->tab, h->plan,
-                                                 (__nv_bfloat16 *)h->T3, h->enc_cols);
+                                                 (__nv_bfloat16 *)h->T3, h->enc_cols, h->enc_wfix);
     AATC_CUDA(cudaGetLastError());
     CUtensorMap m;
     h->tmap_ok = encode_tma(&m, h->T3, D, (unsigned long long)h->Hkv * 2 * 3 * D);
@@ -452,6 +492,7 @@ aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int
     a.nblk = (L_new + EB - 1) / EB;
     a.n_items = h->Hkv * 2 * B * a.nblk;
     a.cols = h->enc_cols;
+    a.wfix = h->enc_wfix;
     a.kp = kp;
     a.vp = vp;
     a.status = h->status;

@@ -100,12 +100,15 @@ struct __align__(16) DecBlob {
 
 // Encoder epilogue constants of one record-order column n (channel order[n]):
 // v = c * inv + off is the quantizer input c/Delta + mid with the bias T mu
-// folded in; codes are clamp(rint(v), 0, top); past n_coded the range is zero (no bits).
+// folded in; codes are clamp(rint(v), 0, |top|); past n_coded the range is zero
+// (no bits, mul = 0).
 struct __align__(16) EncCol {
-    float inv, off, top;
-    int32_t pack;   // bit position of the code in its record word (0..31), | ENC_WORD_END if the word ends with it
+    float inv, off;
+    float top;      // largest code; stored negated when the record word ends with this column's code
+    uint32_t mul;   // 2^(bit position of the code in its record word)
 };
-constexpr int32_t ENC_WORD_END = 256;
+constexpr int ENC_MAX_WORDS = 32;   // record words per tensor at 8 bits per channel
+static_assert(ENC_MAX_WORDS * 32 >= AATC_MAXB * AATC_D, "encoder word table too small");
 
 struct aatc_calib {
     int d, Hkv, Hq, G;
@@ -142,6 +145,7 @@ struct aatc_calib {
     // epilogue columns [H][2][d]
     void *T3;
     EncCol *enc_cols;
+    uint32_t *enc_wfix;       // [H][2][ENC_MAX_WORDS] constant the encoder epilogue subtracts from each record word
     alignas(64) unsigned char tmap_T3[128];   // CUtensorMap over T3 (rows x 128 bf16)
     bool tmap_ok;
     bool fast_layout;         // every value byte holds <= AATC_PIECES pieces (key bytes: at most 8 anyway)
