@@ -14,7 +14,8 @@
 //
 // One persistent CTA per SM works through a contiguous range of (head,
 // tensor, batch row, 128-token block) items:
-//   warp 16, one thread: TMA loads (x tiles: ESTAGES = 2 stages; T: once per
+//   warp 16, one thread: TMA loads (x tiles: ES = 3 stages where shared memory
+//       allows, i.e. records of up to 12 words, else 2; T: once per
 //       head and tensor) and MMA issue into NGRP = 4 tensor-memory
 //       accumulators, item n into accumulator n % 4;
 //   warps 0-15: four epilogue groups of four warps; group g takes items
@@ -44,7 +45,6 @@ using namespace tc;
 
 constexpr int D = AATC_D;
 constexpr int EB = 128;                 // tokens per block (MMA M)
-constexpr int ESTAGES = 2;
 constexpr int NGRP = 4;                 // epilogue groups, one tensor-memory accumulator each
 constexpr int EPI = 4 * NGRP;           // epilogue warps (4 per group: one per tensor-memory lane quarter)
 constexpr int ETHREADS = (EPI + 1) * 32;
@@ -67,6 +67,10 @@ struct EncArgs {
     uint32_t *status;
 };
 
+// ES x stages: a tile's TMA load is issued when the MMAs of the item ES - 1
+// back have finished with its stage, so ES - 1 items of tensor work cover
+// the load's latency
+template <int ES>
 __global__ void __launch_bounds__(ETHREADS, 1)
     k_encode_tc(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxv,
                 const __grid_constant__ CUtensorMap mt, EncArgs a)
@@ -76,12 +80,12 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     // every access through it compiles to a shared-memory instruction
     unsigned char *sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
     unsigned char *Ts = sm;                              // 3 splits x 2 k-halves x 16 KB
-    unsigned char *Xs = Ts + TBYTES;                     // ESTAGES x 32 KB
-    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ESTAGES * XBYTES);   // NGRP x 128 x max(Wk, Wv) words (tiled)
+    unsigned char *Xs = Ts + TBYTES;                     // ES x 32 KB
+    uint32_t *Rs = reinterpret_cast<uint32_t *>(Xs + ES * XBYTES);   // NGRP x 128 x max(Wk, Wv) words (tiled)
     const int Wmax = a.Wk > a.Wv ? a.Wk : a.Wv;
     EncCol *cols_s = reinterpret_cast<EncCol *>(Rs + NGRP * EB * Wmax);  // [NGRP][D]
     uint32_t *wfix_s = reinterpret_cast<uint32_t *>(cols_s + NGRP * D);    // [NGRP][ENC_MAX_WORDS]
-    __shared__ __align__(8) uint64_t x_full[ESTAGES], x_empty[ESTAGES], t_full, mma_done[NGRP], d_empty[NGRP];
+    __shared__ __align__(8) uint64_t x_full[ES], x_empty[ES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
     __shared__ int2 wtab[16];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
@@ -100,7 +104,7 @@ __global__ void __launch_bounds__(ETHREADS, 1)
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == EPI * 32) {
-        for (int s = 0; s < ESTAGES; ++s) {
+        for (int s = 0; s < ES; ++s) {
             mbar_init(&x_full[s], 1);
             mbar_init(&x_empty[s], 1);
         }
@@ -125,19 +129,19 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     if (warp == EPI) {
         if (lane == 0 && count > 0) {
             // ------------------------------------------------ producer + MMA issue
-            // item n: x stage n % ESTAGES, accumulator (and epilogue group) n % NGRP
+            // item n: x stage n % ES, accumulator (and epilogue group) n % NGRP
             auto issue_x = [&](int n) {
                 const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
                 const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
                 const int row = (b * a.H + h) * a.L_new + blk * EB;
                 const CUtensorMap *map = t ? &mxv : &mxk;
-                const int s = n % ESTAGES;
+                const int s = n % ES;
                 mbar_expect(&x_full[s], XBYTES);
                 tma2d(Xs + s * XBYTES, map, 0, row, &x_full[s]);
                 tma2d(Xs + s * XBYTES + XBYTES / 2, map, 64, row, &x_full[s]);
             };
             bool ok = true;
-            for (int n = 0; n < ESTAGES && n < count; ++n) issue_x(n);
+            for (int n = 0; n < ES && n < count; ++n) issue_x(n);
             int ht_loaded = -1, t_uses = 0;
             for (int n = 0; n < count && ok; ++n) {
                 const int item = i0 + n, ht = item / per_ht;
@@ -153,8 +157,8 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                     ++t_uses;
                     ht_loaded = ht;
                 }
-                const int s = n % ESTAGES, g = n % NGRP;
-                ok = ok && mbar_wait1(&x_full[s], (uint32_t)((n / ESTAGES) & 1));
+                const int s = n % ES, g = n % NGRP;
+                ok = ok && mbar_wait1(&x_full[s], (uint32_t)((n / ES) & 1));
                 // the accumulator is free once its group read the item NGRP back
                 if (n >= NGRP) ok = ok && mbar_wait1(&d_empty[g], (uint32_t)(((n / NGRP) - 1) & 1));
                 if (!ok) break;
@@ -172,10 +176,10 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                 mma_commit(&mma_done[g]);
                 mma_commit(&x_empty[s]);
                 // refill the stage the previous item used
-                if (n >= 1 && n - 1 + ESTAGES < count) {
-                    const int sp = (n - 1) % ESTAGES;
-                    ok = ok && mbar_wait1(&x_empty[sp], (uint32_t)(((n - 1) / ESTAGES) & 1));
-                    if (ok) issue_x(n - 1 + ESTAGES);
+                if (n >= 1 && n - 1 + ES < count) {
+                    const int sp = (n - 1) % ES;
+                    ok = ok && mbar_wait1(&x_empty[sp], (uint32_t)(((n - 1) / ES) & 1));
+                    if (ok) issue_x(n - 1 + ES);
                 }
             }
             if (!ok) {
@@ -433,10 +437,24 @@ bool encode_tma(CUtensorMap *m, const void *base, unsigned long long inner, unsi
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t enc_smem(int W)
+size_t enc_smem(int W, int es)
 {
-    return 1024 + TBYTES + ESTAGES * XBYTES + NGRP * (size_t)EB * W * 4 + NGRP * D * sizeof(EncCol) +
+    return 1024 + TBYTES + es * XBYTES + NGRP * (size_t)EB * W * 4 + NGRP * D * sizeof(EncCol) +
            NGRP * ENC_MAX_WORDS * sizeof(uint32_t);
+}
+
+// largest dynamic shared memory a CTA of this device may opt into
+int smem_optin_enc()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        n = (cudaGetDevice(&dev) == cudaSuccess &&
+             cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess && v > 0)
+                ? v
+                : 232448;
+    }
+    return n;
 }
 
 int sm_count_enc()
@@ -496,12 +514,20 @@ aatc_status encode_tc_run(const aatc_calib *h, const void *k, const void *v, int
     a.kp = kp;
     a.vp = vp;
     a.status = h->status;
-    const size_t smem = enc_smem(h->Wk > h->Wv ? h->Wk : h->Wv);
-    aatc_status st = kernel_smem_limit((const void *)k_encode_tc, smem);
+    // three x stages when they fit beside the staging buffers (1 KB left for the
+    // kernel's static shared variables), else two
+    const int W = h->Wk > h->Wv ? h->Wk : h->Wv;
+    const bool three = enc_smem(W, 3) + 1024 <= (size_t)smem_optin_enc();
+    const size_t smem = enc_smem(W, three ? 3 : 2);
+    const void *kern = three ? (const void *)k_encode_tc<3> : (const void *)k_encode_tc<2>;
+    aatc_status st = kernel_smem_limit(kern, smem);
     if (st != AATC_OK) return st;
     int grid = sm_count_enc();
     if (grid > a.n_items) grid = a.n_items;
-    k_encode_tc<<<grid, ETHREADS, smem, s>>>(mk, mv, mt, a);
+    if (three)
+        k_encode_tc<3><<<grid, ETHREADS, smem, s>>>(mk, mv, mt, a);
+    else
+        k_encode_tc<2><<<grid, ETHREADS, smem, s>>>(mk, mv, mt, a);
     AATC_CUDA(cudaGetLastError());
     return AATC_OK;
 }
