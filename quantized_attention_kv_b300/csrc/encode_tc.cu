@@ -14,10 +14,12 @@
 //
 // One persistent CTA per SM works through a contiguous range of (head,
 // tensor, batch row, 128-token block) items:
-//   warp 16, one thread: TMA loads (x tiles: ES = 3 stages where shared memory
-//       allows, i.e. records of up to 12 words, else 2; T: once per
-//       head and tensor) and MMA issue into NGRP = 4 tensor-memory
-//       accumulators, item n into accumulator n % 4;
+//   warp 17, one thread: TMA loads of the x tiles (ES = 3 stages where shared
+//       memory allows, i.e. records of up to 12 words, else 2), each stage
+//       refilled as soon as the MMAs of its previous item are done with it;
+//   warp 16, one thread: TMA loads of T (once per head and tensor) and MMA
+//       issue into NGRP = 4 tensor-memory accumulators, item n into
+//       accumulator n % 4;
 //   warps 0-15: four epilogue groups of four warps; group g takes items
 //       g, g + 4, ..., thread = token = tensor-memory lane: read the 128
 //       accumulators, quantize (v = c inv + off, clamp, round half to even),
@@ -47,7 +49,7 @@ constexpr int D = AATC_D;
 constexpr int EB = 128;                 // tokens per block (MMA M)
 constexpr int NGRP = 4;                 // epilogue groups, one tensor-memory accumulator each
 constexpr int EPI = 4 * NGRP;           // epilogue warps (4 per group: one per tensor-memory lane quarter)
-constexpr int ETHREADS = (EPI + 1) * 32;
+constexpr int ETHREADS = (EPI + 2) * 32;   // + MMA warp + TMA warp
 constexpr uint32_t XBYTES = EB * D * 2; // 32 KB per x tile
 constexpr uint32_t TBYTES = 3 * D * D * 2;
 
@@ -67,9 +69,9 @@ struct EncArgs {
     uint32_t *status;
 };
 
-// ES x stages: a tile's TMA load is issued when the MMAs of the item ES - 1
-// back have finished with its stage, so ES - 1 items of tensor work cover
-// the load's latency
+// ES x stages: a tile's TMA load is issued as soon as the MMAs of the item ES
+// back have finished with its stage, so about ES - 1 items of tensor work
+// cover the load's latency
 template <int ES>
 __global__ void __launch_bounds__(ETHREADS, 1)
     k_encode_tc(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxv,
@@ -126,22 +128,33 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     const int i1 = (int)((long long)(blockIdx.x + 1) * a.n_items / gridDim.x);
     const int count = i1 - i0;
 
-    if (warp == EPI) {
+    if (warp == EPI + 1) {
         if (lane == 0 && count > 0) {
-            // ------------------------------------------------ producer + MMA issue
-            // item n: x stage n % ES, accumulator (and epilogue group) n % NGRP
-            auto issue_x = [&](int n) {
-                const int item = i0 + n, ht = item / per_ht, rem = item % per_ht;
+            // ------------------------------------------------ x-tile loads
+            // item m goes into stage m % ES once the MMAs of item m - ES are done with it
+            bool ok = true;
+            for (int m = 0; m < count && ok; ++m) {
+                const int s = m % ES;
+                if (m >= ES) ok = mbar_wait1(&x_empty[s], (uint32_t)((m / ES - 1) & 1));
+                if (!ok || *(volatile int *)&s_fail) break;
+                const int item = i0 + m, ht = item / per_ht, rem = item % per_ht;
                 const int b = rem / a.nblk, blk = rem % a.nblk, h = ht >> 1, t = ht & 1;
                 const int row = (b * a.H + h) * a.L_new + blk * EB;
                 const CUtensorMap *map = t ? &mxv : &mxk;
-                const int s = n % ES;
                 mbar_expect(&x_full[s], XBYTES);
                 tma2d(Xs + s * XBYTES, map, 0, row, &x_full[s]);
                 tma2d(Xs + s * XBYTES + XBYTES / 2, map, 64, row, &x_full[s]);
-            };
+            }
+            if (!ok) {
+                atomicOr(a.status, AATC_DEV_TIMEOUT);
+                s_fail = 1;
+            }
+        }
+    } else if (warp == EPI) {
+        if (lane == 0 && count > 0) {
+            // ------------------------------------------------ T loads + MMA issue
+            // item n: x stage n % ES, accumulator (and epilogue group) n % NGRP
             bool ok = true;
-            for (int n = 0; n < ES && n < count; ++n) issue_x(n);
             int ht_loaded = -1, t_uses = 0;
             for (int n = 0; n < count && ok; ++n) {
                 const int item = i0 + n, ht = item / per_ht;
@@ -175,19 +188,13 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                     }
                 mma_commit(&mma_done[g]);
                 mma_commit(&x_empty[s]);
-                // refill the stage the previous item used
-                if (n >= 1 && n - 1 + ES < count) {
-                    const int sp = (n - 1) % ES;
-                    ok = ok && mbar_wait1(&x_empty[sp], (uint32_t)(((n - 1) / ES) & 1));
-                    if (ok) issue_x(n - 1 + ES);
-                }
             }
             if (!ok) {
                 atomicOr(a.status, AATC_DEV_TIMEOUT);
                 s_fail = 1;
             }
         }
-    } else {
+    } else if (warp < EPI) {
         // ---------------------------------------------------- epilogue groups
         const int g = warp >> 2, wq = warp & 3;   // group, tensor-memory lane quarter
         const int gt = wq * 32 + lane;             // thread in group = token in block = lane
