@@ -90,13 +90,13 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     __shared__ __align__(8) uint64_t x_full[ES], x_empty[ES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
-    __shared__ int2 wtab[16];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
+    __shared__ int2 wtab[ENC_MAX_WORDS];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // a dependent decode launch may start its prologue (it waits for this grid
     // before reading the cache)
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < 16) {
+    if (tid < ENC_MAX_WORDS) {
         const int r = tid >> 2, nr = min(4, a.Wk - 4 * r);   // key records only
         wtab[tid] = make_int2(64 * r + 2 * (tid - 4 * r), 2 * nr);
     }

@@ -163,6 +163,33 @@ def test_encode_bf16_tensor_core_path(L_new, start, L_cap, B):
     g.check()
 
 
+_bf16_wide = {}
+
+
+@pytest.mark.parametrize("bits", [5.0, 8.0])
+@pytest.mark.parametrize("L_new,start,L_cap,B", [(1024, 0, 1024, 2), (1000, 24, 1056, 1)])
+def test_encode_bf16_tensor_core_wide_records(bits, L_new, start, L_cap, B):
+    """The tensor-core encoder with records of 20 and 32 words: key words past
+    the 16th in the tiled layout, and the two-stage instance (records above 12
+    words)."""
+    if bits not in _bf16_wide:
+        wl = synth.dataclasses.replace(WL["llama_32k"], n_kv_heads=2, n_q_heads=8)
+        k, v, q = synth.calib_inputs(wl, device="cuda")
+        _bf16_wide[bits] = (wl, _oracle_cal(k, v, q, bits))
+    wl, ocal = _bf16_wide[bits]
+    W = ocal["W"]
+    assert W == int(bits * 4)
+    g = aatc.import_calib(ocal, wl.n_q_heads, wl.dtype)
+    kc, vc = synth.cache_inputs(wl, device="cuda", seq_len=L_new, batch=B)
+    kp = torch.full((B, 2, L_cap, W), -1, dtype=torch.int32, device="cuda")
+    vp = kp.clone()
+    aatc.encode(g, kc, vc, kp, vp, start_pos=start)
+    torch.cuda.synchronize()
+    _check_written(kp, kc, ocal, "k", oracle.KEYS, start, 2)
+    _check_written(vp, vc, ocal, "v", oracle.VALUES, start, 2)
+    g.check()
+
+
 def _check_written(p, x, ocal, t, kind, start, heads):
     """Codes of the written tokens vs the oracle (rounding-tie rule), and every
     bit of every other token untouched (the cache started as all ones)."""
