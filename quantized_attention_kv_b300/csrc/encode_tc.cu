@@ -90,16 +90,11 @@ __global__ void __launch_bounds__(ETHREADS, 1)
     __shared__ __align__(8) uint64_t x_full[ES], x_empty[ES], t_full, mma_done[NGRP], d_empty[NGRP];
     __shared__ uint32_t tmem_base;
     __shared__ int s_fail;
-    __shared__ int2 wtab[ENC_MAX_WORDS];   // key record word w: tile offset 64 r + 2 (w - 4 r) and 2 n_r, r = w / 4
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // a dependent decode launch may start its prologue (it waits for this grid
     // before reading the cache)
     asm volatile("griddepcontrol.launch_dependents;");
-    if (tid < ENC_MAX_WORDS) {
-        const int r = tid >> 2, nr = min(4, a.Wk - 4 * r);   // key records only
-        wtab[tid] = make_int2(64 * r + 2 * (tid - 4 * r), 2 * nr);
-    }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
                      "r"(NGRP * D));
@@ -223,7 +218,8 @@ __global__ void __launch_bounds__(ETHREADS, 1)
             const int tl = gt >> 5, ii = gt & 31;
             uint32_t *Rt = R + tl * 32 * W;
             uint16_t *Rt16 = reinterpret_cast<uint16_t *>(Rt);
-            // key word w of token ii sits at ka + wtab[w].x + kb * wtab[w].y (the tiled layout)
+            // key word w of token ii sits at Rk + 64 r + 2 (w - 4 r) + kb 2 n_r, r = w / 4 and
+            // n_r = min(4, W - 4 r) the words of row group r (the tiled layout)
             uint32_t *Rk = Rt + 16 * W * (ii >> 4) + (ii & 1);
             const int kb = (ii & 15) >> 1;
             float fin = 0.f;
@@ -259,8 +255,8 @@ __global__ void __launch_bounds__(ETHREADS, 1)
                         if (cw[q].z < 0) {   // the word ends with this code
                             lo -= wfix[w];
                             if constexpr (TT == 0) {
-                                const int2 wt = wtab[w];
-                                Rk[wt.x + kb * wt.y] = lo;
+                                const int r4 = w >> 2;
+                                Rk[56 * r4 + 2 * w + kb * 2 * min(4, a.Wk - 4 * r4)] = lo;
                             } else {
                                 Rt16[64 * w + ii] = (uint16_t)lo;   // half-words 2w, 2w+1 of token ii
                                 Rt16[64 * w + 32 + ii] = (uint16_t)(lo >> 16);
